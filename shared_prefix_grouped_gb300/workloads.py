@@ -1,0 +1,151 @@
+"""Seeded synthetic workloads for grouped attention over packed [P; R1; ...; RG] sequences.
+
+This module only draws numbers: suffix lengths and the Q/K/V/dO tensors, in the shapes and
+distributions of the long-prefix GRPO workloads the Prefix Grouper pages describe (abstract page:
+long shared prefixes; skill page "prefix-grouper-grpo", Practical Guidance: prefix much longer than
+the responses, G typically 4-8).  It holds none of the method's arithmetic, so the CUDA path and the
+CPU oracle can both take their inputs from here without sharing any computation.
+
+Every draw uses a CPU ``torch.Generator`` seeded from the workload, in fp32, then a cast to the
+workload's dtype (round-to-nearest-even for bf16).  Order of draws: suffix lengths, Q, K, V, dO.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import List, Optional
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One grouped-attention problem: B groups, each a shared prefix followed by G suffixes."""
+
+    name: str
+    dtype: str                       # "f32" or "bf16"
+    num_groups: int                  # B
+    group_size: int                  # G (suffixes per group)
+    prefix_len: int                  # Lp (same for every group of a workload)
+    heads_q: int                     # Hq
+    heads_kv: int                    # Hkv (Hq % Hkv == 0; q-head h uses kv-head h // (Hq // Hkv))
+    head_dim: int                    # d
+    suffix_lens: Optional[tuple] = None   # fixed lengths (len B*G), or None to draw them
+    suffix_range: Optional[tuple] = None  # (lo, hi) inclusive range for uniform draws
+    rope_theta: float = 0.0          # 0 disables RoPE
+    input_scale: float = 1.0         # Q, K, V are N(0,1) * input_scale; dO is N(0,1)
+    seed: int = 1000
+
+
+# The five workloads: index 0 is the small fp32 case, 1..3 the bf16 attention cases, and the
+# decoder-layer workload (index 4) is described by LayerWorkload below.
+WORKLOADS: List[Workload] = [
+    Workload("fp32_h2_d64_p256_g4", "f32", 1, 4, 256, 2, 2, 64,
+             suffix_lens=(32, 48, 64, 16), rope_theta=0.0, seed=1000),
+    Workload("bf16_mha_h32_d128_p4096_g8_r512", "bf16", 1, 8, 4096, 32, 32, 128,
+             suffix_lens=(512,) * 8, rope_theta=1e4, input_scale=128 ** -0.5, seed=1001),
+    Workload("bf16_gqa32x8_d128_b8_p2048_g16_r64-512", "bf16", 8, 16, 2048, 32, 8, 128,
+             suffix_range=(64, 512), rope_theta=1e4, seed=1002),
+    Workload("bf16_gqa32x8_d128_p16384_g16_r256-1024", "bf16", 1, 16, 16384, 32, 8, 128,
+             suffix_range=(256, 1024), rope_theta=5e5, seed=1003),
+]
+
+
+@dataclasses.dataclass(frozen=True)
+class LayerWorkload:
+    """One Llama-style decoder layer over packed groups (random-init weights N(0, 0.02))."""
+
+    name: str = "llama_layer_h4096_gqa32x8_mlp14336_b2_p8192_g8_r1024"
+    hidden: int = 4096
+    heads_q: int = 32
+    heads_kv: int = 8
+    head_dim: int = 128
+    mlp: int = 14336
+    num_groups: int = 2
+    group_size: int = 8
+    prefix_len: int = 8192
+    suffix_len: int = 1024
+    rope_theta: float = 5e5
+    rms_eps: float = 1e-5
+    weight_std: float = 0.02
+    seed: int = 1004
+
+
+def by_name(name: str) -> Workload:
+    for w in WORKLOADS:
+        if w.name == name:
+            return w
+    raise KeyError(name)
+
+
+def torch_dtype(dtype: str) -> torch.dtype:
+    return {"f32": torch.float32, "bf16": torch.bfloat16}[dtype]
+
+
+def draw_suffix_lens(w: Workload, gen: torch.Generator) -> List[int]:
+    """Suffix lengths for all B*G responses, group-major."""
+    n = w.num_groups * w.group_size
+    if w.suffix_lens is not None:
+        assert len(w.suffix_lens) == n
+        return [int(x) for x in w.suffix_lens]
+    lo, hi = w.suffix_range
+    return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=gen)]
+
+
+@dataclasses.dataclass
+class Problem:
+    """Host tensors of one drawn workload, in the packed token order."""
+
+    workload: Workload
+    prefix_lens: List[int]           # per group
+    group_sizes: List[int]           # per group
+    suffix_lens: List[int]           # per response, group-major
+    q: torch.Tensor                  # [T, Hq, d]
+    k: torch.Tensor                  # [T, Hkv, d]
+    v: torch.Tensor                  # [T, Hkv, d]
+    do: torch.Tensor                 # [T, Hq, d]
+
+    @property
+    def total_tokens(self) -> int:
+        return sum(self.prefix_lens) + sum(self.suffix_lens)
+
+
+def make_problem(w: Workload, *, suffix_lens: Optional[List[int]] = None,
+                 prefix_lens: Optional[List[int]] = None,
+                 group_sizes: Optional[List[int]] = None,
+                 seed: Optional[int] = None) -> Problem:
+    """Draw a problem.  Lengths may be overridden (edge cases); values are always drawn."""
+    gen = torch.Generator().manual_seed(w.seed if seed is None else seed)
+    drawn = draw_suffix_lens(w, gen)
+    if suffix_lens is None:
+        suffix_lens = drawn
+    if group_sizes is None:
+        group_sizes = [w.group_size] * w.num_groups
+    if prefix_lens is None:
+        prefix_lens = [w.prefix_len] * len(group_sizes)
+    assert len(suffix_lens) == sum(group_sizes) and len(prefix_lens) == len(group_sizes)
+    T = sum(prefix_lens) + sum(suffix_lens)
+    dt = torch_dtype(w.dtype)
+
+    def draw(heads, scale):
+        x = torch.randn((T, heads, w.head_dim), generator=gen, dtype=torch.float32)
+        if scale != 1.0:
+            x = x * scale
+        return x.to(dt)
+
+    q = draw(w.heads_q, w.input_scale)
+    k = draw(w.heads_kv, w.input_scale)
+    v = draw(w.heads_kv, w.input_scale)
+    do = draw(w.heads_q, 1.0)
+    return Problem(w, list(prefix_lens), list(group_sizes), list(suffix_lens), q, k, v, do)
+
+
+def small_variant(w: Workload, *, prefix_len: int, suffix_lens: List[int], num_groups: int = 1,
+                  heads_q: Optional[int] = None, heads_kv: Optional[int] = None,
+                  seed: Optional[int] = None) -> Workload:
+    """The same dtype/head_dim/RoPE recipe at a size the oracle finishes in seconds."""
+    g = len(suffix_lens) // num_groups
+    return dataclasses.replace(
+        w, name=w.name + "_small", num_groups=num_groups, group_size=g, prefix_len=prefix_len,
+        suffix_lens=tuple(suffix_lens), suffix_range=None,
+        heads_q=heads_q or w.heads_q, heads_kv=heads_kv or w.heads_kv,
+        seed=w.seed if seed is None else seed)
