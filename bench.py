@@ -1,0 +1,447 @@
+"""Benchmark: grouped-attention forward + backward on one GB300 (or N, one process per GPU).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one pass of the whole hot path over one batch: packing is done once (it is input
+construction), then every step runs pg_grouped_attn_fwd (RoPE + attention) and
+pg_grouped_attn_bwd (RoPE, preprocess, dK/dV with the cross-response prefix reduction, dQ,
+inverse RoPE) through the C ABI, on inputs already resident in HBM.  The metric is counted
+grouped-attention TFLOP/s (14 * d * visible pairs * Hq per step), with tokens/s and the fraction of
+the BF16 tensor peak beside it.  With N > 1 every rank runs its own independent batch (groups are
+independent problems: weak scaling, no collective on the data path).
+
+--impl reference times the CPU oracle (the repeated-prefix baseline, fp64) on bounded samples of
+the same workload on the host cores; it prints one line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from shared_prefix_grouped_gb300 import _lib, api, flops, workloads  # noqa: E402
+
+METRIC = "grouped-attn fwd+bwd TFLOP/s, tokens/s & % BF16 peak vs repeated-prefix (1 GB300)"
+DEFAULT_WORKLOAD = workloads.WORKLOADS[1].name
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+L2_BYTES = 129 * 2 ** 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            data = json.load(open(path))
+            flat = {}
+
+            def walk(d):
+                for k, v in d.items():
+                    if isinstance(v, dict):
+                        walk(v)
+                    elif isinstance(v, (int, float)):
+                        flat.setdefault(k, float(v))
+            walk(data)
+            if "bf16_tflops" in flat:
+                return flat, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed region runs."""
+
+    QUERY = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.device = device
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        bus = None
+        try:
+            bus = torch.cuda.get_device_properties(self.device).pci_bus_id
+        except Exception:
+            pass
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        if bus is not None:
+            mine = [r for r in rows if r[1].lower().endswith(str(bus).lower()[-12:])]
+            rows = mine or rows
+        elif len({r[0] for r in rows}) > 1:
+            rows = [r for r in rows if r[0] == str(self.device)] or rows
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[2]) for r in rows if num(r[2]) is not None]
+        mx = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[6:10]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world, device):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(device)
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload_config(w, prob, l2_note):
+    return {"workload": w.name, "groups": w.num_groups, "responses_per_group": w.group_size,
+            "prefix_len": w.prefix_len, "suffix_lens": "fixed" if w.suffix_lens else
+            f"uniform[{w.suffix_range[0]},{w.suffix_range[1]}] seed {w.seed}",
+            "total_tokens": prob.total_tokens, "heads_q": w.heads_q, "heads_kv": w.heads_kv,
+            "head_dim": w.head_dim, "rope_theta": w.rope_theta, "l2": l2_note}
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle sample (cpu_baseline leg and the reference arm)
+# ------------------------------------------------------------------------------------------------
+
+def oracle_sample(prob, head: int, n_resp: int):
+    """Run the oracle on q-head `head`, group 0, its prefix and first n_resp responses.
+    Returns (seconds, counted FLOPs of that grouped sample)."""
+    from oracle import prefix_grouper_oracle as orc
+    w = prob.workload
+    lp = prob.prefix_lens[0]
+    rs = prob.suffix_lens[:prob.group_sizes[0]][:n_resp]
+    T = lp + sum(rs)
+    # the sample is the group's first T packed rows (prefix, then responses in order)
+    lay = orc.pack_layout([lp], [len(rs)], rs)
+    sl = slice(0, T)
+    kh = head // (w.heads_q // w.heads_kv)
+    q = prob.q[sl, head:head + 1]
+    k = prob.k[sl, kh:kh + 1]
+    v = prob.v[sl, kh:kh + 1]
+    do = prob.do[sl, head:head + 1]
+    t0 = time.perf_counter()
+    orc.repeated_prefix(lay, q, k, v, do, theta=w.rope_theta, check_prefix_copies=False)
+    dt = time.perf_counter() - t0
+    fl = flops.attn_flops(flops.group_pairs(lp, rs), 1, w.head_dim, "fwdbwd")
+    return dt, fl
+
+
+def cpu_baseline_leg(prob, budget_s=12.0, max_s=30.0):
+    w = prob.workload
+    G = prob.group_sizes[0]
+    total_t, total_f, heads = 0.0, 0.0, 0
+    for h in range(w.heads_q):
+        dt, fl = oracle_sample(prob, h, G)
+        total_t += dt
+        total_f += fl
+        heads += 1
+        if total_t >= budget_s or total_t + dt > max_s:
+            break
+    return {"value": total_f / total_t / 1e12, "unit": "TFLOP/s", "cores": torch.get_num_threads(),
+            "kind": "oracle",
+            "sample": f"group 0, all {G} responses, {heads} of {w.heads_q} query heads, "
+                      f"fp64 repeated-prefix forward+backward, {total_t:.1f} s"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    w = workloads.by_name(args.workload)
+    prob = workloads.make_problem(w)
+    G = prob.group_sizes[0]
+    per_step_budget = max(1.0, 150.0 / (args.steps + args.warmup))
+    dt, _ = oracle_sample(prob, 0, 1)
+    n_resp = G
+    if dt * G > per_step_budget:
+        n_resp = max(1, int(per_step_budget / dt))
+    times, fls = [], []
+    for i in range(args.warmup + args.steps):
+        dt, fl = oracle_sample(prob, i % w.heads_q, n_resp)
+        if i >= args.warmup:
+            times.append(dt)
+            fls.append(fl)
+    sec = sum(times) / len(times)
+    value = sum(fls) / sum(times) / 1e12
+    sample = (f"per step: group 0, prefix + {n_resp} of {G} responses, one query head "
+              f"(cycling), fp64 repeated-prefix forward+backward")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, prob, "CPU run"),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": torch.get_num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# ------------------------------------------------------------------------------------------------
+# Our arm
+# ------------------------------------------------------------------------------------------------
+
+class Step:
+    """Buffers and calls of one fwd+bwd step through the C ABI."""
+
+    def __init__(self, prob, device, flags=0):
+        w = prob.workload
+        self.w, self.flags, self.device = w, flags, device
+        self.layout = api.pack(prob.prefix_lens, prob.group_sizes, prob.suffix_lens, device)
+        self.q, self.k, self.v, self.do = (t.to(device) for t in (prob.q, prob.k, prob.v, prob.do))
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty((w.heads_q, prob.total_tokens), dtype=torch.float32, device=device)
+        self.dq, self.dk, self.dv = (torch.empty_like(t) for t in (self.q, self.k, self.v))
+        opts = api.make_opts(w.rope_theta, 0.0, flags)
+        self.ws_f = api._workspace(api.workspace_size(self.layout, self.q.dtype, w.heads_q,
+                                                      w.heads_kv, w.head_dim, opts, 0), device)
+        self.ws_b = api._workspace(api.workspace_size(self.layout, self.q.dtype, w.heads_q,
+                                                      w.heads_kv, w.head_dim, opts, 1), device)
+
+    def __call__(self):
+        w = self.w
+        api.grouped_attn_fwd(self.layout, self.q, self.k, self.v, rope_theta=w.rope_theta,
+                             flags=self.flags, out=self.o, lse=self.lse, workspace=self.ws_f)
+        api.grouped_attn_bwd(self.layout, self.q, self.k, self.v, self.o, self.lse, self.do,
+                             rope_theta=w.rope_theta, flags=self.flags, dq=self.dq, dk=self.dk,
+                             dv=self.dv, workspace=self.ws_b)
+
+
+def time_steps(step, n, device):
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    s.record()
+    for _ in range(n):
+        step()
+    e.record()
+    torch.cuda.synchronize(device)
+    return s.elapsed_time(e) / 1e3 / n
+
+
+def run_ours(args):
+    world, rank, local = dist_setup()
+    device = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(device)
+    w = workloads.by_name(args.workload)
+    prob = workloads.make_problem(w, seed=w.seed + rank)   # independent batch per rank
+    flags = _lib.PG_FLAG_SIMT if args.simt else 0
+    step = Step(prob, device, flags)
+    pairs = step.layout.pairs
+    step_flops = flops.attn_flops(pairs, w.heads_q, w.head_dim, "fwdbwd")
+    in_bytes = sum(t.numel() * t.element_size() for t in (step.q, step.k, step.v, step.do))
+    l2_note = (f"inputs larger than L2 (q,k,v,dO = {in_bytes / 2**20:.0f} MiB > 129 MiB L2)"
+               if in_bytes > L2_BYTES else "L2 flushed between steps")
+    flush = None if in_bytes > L2_BYTES else torch.empty(2 * L2_BYTES, dtype=torch.uint8,
+                                                         device=device)
+
+    def one():
+        if flush is not None:
+            flush.zero_()
+        step()
+
+    for _ in range(args.warmup):
+        one()
+    torch.cuda.synchronize(device)
+
+    # ---- timed region: K steps, per-launch events around the dominant kernel -----------------
+    L = _lib.lib()
+    dom_kernel = _lib.PG_KERNEL_BWD_DKDV
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for a, b in ev:       # create the CUDA events
+        a.record()
+        b.record()
+    prof = _lib.PgProfile(dom_kernel, 0, None, None, 0)
+    sampler = ClockSampler(device.index)
+    sampler.start()
+    barrier(world, device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    L.pg_set_profile(prof)
+    for i in range(args.steps):
+        prof.ev_begin = ev[i][0].cuda_event
+        prof.ev_end = ev[i][1].cuda_event
+        one()
+    L.pg_set_profile(None)
+    end.record()
+    barrier(world, device)
+    clocks = sampler.stop()
+    sec = start.elapsed_time(end) / 1e3 / args.steps
+    sec = max_over_ranks(sec, world, device)
+    dom_sec = sum(a.elapsed_time(b) for a, b in ev) / 1e3 / args.steps
+    assert api.device_status() == 0, "a kernel reported an error"
+
+    peaks, peak_src = load_peaks()
+    value = step_flops * world / sec / 1e12
+    dom_flops = flops.attn_flops(pairs, w.heads_q, w.head_dim, "bwd")
+    peak = peaks["bf16_tflops"]
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic (seeded N(0,1) Q/K/V/dO; no dataset)",
+            "config": workload_config(w, prob, l2_note),
+            "tokens_per_s": prob.total_tokens * world / sec,
+            "pct_bf16_peak": 100.0 * value / world / peak,
+            "peak_source": peak_src,
+            "roofline": {"bound": "tensor", "kernel": "bwd dK/dV (+dQ)",
+                         "achieved": dom_flops / dom_sec / 1e12, "peak": peak,
+                         "unit": "TFLOP/s", "frac": dom_flops / dom_sec / 1e12 / peak,
+                         "traffic": None, "peak_source": f"bf16 dense burst, {peak_src}"},
+            "clocks": clocks, "gpu_launches": int(prof.launches)}
+    if rank == 0 and not args.skip_extras:
+        line["e2e"] = e2e_leg(step, prob, device, args, step_flops, world)
+        line["repeated_prefix"] = repeated_leg(prob, device, flags, sec, args)
+        if world == 1:
+            line["cpu_baseline"] = cpu_baseline_leg(prob)
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def e2e_leg(step, prob, device, args, step_flops, world):
+    """Same metric through the public API with host buffers: pinned H2D of q,k,v,dO, fwd+bwd,
+    D2H of o, dq, dk, dv, every step."""
+    host_in = [t.pin_memory() for t in (prob.q, prob.k, prob.v, prob.do)]
+    host_out = [torch.empty_like(t, device="cpu").pin_memory()
+                for t in (step.o, step.dq, step.dk, step.dv)]
+    dev_in = [step.q, step.k, step.v, step.do]
+
+    def e2e():
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        step()
+        for h, d in zip(host_out, (step.o, step.dq, step.dk, step.dv)):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e()
+    sec = time_steps(e2e, args.steps, device)
+    sec = max_over_ranks(sec, world, device)
+    return {"value": step_flops * world / sec / 1e12, "unit": "TFLOP/s",
+            "ms_per_step": sec * 1e3,
+            "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in),
+            "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out)}
+
+
+def repeated_leg(prob, device, flags, grouped_sec, args):
+    """The same attention as the repeated-prefix baseline on this GPU: every [P; Ri] materialised
+    as its own sequence and run through the same kernels."""
+    w = prob.workload
+    lps, gss, rss, idx = [], [], [], []
+    s = 0
+    g0 = 0
+    for b, (lp, G) in enumerate(zip(prob.prefix_lens, prob.group_sizes)):
+        seg0 = g0 + lp
+        for i in range(G):
+            r = prob.suffix_lens[s + i]
+            lps.append(lp)
+            gss.append(1)
+            rss.append(r)
+            idx.append(torch.arange(g0, g0 + lp))
+            idx.append(torch.arange(seg0, seg0 + r))
+            seg0 += r
+        g0 = seg0
+        s += G
+    idx = torch.cat(idx)
+    rep = workloads.Problem(w, lps, gss, rss, prob.q[idx], prob.k[idx], prob.v[idx], prob.do[idx])
+    try:
+        rstep = Step(rep, device, flags)
+    except torch.cuda.OutOfMemoryError:
+        return {"skipped": "out of memory"}
+    for _ in range(2):
+        rstep()
+    n = max(3, min(args.steps, 10))
+    sec = time_steps(rstep, n, device)
+    rep_pairs = rstep.layout.pairs
+    del rstep
+    torch.cuda.empty_cache()
+    return {"ms_per_step": sec * 1e3, "tokens": rep.total_tokens,
+            "counted_tflops": flops.attn_flops(rep_pairs, w.heads_q, w.head_dim) / sec / 1e12,
+            "speedup_grouped_vs_repeated": sec / grouped_sec,
+            "pair_ratio_grouped_over_repeated":
+                flops.total_pairs(prob.prefix_lens, prob.group_sizes, prob.suffix_lens) / rep_pairs}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=[w.name for w in workloads.WORKLOADS])
+    ap.add_argument("--simt", action="store_true", help="force the fp32 SIMT kernels")
+    ap.add_argument("--skip-extras", action="store_true",
+                    help="skip the e2e, repeated-prefix and CPU legs (profiling runs)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,159 @@
+"""Python binding of the grouped-attention C ABI.  Torch supplies device memory and streams only;
+every step of the computation runs in the library's CUDA kernels.
+
+    layout = pack(prefix_lens, group_sizes, suffix_lens)          # pg_pack
+    o, lse = grouped_attn_fwd(layout, q, k, v, rope_theta=1e4)     # pg_grouped_attn_fwd
+    dq, dk, dv = grouped_attn_bwd(layout, q, k, v, o, lse, do)    # pg_grouped_attn_bwd
+"""
+from __future__ import annotations
+
+import ctypes as C
+from typing import Optional, Sequence
+
+import torch
+
+from . import _lib
+from ._lib import PgLayout, PgOpts, check, int_array
+
+_DT = {torch.float32: _lib.PG_F32, torch.bfloat16: _lib.PG_BF16}
+
+
+def _stream_ptr(device: torch.device) -> C.c_void_p:
+    return C.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+class Layout:
+    """A packed batch: the C layout struct plus the device buffers it points into."""
+
+    def __init__(self, prefix_lens, group_sizes, suffix_lens, struct: PgLayout,
+                 position_ids: torch.Tensor, tables: torch.Tensor):
+        self.prefix_lens = list(prefix_lens)
+        self.group_sizes = list(group_sizes)
+        self.suffix_lens = list(suffix_lens)
+        self.struct = struct
+        self.position_ids = position_ids
+        self.tables = tables
+
+    @property
+    def total_tokens(self) -> int:
+        return int(self.struct.total_tokens)
+
+    @property
+    def pairs(self) -> int:
+        return int(self.struct.pairs)
+
+
+def pack_size(prefix_lens, group_sizes, suffix_lens):
+    T, nb = C.c_int64(), C.c_int64()
+    check("pg_pack_size", _lib.lib().pg_pack_size(
+        len(prefix_lens), int_array(prefix_lens), int_array(group_sizes), int_array(suffix_lens),
+        C.byref(T), C.byref(nb)))
+    return T.value, nb.value
+
+
+def pack_host(prefix_lens: Sequence[int], group_sizes: Sequence[int], suffix_lens: Sequence[int]):
+    """Host-only packing (no CUDA): returns (position_ids int32 tensor, tables uint8 tensor, struct)."""
+    T, nb = pack_size(prefix_lens, group_sizes, suffix_lens)
+    pos = torch.empty(T, dtype=torch.int32)
+    tab = torch.empty(nb, dtype=torch.uint8)
+    st = PgLayout()
+    check("pg_pack_host", _lib.lib().pg_pack_host(
+        len(prefix_lens), int_array(prefix_lens), int_array(group_sizes), int_array(suffix_lens),
+        C.cast(pos.data_ptr(), _lib.I32P), C.c_void_p(tab.data_ptr()), nb, C.byref(st)))
+    return pos, tab, st
+
+
+def pack(prefix_lens: Sequence[int], group_sizes: Sequence[int], suffix_lens: Sequence[int],
+         device="cuda") -> Layout:
+    device = torch.device(device)
+    T, nb = pack_size(prefix_lens, group_sizes, suffix_lens)
+    pos = torch.empty(T, dtype=torch.int32, device=device)
+    tab = torch.empty(nb, dtype=torch.uint8, device=device)
+    st = PgLayout()
+    with torch.cuda.device(device):
+        check("pg_pack", _lib.lib().pg_pack(
+            len(prefix_lens), int_array(prefix_lens), int_array(group_sizes),
+            int_array(suffix_lens), C.c_void_p(pos.data_ptr()), C.c_void_p(tab.data_ptr()), nb,
+            C.byref(st), _stream_ptr(device)))
+    return Layout(prefix_lens, group_sizes, suffix_lens, st, pos, tab)
+
+
+def make_opts(rope_theta: float = 0.0, softmax_scale: float = 0.0, flags: int = 0,
+              debug: int = 0) -> PgOpts:
+    return PgOpts(float(softmax_scale), float(rope_theta), int(flags), int(debug))
+
+
+def _dims(q: torch.Tensor, k: torch.Tensor):
+    if q.dim() != 3 or k.dim() != 3:
+        raise ValueError("q must be [T, Hq, d] and k, v [T, Hkv, d]")
+    return q.shape[1], k.shape[1], q.shape[2]
+
+
+def _ptr(t: Optional[torch.Tensor]) -> C.c_void_p:
+    return C.c_void_p(t.data_ptr() if t is not None else 0)
+
+
+def _contig(*ts):
+    for t in ts:
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def workspace_size(layout: Layout, dtype: torch.dtype, Hq: int, Hkv: int, d: int, opts: PgOpts,
+                   phase: int) -> int:
+    n = C.c_size_t()
+    check("pg_workspace_size", _lib.lib().pg_workspace_size(
+        C.byref(layout.struct), _DT[dtype], Hq, Hkv, d, C.byref(opts), phase, C.byref(n)))
+    return n.value
+
+
+def _workspace(n: int, device) -> torch.Tensor:
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def grouped_attn_fwd(layout: Layout, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *,
+                     rope_theta: float = 0.0, softmax_scale: float = 0.0, flags: int = 0,
+                     debug: int = 0, out: Optional[torch.Tensor] = None,
+                     lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
+    Hq, Hkv, d = _dims(q, k)
+    _contig(q, k, v)
+    opts = make_opts(rope_theta, softmax_scale, flags, debug)
+    T = layout.total_tokens
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = _workspace(workspace_size(layout, q.dtype, Hq, Hkv, d, opts, 0), q.device)
+    with torch.cuda.device(q.device):
+        check("pg_grouped_attn_fwd", _lib.lib().pg_grouped_attn_fwd(
+            C.byref(layout.struct), _DT[q.dtype], Hq, Hkv, d, _ptr(q), _ptr(k), _ptr(v),
+            _ptr(out), _ptr(lse), C.byref(opts), _ptr(workspace), workspace.numel(),
+            _stream_ptr(q.device)))
+    return out, lse
+
+
+def grouped_attn_bwd(layout: Layout, q, k, v, o, lse, do, *, rope_theta: float = 0.0,
+                     softmax_scale: float = 0.0, flags: int = 0, debug: int = 0,
+                     dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
+                     dv: Optional[torch.Tensor] = None,
+                     workspace: Optional[torch.Tensor] = None):
+    Hq, Hkv, d = _dims(q, k)
+    _contig(q, k, v, o, lse, do)
+    opts = make_opts(rope_theta, softmax_scale, flags, debug)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = _workspace(workspace_size(layout, q.dtype, Hq, Hkv, d, opts, 1), q.device)
+    with torch.cuda.device(q.device):
+        check("pg_grouped_attn_bwd", _lib.lib().pg_grouped_attn_bwd(
+            C.byref(layout.struct), _DT[q.dtype], Hq, Hkv, d, _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+            _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), C.byref(opts), _ptr(workspace),
+            workspace.numel(), _stream_ptr(q.device)))
+    return dq, dk, dv
+
+
+def device_status(clear: bool = True) -> int:
+    """The kernels' status word (0 = ok); synchronous."""
+    return int(_lib.lib().pg_device_status(1 if clear else 0))

@@ -1,0 +1,466 @@
+// Host side of the grouped-attention C ABI: packing, argument checks, workspace, dispatch.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <numeric>
+#include <vector>
+
+#include "pg_internal.h"
+
+namespace pg {
+
+static thread_local char g_msg[512] = "";
+thread_local pg_profile* g_profile = nullptr;
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+}
+
+pg_status cuda_check(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return PG_OK;
+  set_error("%s: %s", what, cudaGetErrorString(e));
+  return PG_ERR_CUDA;
+}
+
+static int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------------------------------------
+// Packing.  Groups are laid out back to back; within a group the prefix is followed by its
+// responses ("Sequential Concatenation" of the skill page; [P; R1; ...; RG] of the Pith review).
+// ---------------------------------------------------------------------------------------------
+
+struct Plan {
+  int64_t T = 0, segs = 0, max_pos = 0, pairs = 0;
+  int64_t n[4] = {0, 0, 0, 0};
+  int64_t off[4] = {0, 0, 0, 0};
+  int64_t off_tokens = 0, bytes = 0;
+};
+
+static pg_status check_lengths(int32_t B, const int32_t* lp, const int32_t* gs, const int32_t* rs,
+                               Plan* p) {
+  if (B < 1 || !lp || !gs) {
+    set_error("pg_pack: num_groups must be >= 1 and arrays non-NULL");
+    return PG_ERR_INVALID_ARG;
+  }
+  int64_t T = 0, S = 0, maxpos = 0, pairs = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    if (lp[b] < 0 || gs[b] < 0) {
+      set_error("pg_pack: negative prefix length or group size in group %d", b);
+      return PG_ERR_INVALID_ARG;
+    }
+    int64_t L = lp[b];
+    T += L;
+    maxpos = std::max(maxpos, L);
+    pairs += L * (L + 1) / 2;
+    if (gs[b] > 0 && !rs) {
+      set_error("pg_pack: suffix_lens is NULL");
+      return PG_ERR_INVALID_ARG;
+    }
+    for (int32_t i = 0; i < gs[b]; ++i, ++S) {
+      int64_t r = rs[S];
+      if (r < 0) {
+        set_error("pg_pack: negative suffix length at response %lld", (long long)S);
+        return PG_ERR_INVALID_ARG;
+      }
+      T += r;
+      maxpos = std::max(maxpos, L + r);
+      pairs += r * L + r * (r + 1) / 2;
+      if (T >= (int64_t(1) << 30)) break;
+    }
+    if (T >= (int64_t(1) << 30)) break;
+  }
+  if (T <= 0 || T >= (int64_t(1) << 30)) {
+    set_error("pg_pack: total tokens must be in [1, 2^30), got %lld", (long long)T);
+    return PG_ERR_INVALID_ARG;
+  }
+  p->T = T;
+  p->segs = S;
+  p->max_pos = maxpos;
+  p->pairs = pairs;
+  // Work-list lengths: one tile per started block of rows in each group.
+  int64_t n64 = 0, n128 = 0;
+  int64_t s = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    int64_t len = lp[b];
+    for (int32_t i = 0; i < gs[b]; ++i) len += rs[s++];
+    n64 += (len + 63) / 64;
+    n128 += (len + 127) / 128;
+  }
+  p->n[FWD64] = p->n[BWD64] = n64;
+  p->n[FWD128] = p->n[BWD128] = n128;
+  int64_t off = 0;
+  p->off_tokens = off;
+  off = align_up(off + 16 * T, 256);
+  for (int w = 0; w < 4; ++w) {
+    p->off[w] = off;
+    off = align_up(off + 32 * p->n[w], 256);
+  }
+  p->bytes = off;
+  return PG_OK;
+}
+
+template <typename Tile>
+static void sort_by_cost(std::vector<Tile>& v, std::vector<int64_t>& cost) {
+  std::vector<size_t> idx(v.size());
+  std::iota(idx.begin(), idx.end(), 0);
+  std::stable_sort(idx.begin(), idx.end(), [&](size_t a, size_t b) { return cost[a] > cost[b]; });
+  std::vector<Tile> out(v.size());
+  for (size_t i = 0; i < idx.size(); ++i) out[i] = v[idx[i]];
+  v.swap(out);
+}
+
+static void build_tables(int32_t B, const int32_t* lp, const int32_t* gs, const int32_t* rs,
+                         const Plan& p, int32_t* pos, char* tables) {
+  int4* tok = reinterpret_cast<int4*>(tables + p.off_tokens);
+  std::vector<int32_t> seg_end_of(p.T);  // row after the token's own response (or group end)
+  int32_t row = 0;
+  int64_t s = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    int32_t g0 = row, pe = row + lp[b];
+    for (int32_t j = 0; j < lp[b]; ++j, ++row) {
+      tok[row] = make_int4(g0, pe, g0, j);
+      pos[row] = j;
+      seg_end_of[row] = pe;
+    }
+    for (int32_t i = 0; i < gs[b]; ++i, ++s) {
+      int32_t own = row;
+      for (int32_t j = 0; j < rs[s]; ++j, ++row) {
+        tok[row] = make_int4(g0, pe, own, lp[b] + j);
+        pos[row] = lp[b] + j;
+        seg_end_of[row] = own + rs[s];
+      }
+    }
+  }
+  // Work lists, per group, for 64- and 128-row tiles; heaviest first.
+  for (int bm = 64, wi = 0; bm <= 128; bm *= 2, ++wi) {
+    std::vector<FwdTile> ft;
+    std::vector<BwdTile> bt;
+    std::vector<int64_t> fc, bc;
+    int32_t g0 = 0;
+    int64_t sb = 0;
+    for (int32_t b = 0; b < B; ++b) {
+      int32_t pe = g0 + lp[b];
+      int32_t gend = pe;
+      for (int32_t i = 0; i < gs[b]; ++i) gend += rs[sb + i];
+      sb += gs[b];
+      if (gend == g0) continue;
+      for (int32_t q0 = g0; q0 < gend; q0 += bm) {
+        int32_t q1 = std::min(q0 + bm, gend);
+        FwdTile t{};
+        t.q0 = q0;
+        t.q1 = q1;
+        t.g0 = g0;
+        t.pe = pe;
+        t.p_end = std::min(pe, q1);
+        if (q1 > pe) {
+          t.s_lo = tok[std::max(q0, pe)].z;
+          t.s_hi = q1;
+        } else {
+          t.s_lo = t.s_hi = q1;
+        }
+        ft.push_back(t);
+        fc.push_back(int64_t(q1 - q0) * ((t.p_end - g0) + (t.s_hi - t.s_lo)));
+        BwdTile u{};
+        u.k0 = q0;
+        u.k1 = q1;
+        u.g0 = g0;
+        u.pe = pe;
+        u.q_lo = q0;
+        u.q_hi = (q0 < pe) ? gend : seg_end_of[q1 - 1];
+        bt.push_back(u);
+        bc.push_back(int64_t(q1 - q0) * (u.q_hi - u.q_lo));
+      }
+      g0 = gend;
+    }
+    sort_by_cost(ft, fc);
+    sort_by_cost(bt, bc);
+    int fw = wi == 0 ? FWD64 : FWD128, bw = wi == 0 ? BWD64 : BWD128;
+    memcpy(tables + p.off[fw], ft.data(), ft.size() * sizeof(FwdTile));
+    memcpy(tables + p.off[bw], bt.data(), bt.size() * sizeof(BwdTile));
+  }
+}
+
+static void fill_layout(int32_t B, const Plan& p, const int32_t* pos, const void* tables,
+                        pg_layout* L) {
+  memset(L, 0, sizeof(*L));
+  L->num_groups = B;
+  L->num_segments = p.segs;
+  L->total_tokens = p.T;
+  L->max_position = p.max_pos;
+  L->pairs = p.pairs;
+  for (int w = 0; w < 4; ++w) {
+    L->n_tiles[w] = p.n[w];
+    L->off_tiles[w] = p.off[w];
+  }
+  L->off_tokens = p.off_tokens;
+  L->table_bytes = p.bytes;
+  L->position_ids = pos;
+  L->tables = tables;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Attention argument checks and workspace
+// ---------------------------------------------------------------------------------------------
+
+struct WsPlan {
+  size_t q_rot = 0, k_rot = 0, Dbuf = 0, dq_acc = 0, dk_acc = 0, total = 0;
+};
+
+static size_t esize(pg_dtype dt) { return dt == PG_F32 ? 4 : 2; }
+
+static WsPlan ws_plan(const pg_layout* L, pg_dtype dt, int Hq, int Hkv, int d, bool rope,
+                      int phase) {
+  WsPlan w;
+  size_t T = (size_t)L->total_tokens;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = (size_t)align_up((int64_t)(off + bytes), 256);
+    return o;
+  };
+  // Offset 0 is a valid slot; record "absent" as SIZE_MAX.
+  w.q_rot = w.k_rot = w.Dbuf = w.dq_acc = w.dk_acc = SIZE_MAX;
+  if (rope) {
+    w.q_rot = take(T * Hq * d * esize(dt));
+    w.k_rot = take(T * Hkv * d * esize(dt));
+  }
+  if (phase == 1) {
+    w.Dbuf = take(T * Hq * sizeof(float));
+    w.dq_acc = take(T * Hq * d * sizeof(float));
+    w.dk_acc = take(T * Hkv * d * sizeof(float));
+  }
+  w.total = off;
+  return w;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static pg_status check_attn(const pg_layout* L, pg_dtype dt, int Hq, int Hkv, int d,
+                            const pg_opts* opts, std::initializer_list<const void*> ptrs,
+                            const char* who) {
+  if (!L || !L->tables || !L->position_ids || L->total_tokens <= 0) {
+    set_error("%s: layout missing or empty (call pg_pack first)", who);
+    return PG_ERR_INVALID_ARG;
+  }
+  if (dt != PG_F32 && dt != PG_BF16) {
+    set_error("%s: unknown dtype %d", who, (int)dt);
+    return PG_ERR_INVALID_ARG;
+  }
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) {
+    set_error("%s: heads_q (%d) must be a positive multiple of heads_kv (%d)", who, Hq, Hkv);
+    return PG_ERR_INVALID_ARG;
+  }
+  if (d != 64 && d != 128) {
+    set_error("%s: head_dim must be 64 or 128, got %d", who, d);
+    return PG_ERR_INVALID_ARG;
+  }
+  if (opts && (opts->softmax_scale < 0.f || opts->rope_theta < 0.f)) {
+    set_error("%s: softmax_scale and rope_theta must be >= 0", who);
+    return PG_ERR_INVALID_ARG;
+  }
+  int i = 0;
+  for (const void* p : ptrs) {
+    if (!p || !aligned16(p)) {
+      set_error("%s: pointer argument %d is NULL or not 16-byte aligned", who, i);
+      return PG_ERR_INVALID_ARG;
+    }
+    ++i;
+  }
+  return PG_OK;
+}
+
+static AttnArgs make_args(const pg_layout* L, pg_dtype dt, int Hq, int Hkv, int d,
+                          const pg_opts* opts, cudaStream_t s) {
+  AttnArgs a;
+  a.layout = L;
+  a.dtype = dt;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.scale = (opts && opts->softmax_scale > 0.f) ? opts->softmax_scale : 1.0f / sqrtf((float)d);
+  a.theta = opts ? opts->rope_theta : 0.f;
+  a.flags = opts ? opts->flags : 0u;
+  a.debug = opts ? opts->debug : 0u;
+  a.stream = s;
+  return a;
+}
+
+}  // namespace pg
+
+using namespace pg;
+
+extern "C" {
+
+pg_status pg_pack_size(int32_t num_groups, const int32_t* prefix_lens, const int32_t* group_sizes,
+                       const int32_t* suffix_lens, int64_t* total_tokens, int64_t* table_bytes) {
+  Plan p;
+  pg_status st = check_lengths(num_groups, prefix_lens, group_sizes, suffix_lens, &p);
+  if (st != PG_OK) return st;
+  if (total_tokens) *total_tokens = p.T;
+  if (table_bytes) *table_bytes = p.bytes;
+  return PG_OK;
+}
+
+pg_status pg_pack_host(int32_t num_groups, const int32_t* prefix_lens, const int32_t* group_sizes,
+                       const int32_t* suffix_lens, int32_t* position_ids, void* tables,
+                       int64_t table_bytes, pg_layout* layout) {
+  Plan p;
+  pg_status st = check_lengths(num_groups, prefix_lens, group_sizes, suffix_lens, &p);
+  if (st != PG_OK) return st;
+  if (!position_ids || !tables || !layout || table_bytes < p.bytes) {
+    set_error("pg_pack_host: NULL buffer or table buffer smaller than %lld bytes",
+              (long long)p.bytes);
+    return PG_ERR_INVALID_ARG;
+  }
+  memset(tables, 0, (size_t)p.bytes);
+  build_tables(num_groups, prefix_lens, group_sizes, suffix_lens, p, position_ids,
+               static_cast<char*>(tables));
+  fill_layout(num_groups, p, position_ids, tables, layout);
+  return PG_OK;
+}
+
+pg_status pg_pack(int32_t num_groups, const int32_t* prefix_lens, const int32_t* group_sizes,
+                  const int32_t* suffix_lens, int32_t* position_ids_dev, void* tables_dev,
+                  int64_t table_bytes, pg_layout* layout, pg_stream_t stream) {
+  Plan p;
+  pg_status st = check_lengths(num_groups, prefix_lens, group_sizes, suffix_lens, &p);
+  if (st != PG_OK) return st;
+  if (!position_ids_dev || !tables_dev || !layout || table_bytes < p.bytes) {
+    set_error("pg_pack: NULL buffer or table buffer smaller than %lld bytes", (long long)p.bytes);
+    return PG_ERR_INVALID_ARG;
+  }
+  std::vector<int32_t> pos((size_t)p.T);
+  std::vector<char> tab((size_t)p.bytes);
+  pg_layout host;
+  st = pg_pack_host(num_groups, prefix_lens, group_sizes, suffix_lens, pos.data(), tab.data(),
+                    p.bytes, &host);
+  if (st != PG_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  st = cuda_check(cudaMemcpyAsync(position_ids_dev, pos.data(), pos.size() * 4,
+                                  cudaMemcpyHostToDevice, s), "pg_pack: copy position ids");
+  if (st != PG_OK) return st;
+  st = cuda_check(cudaMemcpyAsync(tables_dev, tab.data(), tab.size(), cudaMemcpyHostToDevice, s),
+                  "pg_pack: copy tables");
+  if (st != PG_OK) return st;
+  // Pageable-source copies return once the source has been staged; make that explicit so the
+  // vectors can be released whatever the runtime's staging policy.
+  st = cuda_check(cudaStreamSynchronize(s), "pg_pack: synchronize");
+  if (st != PG_OK) return st;
+  *layout = host;
+  layout->position_ids = position_ids_dev;
+  layout->tables = tables_dev;
+  return PG_OK;
+}
+
+pg_status pg_workspace_size(const pg_layout* layout, pg_dtype dtype, int32_t heads_q,
+                            int32_t heads_kv, int32_t head_dim, const pg_opts* opts, int32_t phase,
+                            size_t* bytes) {
+  if (!bytes || (phase != 0 && phase != 1)) {
+    set_error("pg_workspace_size: bytes is NULL or phase not 0/1");
+    return PG_ERR_INVALID_ARG;
+  }
+  pg_status st = check_attn(layout, dtype, heads_q, heads_kv, head_dim, opts, {},
+                            "pg_workspace_size");
+  if (st != PG_OK) return st;
+  bool rope = opts && opts->rope_theta > 0.f;
+  *bytes = ws_plan(layout, dtype, heads_q, heads_kv, head_dim, rope, phase).total;
+  return PG_OK;
+}
+
+pg_status pg_grouped_attn_fwd(const pg_layout* layout, pg_dtype dtype, int32_t heads_q,
+                              int32_t heads_kv, int32_t head_dim, const void* q, const void* k,
+                              const void* v, void* o, float* lse, const pg_opts* opts,
+                              void* workspace, size_t workspace_bytes, pg_stream_t stream) {
+  const char* who = "pg_grouped_attn_fwd";
+  pg_status st = check_attn(layout, dtype, heads_q, heads_kv, head_dim, opts, {q, k, v, o, lse},
+                            who);
+  if (st != PG_OK) return st;
+  AttnArgs a = make_args(layout, dtype, heads_q, heads_kv, head_dim, opts,
+                         reinterpret_cast<cudaStream_t>(stream));
+  bool rope = a.theta > 0.f;
+  WsPlan w = ws_plan(layout, dtype, heads_q, heads_kv, head_dim, rope, 0);
+  if (w.total > 0 && (!workspace || workspace_bytes < w.total || !aligned16(workspace))) {
+    set_error("%s: workspace must be 16-byte aligned and >= %zu bytes", who, w.total);
+    return PG_ERR_INVALID_ARG;
+  }
+  char* ws = static_cast<char*>(workspace);
+  const void* qx = q;
+  const void* kx = k;
+  if (rope) {
+    st = launch_rope(a, q, ws + w.q_rot, heads_q, k, ws + w.k_rot, heads_kv, false, false);
+    if (st != PG_OK) return st;
+    qx = ws + w.q_rot;
+    kx = ws + w.k_rot;
+  }
+  return launch_fwd_simt(a, qx, kx, v, o, lse);
+}
+
+pg_status pg_grouped_attn_bwd(const pg_layout* layout, pg_dtype dtype, int32_t heads_q,
+                              int32_t heads_kv, int32_t head_dim, const void* q, const void* k,
+                              const void* v, const void* o, const float* lse, const void* dO,
+                              void* dq, void* dk, void* dv, const pg_opts* opts, void* workspace,
+                              size_t workspace_bytes, pg_stream_t stream) {
+  const char* who = "pg_grouped_attn_bwd";
+  pg_status st = check_attn(layout, dtype, heads_q, heads_kv, head_dim, opts,
+                            {q, k, v, o, lse, dO, dq, dk, dv}, who);
+  if (st != PG_OK) return st;
+  AttnArgs a = make_args(layout, dtype, heads_q, heads_kv, head_dim, opts,
+                         reinterpret_cast<cudaStream_t>(stream));
+  bool rope = a.theta > 0.f;
+  WsPlan w = ws_plan(layout, dtype, heads_q, heads_kv, head_dim, rope, 1);
+  if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) {
+    set_error("%s: workspace must be 16-byte aligned and >= %zu bytes", who, w.total);
+    return PG_ERR_INVALID_ARG;
+  }
+  char* ws = static_cast<char*>(workspace);
+  const void* qx = q;
+  const void* kx = k;
+  if (rope) {
+    st = launch_rope(a, q, ws + w.q_rot, heads_q, k, ws + w.k_rot, heads_kv, false, false);
+    if (st != PG_OK) return st;
+    qx = ws + w.q_rot;
+    kx = ws + w.k_rot;
+  }
+  float* Dbuf = reinterpret_cast<float*>(ws + w.Dbuf);
+  float* dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);
+  float* dk_acc = reinterpret_cast<float*>(ws + w.dk_acc);
+  st = launch_bwd_preprocess(a, o, dO, Dbuf);
+  if (st != PG_OK) return st;
+  st = launch_bwd_simt(a, qx, kx, v, o, lse, dO, Dbuf, dq_acc, dk_acc, dv);
+  if (st != PG_OK) return st;
+  // dQ and dK of the rotated q/k back to the caller's q/k (inverse rotation) and dtype.
+  return launch_rope(a, dq_acc, dq, heads_q, dk_acc, dk, heads_kv, true, true);
+}
+
+pg_status pg_set_profile(pg_profile* profile) {
+  g_profile = profile;
+  return PG_OK;
+}
+
+pg_status pg_device_status(int32_t clear) {
+  int32_t code = 0;
+  pg_status st = read_kernel_status(clear != 0, &code);
+  if (st != PG_OK) return st;
+  return static_cast<pg_status>(code);
+}
+
+const char* pg_status_string(pg_status s) {
+  switch (s) {
+    case PG_OK: return "ok";
+    case PG_ERR_INVALID_ARG: return "invalid argument";
+    case PG_ERR_UNSUPPORTED: return "unsupported";
+    case PG_ERR_CUDA: return "CUDA error";
+    case PG_ERR_TIMEOUT: return "bounded wait timed out in a kernel";
+    case PG_ERR_DEVICE: return "kernel-side check failed";
+  }
+  return "unknown status";
+}
+
+const char* pg_last_error_message(void) { return g_msg; }
+
+}  // extern "C"

@@ -1,0 +1,84 @@
+// Internal declarations shared by the host API and the kernels of the grouped-attention library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/pg_grouped_attn.h"
+
+namespace pg {
+
+// Work item of the forward (and of the SIMT dQ kernel): query rows [q0, q1) of one group.
+// Keys are visited in two ranges: the group's prefix [g0, p_end) and the responses' part
+// [s_lo, s_hi).  A query row t sees key s iff s <= t && s >= g0 && (s < pe || s >= own_lo(t)).
+struct FwdTile {
+  int32_t q0, q1;      // query rows
+  int32_t g0, p_end;   // prefix keys [g0, p_end), p_end = min(pe, q1)
+  int32_t s_lo, s_hi;  // response keys [s_lo, s_hi) (empty when the tile has no response rows)
+  int32_t pe, pad;     // row after the group's prefix
+};
+
+// Work item of the key-major backward: key rows [k0, k1) of one group and the query rows
+// [q_lo, q_hi) that can see any of them (the rest of the prefix and every response of the group
+// for a prefix key; the rest of the key's own response otherwise).
+struct BwdTile {
+  int32_t k0, k1;
+  int32_t q_lo, q_hi;
+  int32_t g0, pe;
+  int32_t pad0, pad1;
+};
+
+static_assert(sizeof(FwdTile) == 32, "FwdTile layout");
+static_assert(sizeof(BwdTile) == 32, "BwdTile layout");
+
+enum TileList { FWD64 = 0, FWD128 = 1, BWD64 = 2, BWD128 = 3 };
+
+inline const int4* tokens(const pg_layout* L) {
+  return reinterpret_cast<const int4*>(static_cast<const char*>(L->tables) + L->off_tokens);
+}
+template <typename Tile>
+inline const Tile* tiles(const pg_layout* L, int which) {
+  return reinterpret_cast<const Tile*>(static_cast<const char*>(L->tables) + L->off_tiles[which]);
+}
+
+// Arguments common to every attention kernel launch.
+struct AttnArgs {
+  const pg_layout* layout;
+  pg_dtype dtype;
+  int Hq, Hkv, d;
+  float scale;        // softmax scale
+  float theta;        // RoPE base, 0 = off
+  uint32_t flags, debug;
+  cudaStream_t stream;
+};
+
+void set_error(const char* fmt, ...);
+
+// Profiling hook (pg_set_profile): call before / after every kernel launch.
+extern thread_local pg_profile* g_profile;
+inline void prof_begin(pg_kernel kid, cudaStream_t s) {
+  if (!g_profile) return;
+  ++g_profile->launches;
+  if (g_profile->kernel == kid && g_profile->ev_begin)
+    cudaEventRecord(static_cast<cudaEvent_t>(g_profile->ev_begin), s);
+}
+inline void prof_end(pg_kernel kid, cudaStream_t s) {
+  if (g_profile && g_profile->kernel == kid && g_profile->ev_end)
+    cudaEventRecord(static_cast<cudaEvent_t>(g_profile->ev_end), s);
+}
+// Reads (and optionally clears) the device status words of every kernel file; first error wins.
+pg_status read_kernel_status(bool clear, int32_t* code);
+pg_status cuda_check(cudaError_t e, const char* what);
+
+// SIMT kernels (pg_simt.cu).
+pg_status launch_rope(const AttnArgs& a, const void* x0, void* y0, int heads0, const void* x1,
+                      void* y1, int heads1, bool inverse, bool in_fp32);
+pg_status launch_fwd_simt(const AttnArgs& a, const void* q, const void* k, const void* v, void* o,
+                          float* lse);
+pg_status launch_bwd_simt(const AttnArgs& a, const void* q, const void* k, const void* v,
+                          const void* o, const float* lse, const void* dO, float* Dbuf,
+                          float* dq_acc, float* dk_acc, void* dv);
+pg_status launch_bwd_preprocess(const AttnArgs& a, const void* o, const void* dO, float* Dbuf);
+
+}  // namespace pg

@@ -1,0 +1,149 @@
+"""CPU checks of the C ABI: the library loads and exports every declared symbol, the host-side
+packing matches the oracle bit for bit, and bad arguments are rejected before any launch."""
+import ctypes as C
+import os
+import re
+
+import pytest
+import torch
+
+from oracle import prefix_grouper_oracle as orc
+from shared_prefix_grouped_gb300 import _lib, api, flops
+from shared_prefix_grouped_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    build()
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(pg_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_functions()
+    assert "pg_grouped_attn_fwd" in names and "pg_pack" in names
+    handle = C.CDLL(_lib.LIB_PATH)
+    for n in names:
+        assert hasattr(handle, n), n
+    assert set(names) <= set(_lib.SIGNATURES)
+
+
+TOK_CASES = [
+    ([3, 2], [2, 3], [2, 1, 1, 0, 2]),
+    ([0], [3], [5, 0, 2]),
+    ([7], [0], []),
+    ([130, 0, 64], [3, 2, 1], [1, 200, 63, 65, 0, 128]),
+    ([300], [4], [64, 1, 127, 129]),
+]
+
+
+def expand_mask(tok):
+    """Visibility implied by the library's per-token table {g0, pe, own_lo, pos}."""
+    T = tok.shape[0]
+    t = torch.arange(T)[:, None]
+    s = torch.arange(T)[None, :]
+    g0, pe, own = tok[:, 0:1], tok[:, 1:2], tok[:, 2:3]
+    return (s <= t) & (s >= g0) & ((s < pe) | (s >= own))
+
+
+def unpack(tab, struct):
+    T = struct.total_tokens
+    raw = tab.numpy().tobytes()
+    tok = torch.frombuffer(bytearray(raw[struct.off_tokens: struct.off_tokens + 16 * T]),
+                           dtype=torch.int32).view(T, 4).clone()
+    lists = []
+    for w in range(4):
+        n = struct.n_tiles[w]
+        o = struct.off_tiles[w]
+        lists.append(torch.frombuffer(bytearray(raw[o: o + 32 * n]), dtype=torch.int32)
+                     .view(n, 8).clone() if n else torch.zeros((0, 8), dtype=torch.int32))
+    return tok, lists
+
+
+@pytest.mark.parametrize("case", TOK_CASES)
+def test_pack_host_matches_oracle_bit_exactly(case):
+    plens, gsz, rs = case
+    pos, tab, st = api.pack_host(plens, gsz, rs)
+    lay = orc.pack_layout(plens, gsz, rs)
+    assert st.total_tokens == lay.total_tokens
+    assert torch.equal(pos.to(torch.int64), lay.position_ids)
+    tok, lists = unpack(tab, st)
+    assert torch.equal(tok[:, 3].to(torch.int64), lay.position_ids)
+    mask = orc.visibility_mask(lay)
+    assert torch.equal(expand_mask(tok), mask)
+    assert st.pairs == int(mask.sum()) == flops.total_pairs(plens, gsz, rs)
+    T = lay.total_tokens
+    for w, bm in [(0, 64), (1, 128)]:
+        ft = lists[w]
+        # forward tiles: cover every row once; their key ranges cover every visible key
+        covered = torch.zeros(T, dtype=torch.int32)
+        for q0, q1, g0, p_end, s_lo, s_hi, pe, _ in ft.tolist():
+            assert 0 < q1 - q0 <= bm
+            covered[q0:q1] += 1
+            keys = torch.zeros(T, dtype=torch.bool)
+            keys[g0:p_end] = True
+            keys[s_lo:s_hi] = True
+            assert not bool((mask[q0:q1] & ~keys[None, :]).any())
+        assert torch.equal(covered, torch.ones(T, dtype=torch.int32))
+    for w, bm in [(2, 64), (3, 128)]:
+        bt = lists[w]
+        covered = torch.zeros(T, dtype=torch.int32)
+        for k0, k1, q_lo, q_hi, g0, pe, _, _ in bt.tolist():
+            assert 0 < k1 - k0 <= bm
+            covered[k0:k1] += 1
+            rows = torch.zeros(T, dtype=torch.bool)
+            rows[q_lo:q_hi] = True
+            assert not bool((mask[:, k0:k1] & ~rows[:, None]).any())
+        assert torch.equal(covered, torch.ones(T, dtype=torch.int32))
+
+
+def test_work_lists_are_heaviest_first():
+    _, tab, st = api.pack_host([1000], [4], [100, 300, 50, 7])
+    _, lists = unpack(tab, st)
+    ft = lists[1].tolist()
+    cost = [(q1 - q0) * ((p_end - g0) + (s_hi - s_lo)) for q0, q1, g0, p_end, s_lo, s_hi, _, _ in ft]
+    assert cost == sorted(cost, reverse=True)
+
+
+@pytest.mark.parametrize("plens,gsz,rs", [
+    ([-1], [1], [3]), ([4], [-1], []), ([4], [2], [3, -2]), ([0], [1], [0]), ([], [], []),
+])
+def test_pack_rejects_bad_lengths(plens, gsz, rs):
+    with pytest.raises(_lib.PgError) as e:
+        api.pack_size(plens, gsz, rs)
+    assert e.value.status == _lib.PG_ERR_INVALID_ARG
+
+
+def test_attention_rejects_bad_arguments_on_host():
+    _, tab, st = api.pack_host([8], [1], [4])
+    L = _lib.lib()
+    n = C.c_size_t()
+    opts = _lib.PgOpts(0.0, 0.0, 0, 0)
+    for hq, hkv, d in [(3, 2, 128), (4, 2, 96), (0, 1, 64)]:
+        assert L.pg_workspace_size(C.byref(st), _lib.PG_BF16, hq, hkv, d, C.byref(opts), 0,
+                                   C.byref(n)) == _lib.PG_ERR_INVALID_ARG
+    assert L.pg_workspace_size(C.byref(st), _lib.PG_BF16, 4, 2, 128, C.byref(opts), 0,
+                               C.byref(n)) == _lib.PG_OK
+    # NULL and misaligned pointers are refused before anything is launched
+    buf = torch.empty(4096, dtype=torch.uint8)
+    p = C.c_void_p(buf.data_ptr())
+    bad = C.c_void_p(buf.data_ptr() + 4)
+    args = [C.byref(st), _lib.PG_BF16, 4, 2, 128]
+    assert L.pg_grouped_attn_fwd(*args, None, p, p, p, p, C.byref(opts), p, 4096, None) \
+        == _lib.PG_ERR_INVALID_ARG
+    assert L.pg_grouped_attn_fwd(*args, p, bad, p, p, p, C.byref(opts), p, 4096, None) \
+        == _lib.PG_ERR_INVALID_ARG
+    assert b"16-byte" in L.pg_last_error_message()
+    neg = _lib.PgOpts(-1.0, 0.0, 0, 0)
+    assert L.pg_grouped_attn_fwd(*args, p, p, p, p, p, C.byref(neg), p, 4096, None) \
+        == _lib.PG_ERR_INVALID_ARG

@@ -1,0 +1,148 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle, element by element.
+
+Tolerances (normwise: max|x - ref| / max|ref| per tensor, against the fp64 oracle on the same
+inputs): 1e-5 for the fp32 path, 2e-2 for bf16, on O, LSE, dQ, dK and dV.  Small cases span several
+tiles and ragged tails; the full-size workloads run in the benchmark's launch configuration and are
+compared on sampled heads/groups the oracle computes exactly.
+"""
+import math
+
+import pytest
+import torch
+
+from oracle import prefix_grouper_oracle as orc
+from shared_prefix_grouped_gb300 import api, workloads
+from shared_prefix_grouped_gb300.build import build
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-5, "bf16": 2e-2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build()
+
+
+def run_gpu(prob, flags=0, theta=None):
+    w = prob.workload
+    theta = w.rope_theta if theta is None else theta
+    dev = torch.device("cuda")
+    lay = api.pack(prob.prefix_lens, prob.group_sizes, prob.suffix_lens, dev)
+    q, k, v, do = (t.to(dev) for t in (prob.q, prob.k, prob.v, prob.do))
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((q.shape[1], q.shape[0]), float("nan"), device=dev)
+    api.grouped_attn_fwd(lay, q, k, v, rope_theta=theta, flags=flags, out=o, lse=lse)
+    dq = torch.full_like(q, float("nan"))
+    dk = torch.full_like(k, float("nan"))
+    dv = torch.full_like(v, float("nan"))
+    api.grouped_attn_bwd(lay, q, k, v, o, lse, do, rope_theta=theta, flags=flags, dq=dq, dk=dk,
+                         dv=dv)
+    torch.cuda.synchronize()
+    assert api.device_status() == 0
+    out = {n: t.float().cpu() for n, t in dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv).items()}
+    for n, t in out.items():
+        assert bool(torch.isfinite(t).all()), f"{n} has unwritten or non-finite elements"
+    return out
+
+
+def compare(prob, got, tol, q_heads=None, groups=None, theta=None):
+    w = prob.workload
+    theta = w.rope_theta if theta is None else theta
+    lay = orc.pack_layout(prob.prefix_lens, prob.group_sizes, prob.suffix_lens)
+    ref = orc.repeated_prefix(lay, prob.q, prob.k, prob.v, prob.do, theta=theta, q_heads=q_heads,
+                              groups=groups)
+    errs = {}
+    for n in ["o", "lse", "dq", "dk", "dv"]:
+        r = getattr(ref, n)
+        errs[n] = orc.normwise_error(got[n], r)
+    bad = {n: e for n, e in errs.items() if not e <= tol}
+    assert not bad, f"parity failed (tol {tol}): {errs}"
+    return errs
+
+
+SMALL = [
+    # (workload index, prefix_lens, group_sizes, suffix_lens, heads_q, heads_kv)
+    (0, None, None, None, None, None),                                   # the fp32 workload, full
+    (0, [150, 0], [4, 2], [1, 77, 130, 0, 65, 3], 4, 2),                 # fp32, ragged, GQA
+    (1, [300], [4], [64, 1, 127, 129], 4, 4),                            # bf16 MHA, RoPE 1e4
+    (2, [200, 130], [3, 2], [64, 100, 1, 250, 7], 8, 2),                 # bf16 GQA, two groups
+    (3, [520], [5], [256, 1024, 300, 17, 129], 4, 1),                    # bf16 GQA, theta 5e5
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: f"w{c[0]}")
+@pytest.mark.parametrize("path", ["default", "simt"])
+def test_small_cases(case, path):
+    wi, plens, gsz, rs, hq, hkv = case
+    w = workloads.WORKLOADS[wi]
+    if plens is not None:
+        w = workloads.small_variant(w, prefix_len=plens[0], suffix_lens=rs, heads_q=hq,
+                                    heads_kv=hkv)
+    prob = workloads.make_problem(w, prefix_lens=plens, group_sizes=gsz, suffix_lens=rs)
+    flags = 1 if path == "simt" else 0
+    got = run_gpu(prob, flags=flags)
+    compare(prob, got, TOL[w.dtype])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("lens", [
+    ([0], [3], [5, 1, 9]),          # empty prefix: independent causal responses
+    ([9], [0], []),                 # a prefix with no responses
+    ([1], [1], [0]),                # a single token
+    ([64], [2], [64, 64]),          # exact tile multiples
+    ([3, 0, 70], [1, 2, 0], [0, 2, 1]),  # empty pieces everywhere
+])
+def test_edge_cases(dtype, lens):
+    plens, gsz, rs = lens
+    base = workloads.WORKLOADS[0 if dtype == "f32" else 2]
+    w = workloads.small_variant(base, prefix_len=plens[0], suffix_lens=rs, heads_q=4, heads_kv=2)
+    w = workloads.dataclasses.replace(w, head_dim=128, rope_theta=100.0)
+    prob = workloads.make_problem(w, prefix_lens=plens, group_sizes=gsz, suffix_lens=rs)
+    got = run_gpu(prob)
+    compare(prob, got, TOL[dtype])
+
+
+def test_no_cross_response_leakage_on_gpu():
+    w = workloads.small_variant(workloads.WORKLOADS[1], prefix_len=200, suffix_lens=[90, 140, 33],
+                                heads_q=2, heads_kv=2)
+    prob = workloads.make_problem(w)
+    a = run_gpu(prob)
+    # perturb response 1 (rows 290 .. 429)
+    sl = slice(290, 430)
+    prob.q[sl] = -prob.q[sl]
+    prob.k[sl] = prob.k[sl] * 2
+    prob.v[sl] = prob.v[sl] + 1
+    b = run_gpu(prob)
+    keep = torch.ones(prob.total_tokens, dtype=torch.bool)
+    keep[sl] = False
+    assert torch.equal(a["o"][keep], b["o"][keep])
+    assert torch.equal(a["lse"][:, keep], b["lse"][:, keep])
+    assert not torch.equal(a["o"][sl], b["o"][sl])
+
+
+def test_prefix_gradient_is_deterministic():
+    w = workloads.small_variant(workloads.WORKLOADS[2], prefix_len=400,
+                                suffix_lens=[100, 300, 5, 260], heads_q=8, heads_kv=2)
+    prob = workloads.make_problem(w)
+    a = run_gpu(prob)
+    b = run_gpu(prob)
+    assert torch.equal(a["dk"], b["dk"]) and torch.equal(a["dv"], b["dv"])
+    assert torch.equal(a["o"], b["o"]) and torch.equal(a["lse"], b["lse"])
+
+
+# ---------------------------------------------------------------- full-size workloads ----------
+
+@pytest.mark.parametrize("wi,q_heads,groups", [
+    (1, [0, 31], None),             # bf16 MHA, P=4096, G=8, R=512: two of 32 heads
+    (2, [4, 5, 6, 7], [0, 5]),      # bf16 GQA, 8 groups: kv head 1, groups 0 and 5
+    (3, [8, 9, 10, 11], None),      # bf16 GQA long prefix: kv head 2 with its 4 query heads
+])
+def test_full_size_sampled(wi, q_heads, groups):
+    w = workloads.WORKLOADS[wi]
+    prob = workloads.make_problem(w)
+    got = run_gpu(prob)
+    errs = compare(prob, got, TOL[w.dtype], q_heads=q_heads, groups=groups)
+    print(w.name, errs)
