@@ -64,6 +64,11 @@ typedef struct pg_opts {
 /* Run the fp32-arithmetic SIMT kernels even for bf16 inputs (a slower, independent path). */
 #define PG_FLAG_SIMT 1u
 
+/* Test hook for the bounded-wait error path: the tensor-core forward never signals that P is
+ * ready, so its MMA thread's wait runs out (after 50 ms instead of 2 s), the kernel records
+ * PG_ERR_TIMEOUT in the status word and exits cleanly; the outputs are then undefined. */
+#define PG_DEBUG_WITHHOLD_P 1u
+
 /*
  * Host-side summary of a packed batch, filled by pg_pack / pg_pack_host.  The two pointers refer to
  * the caller's buffers (device buffers for pg_pack, host buffers for pg_pack_host) which must stay
@@ -163,7 +168,8 @@ typedef enum pg_kernel {
   PG_KERNEL_BWD_PREPROCESS = 3,  /* rowsum(dO * O) */
   PG_KERNEL_BWD_DKDV = 4,        /* key-major dK/dV (and dQ where fused) */
   PG_KERNEL_BWD_DQ = 5,          /* query-major dQ */
-  PG_KERNEL_ROPE_BWD = 6         /* inverse RoPE of dQ/dK and the cast to the output dtype */
+  PG_KERNEL_ROPE_BWD = 6,        /* inverse RoPE of dQ/dK and the cast to the output dtype */
+  PG_KERNEL_GEMM = 7             /* the bf16 tensor-core GEMM (decoder-layer path) */
 } pg_kernel;
 
 /*

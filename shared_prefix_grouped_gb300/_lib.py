@@ -48,7 +48,7 @@ class PgProfile(C.Structure):
 
 
 (PG_KERNEL_NONE, PG_KERNEL_ROPE, PG_KERNEL_ATTN_FWD, PG_KERNEL_BWD_PREPROCESS, PG_KERNEL_BWD_DKDV,
- PG_KERNEL_BWD_DQ, PG_KERNEL_ROPE_BWD) = range(7)
+ PG_KERNEL_BWD_DQ, PG_KERNEL_ROPE_BWD, PG_KERNEL_GEMM) = range(8)
 
 I32P = C.POINTER(C.c_int32)
 I64P = C.POINTER(C.c_int64)
@@ -71,6 +71,8 @@ SIGNATURES = {
                                       C.c_int32, VP, VP, VP, VP, VP, VP, VP, VP, VP,
                                       C.POINTER(PgOpts), VP, C.c_size_t, VP]),
     "pg_set_profile": (C.c_int, [C.POINTER(PgProfile)]),
+    "pg_gemm_bf16": (C.c_int, [C.c_int64, C.c_int64, C.c_int64, VP, C.c_int32, C.c_int64, VP,
+                               C.c_int32, C.c_int64, VP, C.c_int, C.c_int64, VP]),
     "pg_device_status": (C.c_int, [C.c_int32]),
     "pg_status_string": (C.c_char_p, [C.c_int]),
     "pg_last_error_message": (C.c_char_p, []),

@@ -157,3 +157,26 @@ def grouped_attn_bwd(layout: Layout, q, k, v, o, lse, do, *, rope_theta: float =
 def device_status(clear: bool = True) -> int:
     """The kernels' status word (0 = ok); synchronous."""
     return int(_lib.lib().pg_device_status(1 if clear else 0))
+
+
+def gemm_bf16(a: torch.Tensor, b: torch.Tensor, *, a_mn: bool = False, b_mn: bool = False,
+              out_dtype: torch.dtype = torch.float32, out: Optional[torch.Tensor] = None):
+    """C[m, n] = sum_k A(m, k) B(n, k) on the tensor cores (pg_gemm_bf16).
+
+    a is [M, K] (a_mn False) or [K, M] (a_mn True); b is [N, K] (b_mn False) or [K, N] (True).
+    """
+    if a.dtype != torch.bfloat16 or b.dtype != torch.bfloat16:
+        raise ValueError("gemm_bf16 takes bf16 operands")
+    _contig(a, b)
+    M, K = (a.shape[1], a.shape[0]) if a_mn else (a.shape[0], a.shape[1])
+    N, Kb = (b.shape[1], b.shape[0]) if b_mn else (b.shape[0], b.shape[1])
+    if K != Kb:
+        raise ValueError("inner dimensions differ")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=a.device)
+    _contig(out)
+    with torch.cuda.device(a.device):
+        check("pg_gemm_bf16", _lib.lib().pg_gemm_bf16(
+            M, N, K, _ptr(a), int(a_mn), a.shape[1], _ptr(b), int(b_mn), b.shape[1], _ptr(out),
+            _DT[out.dtype], out.shape[1], _stream_ptr(a.device)))
+    return out

@@ -29,6 +29,15 @@ pg_status cuda_check(cudaError_t e, const char* what) {
 
 static int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
+pg_status read_kernel_status(bool clear, int32_t* code) {
+  *code = 0;
+  pg_status st = read_status_simt(clear, code);
+  if (st == PG_OK) st = read_status_gemm(clear, code);
+  if (st == PG_OK) st = read_status_fwd_sm100(clear, code);
+  if (st == PG_OK) st = read_status_bwd_sm100(clear, code);
+  return st;
+}
+
 // ---------------------------------------------------------------------------------------------
 // Packing.  Groups are laid out back to back; within a group the prefix is followed by its
 // responses ("Sequential Concatenation" of the skill page; [P; R1; ...; RG] of the Pith review).
@@ -397,6 +406,8 @@ pg_status pg_grouped_attn_fwd(const pg_layout* layout, pg_dtype dtype, int32_t h
     qx = ws + w.q_rot;
     kx = ws + w.k_rot;
   }
+  if (!(a.flags & PG_FLAG_SIMT) && fwd_sm100_supported(a))
+    return launch_fwd_sm100(a, qx, kx, v, o, lse);
   return launch_fwd_simt(a, qx, kx, v, o, lse);
 }
 
@@ -429,8 +440,15 @@ pg_status pg_grouped_attn_bwd(const pg_layout* layout, pg_dtype dtype, int32_t h
   float* Dbuf = reinterpret_cast<float*>(ws + w.Dbuf);
   float* dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);
   float* dk_acc = reinterpret_cast<float*>(ws + w.dk_acc);
-  st = launch_bwd_preprocess(a, o, dO, Dbuf);
+  st = launch_bwd_preprocess(a, o, dO, Dbuf, dq_acc);
   if (st != PG_OK) return st;
+  if (!(a.flags & PG_FLAG_SIMT) && bwd_sm100_supported(a)) {
+    // dK (inverse-rotated, cast) and dV are written by the key-major kernel itself; dQ arrives
+    // in the fp32 accumulator and is rotated back and cast here.
+    st = launch_bwd_sm100(a, qx, kx, v, dO, lse, Dbuf, dq_acc, dk, dv);
+    if (st != PG_OK) return st;
+    return launch_rope(a, dq_acc, dq, heads_q, nullptr, nullptr, 0, true, true);
+  }
   st = launch_bwd_simt(a, qx, kx, v, o, lse, dO, Dbuf, dq_acc, dk_acc, dv);
   if (st != PG_OK) return st;
   // dQ and dK of the rotated q/k back to the caller's q/k (inverse rotation) and dtype.

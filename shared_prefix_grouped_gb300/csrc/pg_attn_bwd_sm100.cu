@@ -1,0 +1,450 @@
+// Grouped-attention backward on the 5th-generation tensor cores (bf16, head_dim 128).
+//
+// Key-major: one CTA owns 128 keys of one group and one key/value head (a BwdTile) and sweeps, in
+// a fixed order, every query head of that KV head and every block of 64 query rows that can see
+// its keys.  For a prefix key block that is the rest of the prefix and then all responses of the
+// group, so the prefix dK / dV -- the sum over the G baseline copies of the shared prefix (Pith
+// review of Prefix Grouper, Appendix A.1 objection: the shared prefix's gradient equals the sum of
+// the copies' gradients) -- is accumulated in TMEM by one CTA in a fixed order: bitwise
+// reproducible, no atomics.  dQ is accumulated across key blocks with fp32 atomics (its summation
+// order is not fixed).
+//
+// Per query block (64 rows), with K, V resident in shared memory and Q, dO double-buffered:
+//   S^T  = K Q^T          M 128 keys x N 64 queries x K 128   (TMEM cols [0, 64))
+//   dP^T = V dO^T         M 128 x N 64 x K 128                 (TMEM cols [64, 128))
+//   P^T  = exp2(S^T * scale * log2 e - LSE_2[q]),  dS^T = P^T * (dP^T - Dsum[q])   (registers,
+//          one thread per key row, rounded to bf16 into shared memory)
+//   dV  += P^T dO         M 128 x N 128 dims x K 64           (TMEM cols [256, 384))
+//   dK  += dS^T Q         M 128 x N 128 x K 64                 (TMEM cols [384, 512))
+//   dQ^T = K^T dS^T       M 128 dims x N 64 queries x K 128    (TMEM cols [128, 192)),
+//          drained by four warps (one thread per head-dim lane) as coalesced fp32 atomics.
+// The MMA thread issues S^T / dP^T of block i before the gradient products of block i-1, so the
+// tensor core computes the next scores while the softmax warps work on the current ones.
+// The epilogue applies the softmax scale and the inverse RoPE rotation to dK in registers (a
+// thread holds a whole key row, so each (k, k + d/2) pair is local) and writes dK, dV in bf16.
+//
+// Warps: 0 TMA producer (+ LSE / Dsum / visibility staging), 1 TMEM allocation and MMA issue,
+// 2..5 softmax (key rows), 6..9 dQ drain.  Every mbarrier wait is bounded.
+#include <limits.h>
+#include <math.h>
+
+#include "pg_internal.h"
+#include "pg_sm100.cuh"
+#include "pg_tmap.h"
+
+namespace pg {
+
+using namespace sm100;
+
+namespace {
+
+constexpr int D = 128;
+constexpr int BKV = 128;        // keys per CTA
+constexpr int BQ = 64;          // query rows per block
+constexpr int NSQ = 2;          // Q / dO stages
+constexpr uint32_t KHALF = BKV * 64 * 2;   // 16 KiB: [128 rows][64 cols] bf16
+constexpr uint32_t QHALF = BQ * 64 * 2;    // 8 KiB:  [64 rows][64 cols] bf16
+constexpr int NTHREADS = 320;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ int s_status_bwd = 0;
+
+struct BwdSmem {
+  uint8_t k[2 * KHALF];
+  uint8_t v[2 * KHALF];
+  uint8_t q[NSQ][2 * QHALF];
+  uint8_t dO[NSQ][2 * QHALF];
+  uint8_t p[KHALF];         // P^T  [128 keys][64 queries] bf16, SW128
+  uint8_t ds[KHALF];        // dS^T [128 keys][64 queries]
+  float lse2[NSQ][BQ];
+  float dsum[NSQ][BQ];
+  int32_t own[NSQ][BQ];
+  uint64_t kv_full;
+  uint64_t qd_full[NSQ], qd_empty[NSQ];
+  uint64_t s_full, s_free, p_full, pds_free, dq_full, dq_free, mma_done;
+  uint32_t tmem;
+};
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void fail(int code) { atomicCAS(&s_status_bwd, 0, code); }
+
+__device__ __forceinline__ void red_add(float* p, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                      const float* __restrict__ lse, const float* __restrict__ Dbuf,
+                      float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dk,
+                      __nv_bfloat16* __restrict__ dv, const int4* __restrict__ tok,
+                      const BwdTile* __restrict__ tiles, int Hq, int Hkv, int Ttot,
+                      float scale_log2, float scale, double log2_theta, uint64_t wait_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  BwdSmem& sm = *reinterpret_cast<BwdSmem*>(base);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile_id = blockIdx.x / Hkv, kh = blockIdx.x % Hkv;
+  const BwdTile tl = tiles[tile_id];
+  if (tl.k0 < 0 || tl.k1 > Ttot || tl.k0 >= tl.k1 || tl.k1 - tl.k0 > BKV || tl.q_lo < 0 ||
+      tl.q_hi > Ttot || tl.q_lo >= tl.q_hi) {
+    if (threadIdx.x == 0) fail(PG_ERR_DEVICE);
+    return;
+  }
+  const int rep = Hq / Hkv;
+  const int nqt = (tl.q_hi - tl.q_lo + BQ - 1) / BQ;
+  const int n_it = rep * nqt;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sm.kv_full, 1);
+    for (int s = 0; s < NSQ; ++s) {
+      mbar_init(&sm.qd_full[s], 1);
+      mbar_init(&sm.qd_empty[s], 1);
+    }
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.s_free, 128);
+    mbar_init(&sm.p_full, 128);
+    mbar_init(&sm.pds_free, 1);
+    mbar_init(&sm.dq_full, 1);
+    mbar_init(&sm.dq_free, 128);
+    mbar_init(&sm.mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem;
+  const uint32_t t_s = tmem, t_dp = tmem + 64, t_dq = tmem + 128, t_dv = tmem + 256,
+                 t_dk = tmem + 384;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer ---------
+    const bool leader = elect_one();
+    if (leader) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      prefetch_tmap(&tdo);
+      mbar_expect_tx(&sm.kv_full, 4 * KHALF);
+      tma_load_2d(sm.k, &tk, &sm.kv_full, kh * D, tl.k0);
+      tma_load_2d(sm.k + KHALF, &tk, &sm.kv_full, kh * D + 64, tl.k0);
+      tma_load_2d(sm.v, &tv, &sm.kv_full, kh * D, tl.k0);
+      tma_load_2d(sm.v + KHALF, &tv, &sm.kv_full, kh * D + 64, tl.k0);
+    }
+    int issued = 0;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int st = it % NSQ;
+      const int h = kh * rep + it / nqt;
+      const int qt = tl.q_lo + (it % nqt) * BQ;
+      if (!warp_wait(&sm.qd_empty[st], ((it / NSQ) & 1) ^ 1, wait_ns)) { ok = false; break; }
+      for (int c = lane; c < BQ; c += 32) {
+        const int t = qt + c;
+        const bool in = t < tl.q_hi;
+        sm.lse2[st][c] = in ? lse[(size_t)h * Ttot + t] * kLog2e : 0.f;
+        sm.dsum[st][c] = in ? Dbuf[(size_t)h * Ttot + t] : 0.f;
+        sm.own[st][c] = in ? tok[t].z : INT_MAX;
+      }
+      __threadfence_block();
+      __syncwarp();
+      if (leader) {
+        mbar_expect_tx(&sm.qd_full[st], 4 * QHALF);
+        tma_load_2d(sm.q[st], &tq, &sm.qd_full[st], h * D, qt);
+        tma_load_2d(sm.q[st] + QHALF, &tq, &sm.qd_full[st], h * D + 64, qt);
+        tma_load_2d(sm.dO[st], &tdo, &sm.qd_full[st], h * D, qt);
+        tma_load_2d(sm.dO[st] + QHALF, &tdo, &sm.qd_full[st], h * D + 64, qt);
+      }
+      __syncwarp();
+      ++issued;
+    }
+    if (!ok && lane == 0) fail(PG_ERR_TIMEOUT);
+    if (leader) {
+      mbar_wait(&sm.kv_full, 0, wait_ns);
+      for (int it = (issued > NSQ ? issued - NSQ : 0); it < issued; ++it)
+        mbar_wait(&sm.qd_full[it % NSQ], (it / NSQ) & 1, wait_ns);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer -------
+    if (elect_one()) {
+      constexpr uint32_t id_s = idesc_bf16(BKV, BQ, 0, 0);     // S^T, dP^T
+      constexpr uint32_t id_g = idesc_bf16(BKV, D, 0, 1);      // dV, dK
+      constexpr uint32_t id_q = idesc_bf16(D, BQ, 1, 1);       // dQ^T
+      const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v);
+      const uint32_t pa = smem_u32(sm.p), dsa = smem_u32(sm.ds);
+      bool ok = mbar_wait(&sm.kv_full, 0, wait_ns);
+      for (int it = 0; ok && it <= n_it; ++it) {
+        if (it < n_it) {
+          const int st = it % NSQ;
+          if (!mbar_wait(&sm.qd_full[st], (it / NSQ) & 1, wait_ns)) { ok = false; break; }
+          if (it > 0 && !mbar_wait(&sm.s_free, (it - 1) & 1, wait_ns)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t qa = smem_u32(sm.q[st]), doa = smem_u32(sm.dO[st]);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ko = (kk >> 2) * KHALF + (kk & 3) * 32;
+            const uint32_t qo = (kk >> 2) * QHALF + (kk & 3) * 32;
+            mma_ss(t_s, sdesc_sw128(ka + ko, 16, 1024), sdesc_sw128(qa + qo, 16, 1024), id_s,
+                   kk != 0);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ko = (kk >> 2) * KHALF + (kk & 3) * 32;
+            const uint32_t qo = (kk >> 2) * QHALF + (kk & 3) * 32;
+            mma_ss(t_dp, sdesc_sw128(va + ko, 16, 1024), sdesc_sw128(doa + qo, 16, 1024), id_s,
+                   kk != 0);
+          }
+          mma_commit(&sm.s_full);
+        }
+        if (it > 0) {
+          const int jp = it - 1, sp = jp % NSQ;
+          if (!mbar_wait(&sm.p_full, jp & 1, wait_ns)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t qa = smem_u32(sm.q[sp]), doa = smem_u32(sm.dO[sp]);
+#pragma unroll
+          for (int kk = 0; kk < BQ / 16; ++kk) {
+            mma_ss(t_dv, sdesc_sw128(pa + kk * 32, 16, 1024),
+                   sdesc_sw128(doa + kk * 2048, QHALF, 1024), id_g, (jp | kk) != 0);
+          }
+#pragma unroll
+          for (int kk = 0; kk < BQ / 16; ++kk) {
+            mma_ss(t_dk, sdesc_sw128(dsa + kk * 32, 16, 1024),
+                   sdesc_sw128(qa + kk * 2048, QHALF, 1024), id_g, (jp | kk) != 0);
+          }
+          mma_commit(&sm.qd_empty[sp]);
+          if (jp > 0 && !mbar_wait(&sm.dq_free, (jp - 1) & 1, wait_ns)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BKV / 16; ++kk) {
+            mma_ss(t_dq, sdesc_sw128(ka + kk * 2048, KHALF, 1024),
+                   sdesc_sw128(dsa + kk * 2048, QHALF, 1024), id_q, kk != 0);
+          }
+          mma_commit(&sm.dq_full);
+          mma_commit(&sm.pds_free);
+        }
+      }
+      if (!ok) fail(PG_ERR_TIMEOUT);
+      mma_commit(&sm.mma_done);
+      mbar_wait(&sm.mma_done, 0, wait_ns);
+    }
+    __syncwarp();
+  } else if (warp < 6) {
+    // ------------------------------------------------------------------ softmax (keys) ----
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int key = tl.k0 + r;
+    const bool kvalid = key < tl.k1;
+    const int keyc = kvalid ? key : tl.k1 - 1;
+    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int st = it % NSQ;
+      const int qt = tl.q_lo + (it % nqt) * BQ;
+      if (!warp_wait(&sm.s_full, it & 1, wait_ns)) { ok = false; break; }
+      if (!warp_wait(&sm.qd_full[st], (it / NSQ) & 1, wait_ns)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sr[64], dr[64];
+      tmem_ld32(t_s + lane_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(t_s + lane_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_ld32(t_dp + lane_addr, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
+      tmem_ld32(t_dp + lane_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&sm.s_free);
+      const bool full = (qt >= tl.k0 + BKV - 1) && (tl.k1 - tl.k0 == BKV) && (tl.k1 <= tl.pe) &&
+                        (qt + BQ <= tl.q_hi);
+      const float* l2 = sm.lse2[st];
+      const float* ds_ = sm.dsum[st];
+      const int32_t* own = sm.own[st];
+      uint32_t pw[32], dw[32];
+#pragma unroll
+      for (int c = 0; c < BQ; c += 2) {
+        float p0, p1;
+        const int t0 = qt + c, t1 = qt + c + 1;
+        const bool v0 = full || (kvalid && t0 < tl.q_hi && keyc <= t0 && keyc >= tl.g0 &&
+                                 (keyc < tl.pe || keyc >= own[c]));
+        const bool v1 = full || (kvalid && t1 < tl.q_hi && keyc <= t1 && keyc >= tl.g0 &&
+                                 (keyc < tl.pe || keyc >= own[c + 1]));
+        p0 = v0 ? fast_exp2(fmaf(__uint_as_float(sr[c]), scale_log2, -l2[c])) : 0.f;
+        p1 = v1 ? fast_exp2(fmaf(__uint_as_float(sr[c + 1]), scale_log2, -l2[c + 1])) : 0.f;
+        const float g0 = p0 * (__uint_as_float(dr[c]) - ds_[c]);
+        const float g1 = p1 * (__uint_as_float(dr[c + 1]) - ds_[c + 1]);
+        pw[c >> 1] = pack_bf16x2(p0, p1);
+        dw[c >> 1] = pack_bf16x2(g0, g1);
+      }
+      // The previous block's gradient products must be done with P^T / dS^T.
+      if (it > 0 && !warp_wait(&sm.pds_free, (it - 1) & 1, wait_ns)) { ok = false; break; }
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint32_t off = sw128_offset(r, ch);
+        *reinterpret_cast<uint4*>(sm.p + off) =
+            make_uint4(pw[4 * ch], pw[4 * ch + 1], pw[4 * ch + 2], pw[4 * ch + 3]);
+        *reinterpret_cast<uint4*>(sm.ds + off) =
+            make_uint4(dw[4 * ch], dw[4 * ch + 1], dw[4 * ch + 2], dw[4 * ch + 3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&sm.p_full);
+    }
+    // Epilogue: dV and scale * dK (inverse-rotated) of this thread's key row.
+    if (ok && warp_wait(&sm.pds_free, (n_it - 1) & 1, wait_ns)) {
+      tc_fence_after();
+      float cs[64], sn[64];
+      if (log2_theta > 0.0) {
+        const double two_pi = 6.283185307179586476925;
+        const double pos = (double)tok[keyc].w;
+#pragma unroll 1
+        for (int k2 = 0; k2 < 64; ++k2) {
+          const double a = pos * exp2(-(2.0 * k2 / D) * log2_theta);
+          const double red = a - two_pi * rint(a / two_pi);
+          sincosf((float)red, &sn[k2], &cs[k2]);
+        }
+      }
+      const size_t off = ((size_t)keyc * Hkv + kh) * D;
+      // dV
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v32[32];
+        tmem_ld32(t_dv + lane_addr + c * 32, v32);
+        tmem_ld_wait();
+        if (kvalid) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(v32[i]), __uint_as_float(v32[i + 1]));
+            w.y = pack_bf16x2(__uint_as_float(v32[i + 2]), __uint_as_float(v32[i + 3]));
+            w.z = pack_bf16x2(__uint_as_float(v32[i + 4]), __uint_as_float(v32[i + 5]));
+            w.w = pack_bf16x2(__uint_as_float(v32[i + 6]), __uint_as_float(v32[i + 7]));
+            *reinterpret_cast<uint4*>(dv + off + c * 32 + i) = w;
+          }
+        }
+      }
+      // dK: columns c and c + 64 form a rotation pair
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        uint32_t a32[32], b32[32];
+        tmem_ld32(t_dk + lane_addr + c * 32, a32);
+        tmem_ld32(t_dk + lane_addr + 64 + c * 32, b32);
+        tmem_ld_wait();
+        float lo[32], hi[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float x1 = __uint_as_float(a32[i]) * scale, x2 = __uint_as_float(b32[i]) * scale;
+          if (log2_theta > 0.0) {
+            const float cc = cs[c * 32 + i], ss = sn[c * 32 + i];
+            lo[i] = x1 * cc + x2 * ss;
+            hi[i] = x2 * cc - x1 * ss;
+          } else {
+            lo[i] = x1;
+            hi[i] = x2;
+          }
+        }
+        if (kvalid) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 w;
+            w.x = pack_bf16x2(lo[i], lo[i + 1]);
+            w.y = pack_bf16x2(lo[i + 2], lo[i + 3]);
+            w.z = pack_bf16x2(lo[i + 4], lo[i + 5]);
+            w.w = pack_bf16x2(lo[i + 6], lo[i + 7]);
+            *reinterpret_cast<uint4*>(dk + off + c * 32 + i) = w;
+            w.x = pack_bf16x2(hi[i], hi[i + 1]);
+            w.y = pack_bf16x2(hi[i + 2], hi[i + 3]);
+            w.z = pack_bf16x2(hi[i + 4], hi[i + 5]);
+            w.w = pack_bf16x2(hi[i + 6], hi[i + 7]);
+            *reinterpret_cast<uint4*>(dk + off + 64 + c * 32 + i) = w;
+          }
+        }
+      }
+    } else {
+      ok = false;
+    }
+    if (!ok) fail(PG_ERR_TIMEOUT);
+  } else {
+    // ------------------------------------------------------------------ dQ drain ---------
+    const int quarter = warp & 3;
+    const int dd = quarter * 32 + lane;            // head-dim index = TMEM lane
+    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int h = kh * rep + it / nqt;
+      const int qt = tl.q_lo + (it % nqt) * BQ;
+      if (!warp_wait(&sm.dq_full, it & 1, wait_ns)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t g[64];
+      tmem_ld32(t_dq + lane_addr, *reinterpret_cast<uint32_t(*)[32]>(&g[0]));
+      tmem_ld32(t_dq + lane_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&g[32]));
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&sm.dq_free);
+      const int cn = min(BQ, tl.q_hi - qt);
+      float* dst = dq_acc + ((size_t)qt * Hq + h) * D + dd;
+#pragma unroll 4
+      for (int c = 0; c < cn; ++c) red_add(dst + (size_t)c * Hq * D, __uint_as_float(g[c]) * scale);
+    }
+    if (!ok) fail(PG_ERR_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+bool bwd_sm100_supported(const AttnArgs& a) { return a.dtype == PG_BF16 && a.d == 128; }
+
+pg_status launch_bwd_sm100(const AttnArgs& a, const void* q, const void* k, const void* v,
+                           const void* dO, const float* lse, const float* Dbuf, float* dq_acc,
+                           void* dk, void* dv) {
+  const pg_layout* L = a.layout;
+  const int64_t T = L->total_tokens;
+  CUtensorMap tq, tk, tv, tdo;
+  pg_status st = make_tmap_2d_bf16(&tq, q, (uint64_t)a.Hq * D, T, (uint64_t)a.Hq * D * 2, 64, BQ);
+  if (st == PG_OK)
+    st = make_tmap_2d_bf16(&tdo, dO, (uint64_t)a.Hq * D, T, (uint64_t)a.Hq * D * 2, 64, BQ);
+  if (st == PG_OK)
+    st = make_tmap_2d_bf16(&tk, k, (uint64_t)a.Hkv * D, T, (uint64_t)a.Hkv * D * 2, 64, BKV);
+  if (st == PG_OK)
+    st = make_tmap_2d_bf16(&tv, v, (uint64_t)a.Hkv * D, T, (uint64_t)a.Hkv * D * 2, 64, BKV);
+  if (st != PG_OK) return st;
+  const size_t smem = sizeof(BwdSmem) + 1024;
+  st = cuda_check(cudaFuncSetAttribute(attn_bwd_sm100_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+                  "bwd smem attribute");
+  if (st != PG_OK) return st;
+  const double l2t = a.theta > 0.f ? log2((double)a.theta) : 0.0;
+  prof_begin(PG_KERNEL_BWD_DKDV, a.stream);
+  attn_bwd_sm100_kernel<<<(unsigned)(L->n_tiles[BWD128] * a.Hkv), NTHREADS, smem, a.stream>>>(
+      tq, tk, tv, tdo, lse, Dbuf, dq_acc, static_cast<__nv_bfloat16*>(dk),
+      static_cast<__nv_bfloat16*>(dv), tokens(L), tiles<BwdTile>(L, BWD128), a.Hq, a.Hkv, (int)T,
+      a.scale * kLog2e, a.scale, l2t, 2000000000ull);
+  prof_end(PG_KERNEL_BWD_DKDV, a.stream);
+  return cuda_check(cudaGetLastError(), "bwd sm100 launch");
+}
+
+pg_status read_status_bwd_sm100(bool clear, int32_t* code) {
+  int32_t v = 0;
+  pg_status st = cuda_check(cudaMemcpyFromSymbol(&v, s_status_bwd, sizeof(v)), "read status");
+  if (st != PG_OK) return st;
+  if (clear && v != 0) {
+    int32_t z = 0;
+    st = cuda_check(cudaMemcpyToSymbol(s_status_bwd, &z, sizeof(z)), "clear status");
+    if (st != PG_OK) return st;
+  }
+  if (*code == 0) *code = v;
+  return PG_OK;
+}
+
+}  // namespace pg

@@ -1,0 +1,383 @@
+// Grouped-attention forward on the 5th-generation tensor cores (bf16, head_dim 128).
+//
+// One CTA owns 128 packed query rows of one group and one query head (a FwdTile), and streams the
+// key/value tiles its rows can see: the group's prefix [g0, p_end) -- every response row sees all
+// of it, prefix rows causally -- then the responses' part [s_lo, s_hi) (Pith review of Prefix
+// Grouper, "What carries the argument": prefix self-attention plus suffix attention over the
+// prefix and the row's own response).  All CTAs of a group read the same prefix K/V tiles, which
+// stay resident in L2 across the group's query tiles and heads.
+//
+// Warp roles (192 threads):
+//   warp 0      TMA producer: Q once, then K and V tiles into a 2-stage ring (128-byte swizzle)
+//   warp 1      TMEM allocation and the MMA issuer (one elected thread):
+//                 S = Q K^T   (M 128 x N 128 keys x K 128, fp32 in TMEM columns [0, 128))
+//                 O += P V    (M 128 x N 128 dims x K 128 keys, fp32 in TMEM columns [128, 256))
+//   warps 2..5  softmax, one thread per query row (TMEM lane = row): S from TMEM to registers,
+//               masking, online max / sum in fp32 (exp2 with the scale folded in), P rounded to
+//               bf16 into shared memory (the A operand of P V), O rescaled in TMEM when the
+//               running max grows by more than 2^8, and the final O / l, LSE epilogue.
+// The MMA thread issues S_{j+1} as soon as the softmax has read S_j, so the tensor core computes
+// the next scores while the softmax exponentiates the current ones.
+//
+// Every mbarrier wait is bounded (PG_ERR_TIMEOUT in the status word, then an orderly exit: copies
+// in flight are awaited, MMAs committed, TMEM freed).
+#include <math.h>
+
+#include "pg_internal.h"
+#include "pg_sm100.cuh"
+#include "pg_tmap.h"
+
+namespace pg {
+
+using namespace sm100;
+
+namespace {
+
+constexpr int D = 128;          // head_dim
+constexpr int BM = 128;         // query rows per CTA
+constexpr int BN = 128;         // keys per tile
+constexpr int NS = 2;           // K/V pipeline stages
+constexpr uint32_t HALF = BM * 64 * 2;     // one 64-column SW128 half tile: 16 KiB
+constexpr uint32_t TILE = 2 * HALF;        // a 128 x 128 bf16 tile: 32 KiB
+constexpr int NTHREADS = 192;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+__device__ int s_status_fwd = 0;
+
+struct FwdSmem {
+  uint8_t q[TILE];
+  uint8_t k[NS][TILE];
+  uint8_t v[NS][TILE];
+  uint8_t p[TILE];
+  uint64_t q_full;
+  uint64_t k_full[NS], v_full[NS], kv_empty[NS];
+  uint64_t s_full, s_free, p_full, o_ready, mma_done;
+  uint32_t tmem;
+};
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void fail(int code) { atomicCAS(&s_status_fwd, 0, code); }
+
+// Key tile j of a CTA: tiles of the prefix range first, then of the responses' range.
+struct KeyTiles {
+  int g0, p_end, s_lo, s_hi, n_a, n;
+  __device__ KeyTiles(const FwdTile& t) {
+    g0 = t.g0;
+    p_end = t.p_end;
+    s_lo = t.s_lo;
+    s_hi = t.s_hi;
+    n_a = (p_end - g0 + BN - 1) / BN;
+    n = n_a + (s_hi - s_lo + BN - 1) / BN;
+  }
+  __device__ void get(int j, int& kt, int& hi) const {
+    if (j < n_a) {
+      kt = g0 + j * BN;
+      hi = p_end;
+    } else {
+      kt = s_lo + (j - n_a) * BN;
+      hi = s_hi;
+    }
+  }
+};
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                      const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ o,
+                      float* __restrict__ lse, const int4* __restrict__ tok,
+                      const FwdTile* __restrict__ tiles, int Hq, int Hkv, int Ttot,
+                      float scale_log2, uint64_t wait_ns, uint32_t debug) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  FwdSmem& sm = *reinterpret_cast<FwdSmem*>(base);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile_id = blockIdx.x / Hq, h = blockIdx.x % Hq;
+  const int kh = h / (Hq / Hkv);
+  const FwdTile tl = tiles[tile_id];
+  if (tl.q0 < 0 || tl.q1 > Ttot || tl.q0 >= tl.q1 || tl.q1 - tl.q0 > BM || tl.g0 < 0 ||
+      tl.s_hi > Ttot) {
+    if (threadIdx.x == 0) fail(PG_ERR_DEVICE);
+    return;
+  }
+  const KeyTiles kts(tl);
+  const int n = kts.n;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sm.q_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.kv_empty[s], 1);
+    }
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.s_free, 128);
+    mbar_init(&sm.p_full, 128);
+    mbar_init(&sm.o_ready, 1);
+    mbar_init(&sm.mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem;
+  const uint32_t tmem_s = tmem, tmem_o = tmem + 128;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer -----
+    if (elect_one()) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      const int xq = h * D, xk = kh * D;
+      mbar_expect_tx(&sm.q_full, TILE);
+      tma_load_2d(sm.q, &tq, &sm.q_full, xq, tl.q0);
+      tma_load_2d(sm.q + HALF, &tq, &sm.q_full, xq + 64, tl.q0);
+      int issued = 0;
+      for (int j = 0; j < n; ++j) {
+        const int s = j % NS;
+        const uint32_t ph = (j / NS) & 1;
+        if (!mbar_wait(&sm.kv_empty[s], ph ^ 1, wait_ns)) {
+          fail(PG_ERR_TIMEOUT);
+          break;
+        }
+        int kt, hi;
+        kts.get(j, kt, hi);
+        mbar_expect_tx(&sm.k_full[s], TILE);
+        tma_load_2d(sm.k[s], &tk, &sm.k_full[s], xk, kt);
+        tma_load_2d(sm.k[s] + HALF, &tk, &sm.k_full[s], xk + 64, kt);
+        mbar_expect_tx(&sm.v_full[s], TILE);
+        tma_load_2d(sm.v[s], &tv, &sm.v_full[s], xk, kt);
+        tma_load_2d(sm.v[s] + HALF, &tv, &sm.v_full[s], xk + 64, kt);
+        ++issued;
+      }
+      // Leave no copy in flight: the last stages' loads must have landed before exit.
+      mbar_wait(&sm.q_full, 0, wait_ns);
+      for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j) {
+        mbar_wait(&sm.k_full[j % NS], (j / NS) & 1, wait_ns);
+        mbar_wait(&sm.v_full[j % NS], (j / NS) & 1, wait_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer -------
+    if (elect_one()) {
+      constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
+      constexpr uint32_t idesc_pv = idesc_bf16(BM, D, 0, 1);
+      const uint32_t q0a = smem_u32(sm.q), pa = smem_u32(sm.p);
+      bool ok = mbar_wait(&sm.q_full, 0, wait_ns);
+      for (int j = 0; ok && j <= n; ++j) {
+        if (j < n) {
+          const int s = j % NS;
+          if (!mbar_wait(&sm.k_full[s], (j / NS) & 1, wait_ns)) { ok = false; break; }
+          if (j > 0 && !mbar_wait(&sm.s_free, (j - 1) & 1, wait_ns)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t ka = smem_u32(sm.k[s]);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
+            mma_ss(tmem_s, sdesc_sw128(q0a + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                   idesc_s, kk != 0);
+          }
+          mma_commit(&sm.s_full);
+        }
+        if (j > 0) {
+          const int jp = j - 1, s = jp % NS;
+          if (!mbar_wait(&sm.p_full, jp & 1, wait_ns)) { ok = false; break; }
+          if (!mbar_wait(&sm.v_full[s], (jp / NS) & 1, wait_ns)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t va = smem_u32(sm.v[s]);
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint32_t poff = (kk >> 2) * HALF + (kk & 3) * 32;
+            mma_ss(tmem_o, sdesc_sw128(pa + poff, 16, 1024),
+                   sdesc_sw128(va + kk * 2048, HALF, 1024), idesc_pv, (jp | kk) != 0);
+          }
+          mma_commit(&sm.kv_empty[s]);
+          mma_commit(&sm.o_ready);
+        }
+      }
+      if (!ok) fail(PG_ERR_TIMEOUT);
+      // Every MMA issued above completes before TMEM is released.
+      mma_commit(&sm.mma_done);
+      mbar_wait(&sm.mma_done, 0, wait_ns);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ softmax ----------
+    const int quarter = warp & 3;                 // TMEM lanes this warp may access
+    const int r = quarter * 32 + lane;            // query row within the tile
+    const int row = tl.q0 + r;
+    const bool valid = row < tl.q1;
+    const int rowc = valid ? row : tl.q1 - 1;
+    const int4 ti = tok[rowc];                    // {g0, pe, own_lo, pos}
+    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    uint8_t* prow = sm.p;
+    for (int j = 0; j < n; ++j) {
+      int kt, hi;
+      kts.get(j, kt, hi);
+      if (!warp_wait(&sm.s_full, j & 1, wait_ns)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sr[128];
+      tmem_ld32(tmem_s + lane_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(tmem_s + lane_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_ld32(tmem_s + lane_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+      tmem_ld32(tmem_s + lane_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&sm.s_free);
+      // Scores in log2 units; mask where the tile is not entirely visible to every row.
+      const bool full_tile = (j < kts.n_a) && (kt + BN <= hi) && (kt + BN - 1 <= tl.q0);
+      float mx = -INFINITY;
+      if (full_tile) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const float x = __uint_as_float(sr[c]) * scale_log2;
+          sr[c] = __float_as_uint(x);
+          mx = fmaxf(mx, x);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const int s = kt + c;
+          const bool vis = s < hi && s <= rowc && s >= ti.x && (s < ti.y || s >= ti.z);
+          const float x = vis ? __uint_as_float(sr[c]) * scale_log2 : -INFINITY;
+          sr[c] = __float_as_uint(x);
+          mx = fmaxf(mx, x);
+        }
+      }
+      const float m_new = fmaxf(m_used, mx);
+      const bool rescale = m_new > m_used + kRescaleThreshold;   // false when m_new is -inf
+      float corr = 1.f;
+      if (rescale) {
+        corr = (m_used == -INFINITY) ? 0.f : fast_exp2(m_used - m_new);
+        m_used = m_new;
+        l *= corr;
+      }
+      const float mref = (m_used == -INFINITY) ? 0.f : m_used;
+      // P V of the previous tile must be complete before O is rescaled or P is overwritten.
+      if (j > 0) {
+        if (!warp_wait(&sm.o_ready, (j - 1) & 1, wait_ns)) { ok = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t orr[32];
+            tmem_ld32(tmem_o + lane_addr + c * 32, orr);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * corr);
+            tmem_st32(tmem_o + lane_addr + c * 32, orr);
+          }
+          tmem_st_wait();
+        }
+      }
+      // P = exp2(s - m), rounded to bf16, written as the SW128 K-major A operand.
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch) {
+        uint32_t w4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = fast_exp2(__uint_as_float(sr[ch * 8 + 2 * e]) - mref);
+          const float p1 = fast_exp2(__uint_as_float(sr[ch * 8 + 2 * e + 1]) - mref);
+          l += p0 + p1;
+          w4[e] = pack_bf16x2(p0, p1);
+        }
+        const uint32_t off = (ch >> 3) * HALF + sw128_offset(r, ch & 7);
+        *reinterpret_cast<uint4*>(prow + off) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      }
+      if (debug & PG_DEBUG_WITHHOLD_P) continue;   // test hook: never signal P (bounded waits)
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&sm.p_full);
+    }
+    // Epilogue: O / l and the natural-log LSE.
+    if (ok && n > 0 && warp_wait(&sm.o_ready, (n - 1) & 1, wait_ns)) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+      __nv_bfloat16* orow = o + ((size_t)rowc * Hq + h) * D;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t orr[32];
+        tmem_ld32(tmem_o + lane_addr + c * 32, orr);
+        tmem_ld_wait();
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(orr[i]) * inv, __uint_as_float(orr[i + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(orr[i + 2]) * inv, __uint_as_float(orr[i + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(orr[i + 4]) * inv, __uint_as_float(orr[i + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(orr[i + 6]) * inv, __uint_as_float(orr[i + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + c * 32 + i) = w;
+          }
+        }
+      }
+      if (valid) lse[(size_t)h * Ttot + row] = (m_used + log2f(l)) * kLn2;
+    } else if (n > 0) {
+      ok = false;
+    }
+    if (!ok) fail(PG_ERR_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+}  // namespace
+
+bool fwd_sm100_supported(const AttnArgs& a) { return a.dtype == PG_BF16 && a.d == 128; }
+
+pg_status launch_fwd_sm100(const AttnArgs& a, const void* q, const void* k, const void* v, void* o,
+                           float* lse) {
+  const pg_layout* L = a.layout;
+  const int64_t T = L->total_tokens;
+  CUtensorMap tq, tk, tv;
+  pg_status st = make_tmap_2d_bf16(&tq, q, (uint64_t)a.Hq * D, T, (uint64_t)a.Hq * D * 2, 64, BM);
+  if (st == PG_OK)
+    st = make_tmap_2d_bf16(&tk, k, (uint64_t)a.Hkv * D, T, (uint64_t)a.Hkv * D * 2, 64, BN);
+  if (st == PG_OK)
+    st = make_tmap_2d_bf16(&tv, v, (uint64_t)a.Hkv * D, T, (uint64_t)a.Hkv * D * 2, 64, BN);
+  if (st != PG_OK) return st;
+  const size_t smem = sizeof(FwdSmem) + 1024;
+  st = cuda_check(cudaFuncSetAttribute(attn_fwd_sm100_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+                  "fwd smem attribute");
+  if (st != PG_OK) return st;
+  const uint64_t wait_ns = (a.debug & PG_DEBUG_WITHHOLD_P) ? 50000000ull : 2000000000ull;
+  prof_begin(PG_KERNEL_ATTN_FWD, a.stream);
+  attn_fwd_sm100_kernel<<<(unsigned)(L->n_tiles[FWD128] * a.Hq), NTHREADS, smem, a.stream>>>(
+      tq, tk, tv, static_cast<__nv_bfloat16*>(o), lse, tokens(L), tiles<FwdTile>(L, FWD128),
+      a.Hq, a.Hkv, (int)T, a.scale * kLog2e, wait_ns, a.debug);
+  prof_end(PG_KERNEL_ATTN_FWD, a.stream);
+  return cuda_check(cudaGetLastError(), "fwd sm100 launch");
+}
+
+pg_status read_status_fwd_sm100(bool clear, int32_t* code) {
+  int32_t v = 0;
+  pg_status st = cuda_check(cudaMemcpyFromSymbol(&v, s_status_fwd, sizeof(v)), "read status");
+  if (st != PG_OK) return st;
+  if (clear && v != 0) {
+    int32_t z = 0;
+    st = cuda_check(cudaMemcpyToSymbol(s_status_fwd, &z, sizeof(z)), "clear status");
+    if (st != PG_OK) return st;
+  }
+  if (*code == 0) *code = v;
+  return PG_OK;
+}
+
+}  // namespace pg

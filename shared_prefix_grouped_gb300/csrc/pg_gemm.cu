@@ -1,0 +1,216 @@
+// BF16 GEMM on the 5th-generation tensor cores: TMA-staged operands (128-byte swizzle), tcgen05.mma
+// issued by one thread, fp32 accumulator in TMEM, read back with tcgen05.ld for the epilogue.
+//
+//   C[m, n] = sum_k A(m, k) * B(n, k)
+//   A(m, k) = A[m * lda + k] (K-major)  or  A[k * lda + m] (MN-major, "transposed")
+//   B(n, k) = B[n * ldb + k] (K-major)  or  B[k * ldb + n] (MN-major)
+//
+// One CTA computes a 128 x 128 tile of C; 4 warps: warp 0 issues TMA loads into a 4-stage ring,
+// warp 1 issues the MMAs (K = 16 each, 4 per 64-wide K block), then all four warps drain TMEM
+// (warp w owns accumulator lanes / C rows 32w .. 32w + 31).
+#include "pg_internal.h"
+#include "pg_sm100.cuh"
+#include "pg_tmap.h"
+
+namespace pg {
+
+using namespace sm100;
+
+namespace {
+
+constexpr int BM = 128, BN = 128, BK = 64, STAGES = 4;
+constexpr uint32_t TILE_BYTES = BM * BK * 2;   // 16 KiB per operand per stage
+constexpr uint64_t WAIT_NS = 2000000000ull;    // 2 s bound on every wait
+
+__device__ int s_status_gemm = 0;
+
+struct GemmSmem {
+  uint8_t a[STAGES][TILE_BYTES];
+  uint8_t b[STAGES][TILE_BYTES];
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t done;
+  uint32_t tmem;
+};
+
+template <int A_MN, int B_MN, typename OutT>
+__global__ void __launch_bounds__(128, 1)
+gemm_bf16_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
+                 OutT* __restrict__ C, int M, int N, int K, long long ldc) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  GemmSmem& sm = *reinterpret_cast<GemmSmem*>(base);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  const int nk = (K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    mbar_init(&sm.done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&sm.tmem, BN);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem;
+  bool ok = true;
+  int issued = 0;   // TMA stages issued by the producer
+
+  if (warp == 0) {
+    if (elect_one()) {
+      prefetch_tmap(&ta);
+      prefetch_tmap(&tb);
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % STAGES;
+        const uint32_t ph = (kb / STAGES) & 1;
+        if (!mbar_wait(&sm.empty[s], ph ^ 1, WAIT_NS)) { ok = false; break; }
+        mbar_expect_tx(&sm.full[s], 2 * TILE_BYTES);
+        if (!A_MN) {
+          tma_load_2d(sm.a[s], &ta, &sm.full[s], kb * BK, m0);
+        } else {
+          tma_load_2d(sm.a[s], &ta, &sm.full[s], m0, kb * BK);
+          tma_load_2d(sm.a[s] + TILE_BYTES / 2, &ta, &sm.full[s], m0 + 64, kb * BK);
+        }
+        if (!B_MN) {
+          tma_load_2d(sm.b[s], &tb, &sm.full[s], kb * BK, n0);
+        } else {
+          tma_load_2d(sm.b[s], &tb, &sm.full[s], n0, kb * BK);
+          tma_load_2d(sm.b[s] + TILE_BYTES / 2, &tb, &sm.full[s], n0 + 64, kb * BK);
+        }
+        ++issued;
+      }
+      // Do not leave the kernel with copies in flight: wait (bounded) for the last stages.
+      for (int kb = (issued > STAGES ? issued - STAGES : 0); kb < issued; ++kb)
+        mbar_wait(&sm.full[kb % STAGES], (kb / STAGES) & 1, WAIT_NS);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (elect_one()) {
+      constexpr uint32_t idesc = idesc_bf16(BM, BN, A_MN, B_MN);
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % STAGES;
+        if (!mbar_wait(&sm.full[s], (kb / STAGES) & 1, WAIT_NS)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(sm.a[s]), b0 = smem_u32(sm.b[s]);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint64_t ad = A_MN ? sdesc_sw128(a0 + kk * 2048, TILE_BYTES / 2, 1024)
+                                   : sdesc_sw128(a0 + kk * 32, 16, 1024);
+          const uint64_t bd = B_MN ? sdesc_sw128(b0 + kk * 2048, TILE_BYTES / 2, 1024)
+                                   : sdesc_sw128(b0 + kk * 32, 16, 1024);
+          mma_ss(tmem, ad, bd, idesc, (kb | kk) != 0);
+        }
+        mma_commit(&sm.empty[s]);
+      }
+      mma_commit(&sm.done);
+    }
+    __syncwarp();
+  }
+
+  // Epilogue: every warp drains its 32 accumulator lanes.
+  if (!mbar_wait(&sm.done, 0, WAIT_NS)) ok = false;
+  tc_fence_after();
+  const int row = m0 + warp * 32 + lane;
+  if (ok) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c * 32, r);
+      tmem_ld_wait();
+      const int col0 = n0 + c * 32;
+      if (row < M) {
+        OutT* dst = C + (long long)row * ldc + col0;
+        for (int j = 0; j < 32; ++j) {
+          if (col0 + j < N) {
+            const float x = __uint_as_float(r[j]);
+            if constexpr (sizeof(OutT) == 4) dst[j] = x;
+            else dst[j] = __float2bfloat16_rn(x);
+          }
+        }
+      }
+    }
+  }
+  if (!ok) atomicCAS(&s_status_gemm, 0, (int)PG_ERR_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, BN);
+  }
+}
+
+template <int A_MN, int B_MN, typename OutT>
+pg_status launch(const CUtensorMap& ta, const CUtensorMap& tb, void* C, int M, int N, int K,
+                 long long ldc, cudaStream_t s) {
+  auto kern = gemm_bf16_kernel<A_MN, B_MN, OutT>;
+  const size_t smem = sizeof(GemmSmem) + 1024;
+  pg_status st = cuda_check(
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+      "gemm smem attribute");
+  if (st != PG_OK) return st;
+  dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
+  prof_begin(PG_KERNEL_GEMM, s);
+  kern<<<grid, 128, smem, s>>>(ta, tb, static_cast<OutT*>(C), M, N, K, ldc);
+  prof_end(PG_KERNEL_GEMM, s);
+  return cuda_check(cudaGetLastError(), "gemm launch");
+}
+
+}  // namespace
+
+pg_status read_status_gemm(bool clear, int32_t* code) {
+  int32_t v = 0;
+  pg_status st = cuda_check(cudaMemcpyFromSymbol(&v, s_status_gemm, sizeof(v)), "read status");
+  if (st != PG_OK) return st;
+  if (clear && v != 0) {
+    int32_t z = 0;
+    st = cuda_check(cudaMemcpyToSymbol(s_status_gemm, &z, sizeof(z)), "clear status");
+    if (st != PG_OK) return st;
+  }
+  if (*code == 0) *code = v;
+  return PG_OK;
+}
+
+}  // namespace pg
+
+using namespace pg;
+
+extern "C" pg_status pg_gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, int32_t a_mn,
+                                  int64_t lda, const void* B, int32_t b_mn, int64_t ldb, void* C,
+                                  pg_dtype c_dtype, int64_t ldc, pg_stream_t stream) {
+  if (M < 1 || N < 1 || K < 1 || M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 31) ||
+      !A || !B || !C || (a_mn != 0 && a_mn != 1) || (b_mn != 0 && b_mn != 1) ||
+      (c_dtype != PG_F32 && c_dtype != PG_BF16)) {
+    set_error("pg_gemm_bf16: bad sizes, NULL pointer or bad layout flag");
+    return PG_ERR_INVALID_ARG;
+  }
+  if (lda % 8 || ldb % 8 || lda < (a_mn ? M : K) || ldb < (b_mn ? N : K) || ldc < N) {
+    set_error("pg_gemm_bf16: leading dimensions must cover the rows and be multiples of 8");
+    return PG_ERR_INVALID_ARG;
+  }
+  CUtensorMap ta, tb;
+  pg_status st = a_mn ? make_tmap_2d_bf16(&ta, A, M, K, lda * 2, 64, 64)
+                      : make_tmap_2d_bf16(&ta, A, K, M, lda * 2, 64, 128);
+  if (st != PG_OK) return st;
+  st = b_mn ? make_tmap_2d_bf16(&tb, B, N, K, ldb * 2, 64, 64)
+            : make_tmap_2d_bf16(&tb, B, K, N, ldb * 2, 64, 128);
+  if (st != PG_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int m = (int)M, n = (int)N, k = (int)K;
+  if (c_dtype == PG_F32) {
+    if (!a_mn && !b_mn) return launch<0, 0, float>(ta, tb, C, m, n, k, ldc, s);
+    if (!a_mn && b_mn) return launch<0, 1, float>(ta, tb, C, m, n, k, ldc, s);
+    if (a_mn && !b_mn) return launch<1, 0, float>(ta, tb, C, m, n, k, ldc, s);
+    return launch<1, 1, float>(ta, tb, C, m, n, k, ldc, s);
+  }
+  if (!a_mn && !b_mn) return launch<0, 0, __nv_bfloat16>(ta, tb, C, m, n, k, ldc, s);
+  if (!a_mn && b_mn) return launch<0, 1, __nv_bfloat16>(ta, tb, C, m, n, k, ldc, s);
+  if (a_mn && !b_mn) return launch<1, 0, __nv_bfloat16>(ta, tb, C, m, n, k, ldc, s);
+  return launch<1, 1, __nv_bfloat16>(ta, tb, C, m, n, k, ldc, s);
+}

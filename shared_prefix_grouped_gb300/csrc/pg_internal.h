@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "../../include/pg_grouped_attn.h"
+#include "../../include/pg_layer.h"
 
 namespace pg {
 
@@ -69,6 +70,19 @@ inline void prof_end(pg_kernel kid, cudaStream_t s) {
 }
 // Reads (and optionally clears) the device status words of every kernel file; first error wins.
 pg_status read_kernel_status(bool clear, int32_t* code);
+pg_status read_status_simt(bool clear, int32_t* code);
+pg_status read_status_gemm(bool clear, int32_t* code);
+pg_status read_status_fwd_sm100(bool clear, int32_t* code);
+pg_status read_status_bwd_sm100(bool clear, int32_t* code);
+
+// Tensor-core kernels (pg_attn_*_sm100.cu).
+bool fwd_sm100_supported(const AttnArgs& a);
+pg_status launch_fwd_sm100(const AttnArgs& a, const void* q, const void* k, const void* v, void* o,
+                           float* lse);
+bool bwd_sm100_supported(const AttnArgs& a);
+pg_status launch_bwd_sm100(const AttnArgs& a, const void* q, const void* k, const void* v,
+                           const void* dO, const float* lse, const float* Dbuf, float* dq_acc,
+                           void* dk, void* dv);
 pg_status cuda_check(cudaError_t e, const char* what);
 
 // SIMT kernels (pg_simt.cu).
@@ -79,6 +93,7 @@ pg_status launch_fwd_simt(const AttnArgs& a, const void* q, const void* k, const
 pg_status launch_bwd_simt(const AttnArgs& a, const void* q, const void* k, const void* v,
                           const void* o, const float* lse, const void* dO, float* Dbuf,
                           float* dq_acc, float* dk_acc, void* dv);
-pg_status launch_bwd_preprocess(const AttnArgs& a, const void* o, const void* dO, float* Dbuf);
+pg_status launch_bwd_preprocess(const AttnArgs& a, const void* o, const void* dO, float* Dbuf,
+                                float* dq_acc);
 
 }  // namespace pg

@@ -224,7 +224,8 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
 // ---------------------------------------------------------------------------------------------
 template <typename T>
 __global__ void bwd_pre_kernel(const T* __restrict__ o, const T* __restrict__ dO,
-                               float* __restrict__ Dbuf, int Hq, int D, int Ttot) {
+                               float* __restrict__ Dbuf, float* __restrict__ dq_acc, int Hq, int D,
+                               int Ttot) {
   const int lane = threadIdx.x & 31;
   const size_t warp = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (warp >= (size_t)Ttot * Hq) return;
@@ -234,6 +235,7 @@ __global__ void bwd_pre_kernel(const T* __restrict__ o, const T* __restrict__ dO
   for (int c = lane * 4; c < D; c += 128) {
     float4 a = Vec<T>::load4(o + base + c), b = Vec<T>::load4(dO + base + c);
     acc += dot4(a, b);
+    *reinterpret_cast<float4*>(dq_acc + base + c) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -527,18 +529,19 @@ pg_status launch_fwd_simt(const AttnArgs& a, const void* q, const void* k, const
                    : fwd_simt_t<__nv_bfloat16, 128>(a, q, k, v, o, lse);
 }
 
-pg_status launch_bwd_preprocess(const AttnArgs& a, const void* o, const void* dO, float* Dbuf) {
+pg_status launch_bwd_preprocess(const AttnArgs& a, const void* o, const void* dO, float* Dbuf,
+                                float* dq_acc) {
   const int T = (int)a.layout->total_tokens;
   const size_t warps = (size_t)T * a.Hq;
   const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
   prof_begin(PG_KERNEL_BWD_PREPROCESS, a.stream);
   if (a.dtype == PG_F32)
     bwd_pre_kernel<float><<<blocks, 256, 0, a.stream>>>(
-        static_cast<const float*>(o), static_cast<const float*>(dO), Dbuf, a.Hq, a.d, T);
+        static_cast<const float*>(o), static_cast<const float*>(dO), Dbuf, dq_acc, a.Hq, a.d, T);
   else
     bwd_pre_kernel<__nv_bfloat16><<<blocks, 256, 0, a.stream>>>(
-        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), Dbuf, a.Hq,
-        a.d, T);
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), Dbuf, dq_acc,
+        a.Hq, a.d, T);
   prof_end(PG_KERNEL_BWD_PREPROCESS, a.stream);
   return cuda_check(cudaGetLastError(), "bwd preprocess launch");
 }
@@ -568,9 +571,5 @@ pg_status read_status_simt(bool clear, int32_t* code) {
   return PG_OK;
 }
 
-pg_status read_kernel_status(bool clear, int32_t* code) {
-  *code = 0;
-  return read_status_simt(clear, code);
-}
 
 }  // namespace pg

@@ -1,0 +1,14 @@
+#pragma once
+#include <cuda.h>
+
+#include "pg_internal.h"
+
+namespace pg {
+
+// 2-D bf16 tensor map with 128-byte swizzle: `inner` contiguous elements per row, `outer` rows
+// `row_stride_bytes` apart; boxes of box_inner (<= 64) x box_outer elements; out-of-range
+// elements of a box read as zero.
+pg_status make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                            uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+
+}  // namespace pg
