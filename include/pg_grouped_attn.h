@@ -191,6 +191,34 @@ typedef struct pg_profile {
  * must outlive its installation. */
 pg_status pg_set_profile(pg_profile* profile);
 
+/* Size of the built-in scratch of pg_grouped_attn_fwd_noalloc: 16 MiB per GPU. */
+#define PG_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * pg_grouped_attn_fwd without a workspace argument, for callers that cannot allocate device
+ * memory: for example a host program that owns a fixed device-memory plan and hands this library
+ * only the tensors it already holds, or code running at a point where a cudaMalloc would
+ * synchronise the device or is not permitted.  The paper has no counterpart; this is a
+ * deployment convenience.
+ *
+ * Scratch (the RoPE-rotated Q and K the kernel reads) comes from a 16 MiB array
+ * (PG_NOALLOC_SCRATCH_BYTES) that the library reserves statically on every GPU it is loaded on,
+ * for the life of the process.  A problem whose scratch would exceed it (pg_workspace_size(...,
+ * phase 0) > PG_NOALLOC_SCRATCH_BYTES) is rejected with PG_ERR_INVALID_ARG before anything runs;
+ * use pg_grouped_attn_fwd with a caller workspace for it.  Nothing here calls cudaMalloc,
+ * cudaFree or any allocating routine.
+ *
+ * The first call on each device looks up the array's device address (with that device current)
+ * and caches it; make that first call before any stream capture.  Every call shares the one array
+ * and leaves its contents behind (no part of it needs to start at zero): calls that can overlap on
+ * the GPU -- on different streams without ordering between them -- race on it and must not be
+ * issued.  Arguments, results and errors are otherwise those of pg_grouped_attn_fwd.
+ */
+pg_status pg_grouped_attn_fwd_noalloc(const pg_layout* layout, pg_dtype dtype, int32_t heads_q,
+                                      int32_t heads_kv, int32_t head_dim, const void* q,
+                                      const void* k, const void* v, void* o, float* lse,
+                                      const pg_opts* opts, pg_stream_t stream);
+
 /*
  * Read (synchronously, on the current device) the status word kernels set when a bounded wait
  * runs out or a kernel-side check fails; PG_OK if none did.  clear != 0 resets it afterwards.

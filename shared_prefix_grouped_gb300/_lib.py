@@ -70,6 +70,9 @@ SIGNATURES = {
     "pg_grouped_attn_bwd": (C.c_int, [C.POINTER(PgLayout), C.c_int, C.c_int32, C.c_int32,
                                       C.c_int32, VP, VP, VP, VP, VP, VP, VP, VP, VP,
                                       C.POINTER(PgOpts), VP, C.c_size_t, VP]),
+    "pg_grouped_attn_fwd_noalloc": (C.c_int, [C.POINTER(PgLayout), C.c_int, C.c_int32,
+                                              C.c_int32, C.c_int32, VP, VP, VP, VP, VP,
+                                              C.POINTER(PgOpts), VP]),
     "pg_set_profile": (C.c_int, [C.POINTER(PgProfile)]),
     "pg_gemm_bf16": (C.c_int, [C.c_int64, C.c_int64, C.c_int64, VP, C.c_int32, C.c_int64, VP,
                                C.c_int32, C.c_int64, VP, C.c_int, C.c_int64, VP]),
