@@ -217,7 +217,7 @@ static void fill_layout(int32_t B, const Plan& p, const int32_t* pos, const void
 // ---------------------------------------------------------------------------------------------
 
 struct WsPlan {
-  size_t q_rot = 0, k_rot = 0, Dbuf = 0, dq_acc = 0, dk_acc = 0, total = 0;
+  size_t q_rot = 0, k_rot = 0, rope_tab = 0, Dbuf = 0, lse2 = 0, dq_acc = 0, dk_acc = 0, total = 0;
 };
 
 static size_t esize(pg_dtype dt) { return dt == PG_F32 ? 4 : 2; }
@@ -233,13 +233,16 @@ static WsPlan ws_plan(const pg_layout* L, pg_dtype dt, int Hq, int Hkv, int d, b
     return o;
   };
   // Offset 0 is a valid slot; record "absent" as SIZE_MAX.
-  w.q_rot = w.k_rot = w.Dbuf = w.dq_acc = w.dk_acc = SIZE_MAX;
+  w.q_rot = w.k_rot = w.rope_tab = w.Dbuf = w.lse2 = w.dq_acc = w.dk_acc = SIZE_MAX;
   if (rope) {
     w.q_rot = take(T * Hq * d * esize(dt));
     w.k_rot = take(T * Hkv * d * esize(dt));
+    if (phase == 1) w.rope_tab = take(T * (d / 2) * sizeof(float2));
   }
   if (phase == 1) {
-    w.Dbuf = take(T * Hq * sizeof(float));
+    const size_t Tp = (size_t)padded_tokens(L);
+    w.Dbuf = take(Tp * Hq * sizeof(float));
+    w.lse2 = take(Tp * Hq * sizeof(float));
     w.dq_acc = take(T * Hq * d * sizeof(float));
     w.dk_acc = take(T * Hkv * d * sizeof(float));
   }
@@ -401,7 +404,8 @@ pg_status pg_grouped_attn_fwd(const pg_layout* layout, pg_dtype dtype, int32_t h
   const void* qx = q;
   const void* kx = k;
   if (rope) {
-    st = launch_rope(a, q, ws + w.q_rot, heads_q, k, ws + w.k_rot, heads_kv, false, false);
+    st = launch_rope(a, q, ws + w.q_rot, heads_q, k, ws + w.k_rot, heads_kv, false, false,
+                     nullptr, nullptr);
     if (st != PG_OK) return st;
     qx = ws + w.q_rot;
     kx = ws + w.k_rot;
@@ -431,28 +435,33 @@ pg_status pg_grouped_attn_bwd(const pg_layout* layout, pg_dtype dtype, int32_t h
   char* ws = static_cast<char*>(workspace);
   const void* qx = q;
   const void* kx = k;
+  float2* rope_tab = rope ? reinterpret_cast<float2*>(ws + w.rope_tab) : nullptr;
   if (rope) {
-    st = launch_rope(a, q, ws + w.q_rot, heads_q, k, ws + w.k_rot, heads_kv, false, false);
+    st = launch_rope(a, q, ws + w.q_rot, heads_q, k, ws + w.k_rot, heads_kv, false, false,
+                     rope_tab, nullptr);
     if (st != PG_OK) return st;
     qx = ws + w.q_rot;
     kx = ws + w.k_rot;
   }
   float* Dbuf = reinterpret_cast<float*>(ws + w.Dbuf);
+  float* lse2 = reinterpret_cast<float*>(ws + w.lse2);
   float* dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);
   float* dk_acc = reinterpret_cast<float*>(ws + w.dk_acc);
-  st = launch_bwd_preprocess(a, o, dO, Dbuf, dq_acc);
+  st = launch_bwd_preprocess(a, o, dO, lse, Dbuf, lse2, dq_acc);
   if (st != PG_OK) return st;
   if (!(a.flags & PG_FLAG_SIMT) && bwd_sm100_supported(a)) {
     // dK (inverse-rotated, cast) and dV are written by the key-major kernel itself; dQ arrives
     // in the fp32 accumulator and is rotated back and cast here.
-    st = launch_bwd_sm100(a, qx, kx, v, dO, lse, Dbuf, dq_acc, dk, dv);
+    st = launch_bwd_sm100(a, qx, kx, v, dO, lse2, Dbuf, dq_acc, dk, dv, rope_tab);
     if (st != PG_OK) return st;
-    return launch_rope(a, dq_acc, dq, heads_q, nullptr, nullptr, 0, true, true);
+    return launch_rope(a, dq_acc, dq, heads_q, nullptr, nullptr, 0, true, true, nullptr,
+                       rope_tab);
   }
   st = launch_bwd_simt(a, qx, kx, v, o, lse, dO, Dbuf, dq_acc, dk_acc, dv);
   if (st != PG_OK) return st;
   // dQ and dK of the rotated q/k back to the caller's q/k (inverse rotation) and dtype.
-  return launch_rope(a, dq_acc, dq, heads_q, dk_acc, dk, heads_kv, true, true);
+  return launch_rope(a, dq_acc, dq, heads_q, dk_acc, dk, heads_kv, true, true, nullptr,
+                     rope_tab);
 }
 
 pg_status pg_set_profile(pg_profile* profile) {

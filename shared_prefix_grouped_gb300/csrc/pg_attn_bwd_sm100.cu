@@ -9,7 +9,8 @@
 // reproducible, no atomics.  dQ is accumulated across key blocks with fp32 atomics (its summation
 // order is not fixed).
 //
-// Per query block (64 rows), with K, V resident in shared memory and Q, dO double-buffered:
+// Per query block (64 rows), with K, V resident in shared memory and Q, dO, the blocks' LSE (log2
+// units), rowsum(dO * O) and visibility entries arriving by TMA in a 3-stage ring:
 //   S^T  = K Q^T          M 128 keys x N 64 queries x K 128   (TMEM cols [0, 64))
 //   dP^T = V dO^T         M 128 x N 64 x K 128                 (TMEM cols [64, 128))
 //   P^T  = exp2(S^T * scale * log2 e - LSE_2[q]),  dS^T = P^T * (dP^T - Dsum[q])   (registers,
@@ -21,10 +22,11 @@
 // The MMA thread issues S^T / dP^T of block i before the gradient products of block i-1, so the
 // tensor core computes the next scores while the softmax warps work on the current ones.
 // The epilogue applies the softmax scale and the inverse RoPE rotation to dK in registers (a
-// thread holds a whole key row, so each (k, k + d/2) pair is local) and writes dK, dV in bf16.
+// thread holds a whole key row, so each (k, k + d/2) pair is local; cos/sin come from the table
+// the RoPE pass of the same call wrote) and writes dK, dV in bf16.
 //
-// Warps: 0 TMA producer (+ LSE / Dsum / visibility staging), 1 TMEM allocation and MMA issue,
-// 2..5 softmax (key rows), 6..9 dQ drain.  Every mbarrier wait is bounded.
+// Warps: 0 TMA producer, 1 TMEM allocation and MMA issue, 2..9 softmax (key rows; two
+// warpgroups split the 64 query columns), 10..13 dQ drain.  Every mbarrier wait is bounded.
 #include <limits.h>
 #include <math.h>
 
@@ -41,10 +43,10 @@ namespace {
 constexpr int D = 128;
 constexpr int BKV = 128;        // keys per CTA
 constexpr int BQ = 64;          // query rows per block
-constexpr int NSQ = 2;          // Q / dO stages
+constexpr int NSQ = 3;          // Q / dO stages
 constexpr uint32_t KHALF = BKV * 64 * 2;   // 16 KiB: [128 rows][64 cols] bf16
 constexpr uint32_t QHALF = BQ * 64 * 2;    // 8 KiB:  [64 rows][64 cols] bf16
-constexpr int NTHREADS = 320;
+constexpr int NTHREADS = 448;
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ int s_status_bwd = 0;
@@ -56,9 +58,9 @@ struct BwdSmem {
   uint8_t dO[NSQ][2 * QHALF];
   uint8_t p[KHALF];         // P^T  [128 keys][64 queries] bf16, SW128
   uint8_t ds[KHALF];        // dS^T [128 keys][64 queries]
-  float lse2[NSQ][BQ];
-  float dsum[NSQ][BQ];
-  int32_t own[NSQ][BQ];
+  alignas(128) float lse2[NSQ][BQ];
+  alignas(128) float dsum[NSQ][BQ];
+  alignas(128) int4 tokq[NSQ][BQ];   // per-token {g0, pe, own_lo, pos} of the block's queries
   uint64_t kv_full;
   uint64_t qd_full[NSQ], qd_empty[NSQ];
   uint64_t s_full, s_free, p_full, pds_free, dq_full, dq_free, mma_done;
@@ -80,11 +82,13 @@ __device__ __forceinline__ void red_add(float* p, float v) {
 __global__ void __launch_bounds__(NTHREADS, 1)
 attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                      const float* __restrict__ lse, const float* __restrict__ Dbuf,
+                      const __grid_constant__ CUtensorMap tl2, const __grid_constant__ CUtensorMap tds,
+                      const __grid_constant__ CUtensorMap ttok,
                       float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dk,
                       __nv_bfloat16* __restrict__ dv, const int4* __restrict__ tok,
                       const BwdTile* __restrict__ tiles, int Hq, int Hkv, int Ttot,
-                      float scale_log2, float scale, double log2_theta, uint64_t wait_ns) {
+                      float scale_log2, float scale, const float2* __restrict__ rope_tab,
+                      uint64_t wait_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   BwdSmem& sm = *reinterpret_cast<BwdSmem*>(base);
@@ -97,7 +101,10 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     return;
   }
   const int rep = Hq / Hkv;
-  const int nqt = (tl.q_hi - tl.q_lo + BQ - 1) / BQ;
+  // Query blocks start at a multiple of 4 rows (16-byte aligned TMA coordinates for the fp32
+  // rows); the few rows before q_lo that this adds never see the block's keys (they are masked).
+  const int qt0 = tl.q_lo & ~3;
+  const int nqt = (tl.q_hi - qt0 + BQ - 1) / BQ;
   const int n_it = rep * nqt;
 
   if (threadIdx.x == 0) {
@@ -107,8 +114,8 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       mbar_init(&sm.qd_empty[s], 1);
     }
     mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.s_free, 128);
-    mbar_init(&sm.p_full, 128);
+    mbar_init(&sm.s_free, 256);
+    mbar_init(&sm.p_full, 256);
     mbar_init(&sm.pds_free, 1);
     mbar_init(&sm.dq_full, 1);
     mbar_init(&sm.dq_free, 128);
@@ -134,6 +141,9 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
       prefetch_tmap(&tdo);
+      prefetch_tmap(&tl2);
+      prefetch_tmap(&tds);
+      prefetch_tmap(&ttok);
       mbar_expect_tx(&sm.kv_full, 4 * KHALF);
       tma_load_2d(sm.k, &tk, &sm.kv_full, kh * D, tl.k0);
       tma_load_2d(sm.k + KHALF, &tk, &sm.kv_full, kh * D + 64, tl.k0);
@@ -145,23 +155,17 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     for (int it = 0; it < n_it; ++it) {
       const int st = it % NSQ;
       const int h = kh * rep + it / nqt;
-      const int qt = tl.q_lo + (it % nqt) * BQ;
+      const int qt = qt0 + (it % nqt) * BQ;
       if (!warp_wait(&sm.qd_empty[st], ((it / NSQ) & 1) ^ 1, wait_ns)) { ok = false; break; }
-      for (int c = lane; c < BQ; c += 32) {
-        const int t = qt + c;
-        const bool in = t < tl.q_hi;
-        sm.lse2[st][c] = in ? lse[(size_t)h * Ttot + t] * kLog2e : 0.f;
-        sm.dsum[st][c] = in ? Dbuf[(size_t)h * Ttot + t] : 0.f;
-        sm.own[st][c] = in ? tok[t].z : INT_MAX;
-      }
-      __threadfence_block();
-      __syncwarp();
       if (leader) {
-        mbar_expect_tx(&sm.qd_full[st], 4 * QHALF);
+        mbar_expect_tx(&sm.qd_full[st], 4 * QHALF + 2 * BQ * 4 + BQ * 16);
         tma_load_2d(sm.q[st], &tq, &sm.qd_full[st], h * D, qt);
         tma_load_2d(sm.q[st] + QHALF, &tq, &sm.qd_full[st], h * D + 64, qt);
         tma_load_2d(sm.dO[st], &tdo, &sm.qd_full[st], h * D, qt);
         tma_load_2d(sm.dO[st] + QHALF, &tdo, &sm.qd_full[st], h * D + 64, qt);
+        tma_load_2d(sm.lse2[st], &tl2, &sm.qd_full[st], qt, h);
+        tma_load_2d(sm.dsum[st], &tds, &sm.qd_full[st], qt, h);
+        tma_load_2d(sm.tokq[st], &ttok, &sm.qd_full[st], 0, qt);
       }
       __syncwarp();
       ++issued;
@@ -237,55 +241,75 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       mbar_wait(&sm.mma_done, 0, wait_ns);
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp < 10) {
     // ------------------------------------------------------------------ softmax (keys) ----
+    // Two warpgroups: warps 2..5 take query columns 0..31 of the block, warps 6..9 columns
+    // 32..63; warp w reads TMEM lanes 32 * (w % 4) .. + 31 (its key rows).
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
     const int key = tl.k0 + r;
     const bool kvalid = key < tl.k1;
     const int keyc = kvalid ? key : tl.k1 - 1;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    const int c0 = half * 32;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int st = it % NSQ;
-      const int qt = tl.q_lo + (it % nqt) * BQ;
+      const int qt = qt0 + (it % nqt) * BQ;
       if (!warp_wait(&sm.s_full, it & 1, wait_ns)) { ok = false; break; }
       if (!warp_wait(&sm.qd_full[st], (it / NSQ) & 1, wait_ns)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sr[64], dr[64];
-      tmem_ld32(t_s + lane_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(t_s + lane_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tmem_ld32(t_dp + lane_addr, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
-      tmem_ld32(t_dp + lane_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+      uint32_t sr[32], dr[32];
+      tmem_ld32(t_s + lane_addr + c0, sr);
+      tmem_ld32(t_dp + lane_addr + c0, dr);
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&sm.s_free);
       const bool full = (qt >= tl.k0 + BKV - 1) && (tl.k1 - tl.k0 == BKV) && (tl.k1 <= tl.pe) &&
                         (qt + BQ <= tl.q_hi);
-      const float* l2 = sm.lse2[st];
-      const float* ds_ = sm.dsum[st];
-      const int32_t* own = sm.own[st];
-      uint32_t pw[32], dw[32];
+      const float4* l2v = reinterpret_cast<const float4*>(sm.lse2[st] + c0);
+      const float4* dsv = reinterpret_cast<const float4*>(sm.dsum[st] + c0);
+      uint32_t pw[16], dw[16];
+      if (full) {
 #pragma unroll
-      for (int c = 0; c < BQ; c += 2) {
-        float p0, p1;
-        const int t0 = qt + c, t1 = qt + c + 1;
-        const bool v0 = full || (kvalid && t0 < tl.q_hi && keyc <= t0 && keyc >= tl.g0 &&
-                                 (keyc < tl.pe || keyc >= own[c]));
-        const bool v1 = full || (kvalid && t1 < tl.q_hi && keyc <= t1 && keyc >= tl.g0 &&
-                                 (keyc < tl.pe || keyc >= own[c + 1]));
-        p0 = v0 ? fast_exp2(fmaf(__uint_as_float(sr[c]), scale_log2, -l2[c])) : 0.f;
-        p1 = v1 ? fast_exp2(fmaf(__uint_as_float(sr[c + 1]), scale_log2, -l2[c + 1])) : 0.f;
-        const float g0 = p0 * (__uint_as_float(dr[c]) - ds_[c]);
-        const float g1 = p1 * (__uint_as_float(dr[c + 1]) - ds_[c + 1]);
-        pw[c >> 1] = pack_bf16x2(p0, p1);
-        dw[c >> 1] = pack_bf16x2(g0, g1);
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 l = l2v[c4], dd = dsv[c4];
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[4 * c4]), scale_log2, -l.x));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[4 * c4 + 1]), scale_log2, -l.y));
+          const float p2 = fast_exp2(fmaf(__uint_as_float(sr[4 * c4 + 2]), scale_log2, -l.z));
+          const float p3 = fast_exp2(fmaf(__uint_as_float(sr[4 * c4 + 3]), scale_log2, -l.w));
+          pw[2 * c4] = pack_bf16x2(p0, p1);
+          pw[2 * c4 + 1] = pack_bf16x2(p2, p3);
+          dw[2 * c4] = pack_bf16x2(p0 * (__uint_as_float(dr[4 * c4]) - dd.x),
+                                   p1 * (__uint_as_float(dr[4 * c4 + 1]) - dd.y));
+          dw[2 * c4 + 1] = pack_bf16x2(p2 * (__uint_as_float(dr[4 * c4 + 2]) - dd.z),
+                                       p3 * (__uint_as_float(dr[4 * c4 + 3]) - dd.w));
+        }
+      } else {
+        const int4* tq4 = sm.tokq[st] + c0;
+        const float* l2 = sm.lse2[st] + c0;
+        const float* ds_ = sm.dsum[st] + c0;
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const int t0 = qt + c0 + c, t1 = t0 + 1;
+          const bool v0 = kvalid && t0 < tl.q_hi && keyc <= t0 && keyc >= tl.g0 &&
+                          (keyc < tl.pe || keyc >= tq4[c].z);
+          const bool v1 = kvalid && t1 < tl.q_hi && keyc <= t1 && keyc >= tl.g0 &&
+                          (keyc < tl.pe || keyc >= tq4[c + 1].z);
+          const float p0 = v0 ? fast_exp2(fmaf(__uint_as_float(sr[c]), scale_log2, -l2[c])) : 0.f;
+          const float p1 =
+              v1 ? fast_exp2(fmaf(__uint_as_float(sr[c + 1]), scale_log2, -l2[c + 1])) : 0.f;
+          pw[c >> 1] = pack_bf16x2(p0, p1);
+          dw[c >> 1] = pack_bf16x2(v0 ? p0 * (__uint_as_float(dr[c]) - ds_[c]) : 0.f,
+                                   v1 ? p1 * (__uint_as_float(dr[c + 1]) - ds_[c + 1]) : 0.f);
+        }
       }
       // The previous block's gradient products must be done with P^T / dS^T.
       if (it > 0 && !warp_wait(&sm.pds_free, (it - 1) & 1, wait_ns)) { ok = false; break; }
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const uint32_t off = sw128_offset(r, ch);
+      for (int ch = 0; ch < 4; ++ch) {
+        const uint32_t off = sw128_offset(r, half * 4 + ch);
         *reinterpret_cast<uint4*>(sm.p + off) =
             make_uint4(pw[4 * ch], pw[4 * ch + 1], pw[4 * ch + 2], pw[4 * ch + 3]);
         *reinterpret_cast<uint4*>(sm.ds + off) =
@@ -295,73 +319,66 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       tc_fence_before();
       mbar_arrive(&sm.p_full);
     }
-    // Epilogue: dV and scale * dK (inverse-rotated) of this thread's key row.
+    // Epilogue of this thread's key row: warps 2..5 write dV, warps 6..9 write scale * dK,
+    // rotated back by the key's RoPE angle (columns c and c + 64 form a rotation pair).
     if (ok && warp_wait(&sm.pds_free, (n_it - 1) & 1, wait_ns)) {
       tc_fence_after();
-      float cs[64], sn[64];
-      if (log2_theta > 0.0) {
-        const double two_pi = 6.283185307179586476925;
-        const double pos = (double)tok[keyc].w;
-#pragma unroll 1
-        for (int k2 = 0; k2 < 64; ++k2) {
-          const double a = pos * exp2(-(2.0 * k2 / D) * log2_theta);
-          const double red = a - two_pi * rint(a / two_pi);
-          sincosf((float)red, &sn[k2], &cs[k2]);
-        }
-      }
       const size_t off = ((size_t)keyc * Hkv + kh) * D;
-      // dV
+      if (half == 0) {
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v32[32];
-        tmem_ld32(t_dv + lane_addr + c * 32, v32);
-        tmem_ld_wait();
-        if (kvalid) {
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v32[32];
+          tmem_ld32(t_dv + lane_addr + c * 32, v32);
+          tmem_ld_wait();
+          if (kvalid) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(v32[i]), __uint_as_float(v32[i + 1]));
-            w.y = pack_bf16x2(__uint_as_float(v32[i + 2]), __uint_as_float(v32[i + 3]));
-            w.z = pack_bf16x2(__uint_as_float(v32[i + 4]), __uint_as_float(v32[i + 5]));
-            w.w = pack_bf16x2(__uint_as_float(v32[i + 6]), __uint_as_float(v32[i + 7]));
-            *reinterpret_cast<uint4*>(dv + off + c * 32 + i) = w;
+            for (int i = 0; i < 32; i += 8) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(v32[i]), __uint_as_float(v32[i + 1]));
+              w.y = pack_bf16x2(__uint_as_float(v32[i + 2]), __uint_as_float(v32[i + 3]));
+              w.z = pack_bf16x2(__uint_as_float(v32[i + 4]), __uint_as_float(v32[i + 5]));
+              w.w = pack_bf16x2(__uint_as_float(v32[i + 6]), __uint_as_float(v32[i + 7]));
+              *reinterpret_cast<uint4*>(dv + off + c * 32 + i) = w;
+            }
           }
         }
-      }
-      // dK: columns c and c + 64 form a rotation pair
+      } else {
+        const float2* cs = rope_tab ? rope_tab + (size_t)keyc * (D / 2) : nullptr;
 #pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        uint32_t a32[32], b32[32];
-        tmem_ld32(t_dk + lane_addr + c * 32, a32);
-        tmem_ld32(t_dk + lane_addr + 64 + c * 32, b32);
-        tmem_ld_wait();
-        float lo[32], hi[32];
+        for (int c = 0; c < 2; ++c) {
+          uint32_t a32[32], b32[32];
+          tmem_ld32(t_dk + lane_addr + c * 32, a32);
+          tmem_ld32(t_dk + lane_addr + 64 + c * 32, b32);
+          tmem_ld_wait();
+          float lo[32], hi[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float x1 = __uint_as_float(a32[i]) * scale, x2 = __uint_as_float(b32[i]) * scale;
-          if (log2_theta > 0.0) {
-            const float cc = cs[c * 32 + i], ss = sn[c * 32 + i];
-            lo[i] = x1 * cc + x2 * ss;
-            hi[i] = x2 * cc - x1 * ss;
-          } else {
-            lo[i] = x1;
-            hi[i] = x2;
+          for (int i = 0; i < 32; ++i) {
+            const float x1 = __uint_as_float(a32[i]) * scale;
+            const float x2 = __uint_as_float(b32[i]) * scale;
+            if (cs) {
+              const float2 e = cs[c * 32 + i];   // (cos, sin)
+              lo[i] = x1 * e.x + x2 * e.y;
+              hi[i] = x2 * e.x - x1 * e.y;
+            } else {
+              lo[i] = x1;
+              hi[i] = x2;
+            }
           }
-        }
-        if (kvalid) {
+          if (kvalid) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            uint4 w;
-            w.x = pack_bf16x2(lo[i], lo[i + 1]);
-            w.y = pack_bf16x2(lo[i + 2], lo[i + 3]);
-            w.z = pack_bf16x2(lo[i + 4], lo[i + 5]);
-            w.w = pack_bf16x2(lo[i + 6], lo[i + 7]);
-            *reinterpret_cast<uint4*>(dk + off + c * 32 + i) = w;
-            w.x = pack_bf16x2(hi[i], hi[i + 1]);
-            w.y = pack_bf16x2(hi[i + 2], hi[i + 3]);
-            w.z = pack_bf16x2(hi[i + 4], hi[i + 5]);
-            w.w = pack_bf16x2(hi[i + 6], hi[i + 7]);
-            *reinterpret_cast<uint4*>(dk + off + 64 + c * 32 + i) = w;
+            for (int i = 0; i < 32; i += 8) {
+              uint4 w;
+              w.x = pack_bf16x2(lo[i], lo[i + 1]);
+              w.y = pack_bf16x2(lo[i + 2], lo[i + 3]);
+              w.z = pack_bf16x2(lo[i + 4], lo[i + 5]);
+              w.w = pack_bf16x2(lo[i + 6], lo[i + 7]);
+              *reinterpret_cast<uint4*>(dk + off + c * 32 + i) = w;
+              w.x = pack_bf16x2(hi[i], hi[i + 1]);
+              w.y = pack_bf16x2(hi[i + 2], hi[i + 3]);
+              w.z = pack_bf16x2(hi[i + 4], hi[i + 5]);
+              w.w = pack_bf16x2(hi[i + 6], hi[i + 7]);
+              *reinterpret_cast<uint4*>(dk + off + 64 + c * 32 + i) = w;
+            }
           }
         }
       }
@@ -377,7 +394,7 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int h = kh * rep + it / nqt;
-      const int qt = tl.q_lo + (it % nqt) * BQ;
+      const int qt = qt0 + (it % nqt) * BQ;
       if (!warp_wait(&sm.dq_full, it & 1, wait_ns)) { ok = false; break; }
       tc_fence_after();
       uint32_t g[64];
@@ -406,11 +423,12 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
 bool bwd_sm100_supported(const AttnArgs& a) { return a.dtype == PG_BF16 && a.d == 128; }
 
 pg_status launch_bwd_sm100(const AttnArgs& a, const void* q, const void* k, const void* v,
-                           const void* dO, const float* lse, const float* Dbuf, float* dq_acc,
-                           void* dk, void* dv) {
+                           const void* dO, const float* lse2, const float* Dbuf, float* dq_acc,
+                           void* dk, void* dv, const float2* rope_tab) {
   const pg_layout* L = a.layout;
   const int64_t T = L->total_tokens;
-  CUtensorMap tq, tk, tv, tdo;
+  const int64_t Tp = padded_tokens(L);
+  CUtensorMap tq, tk, tv, tdo, tl2, tds, ttok;
   pg_status st = make_tmap_2d_bf16(&tq, q, (uint64_t)a.Hq * D, T, (uint64_t)a.Hq * D * 2, 64, BQ);
   if (st == PG_OK)
     st = make_tmap_2d_bf16(&tdo, dO, (uint64_t)a.Hq * D, T, (uint64_t)a.Hq * D * 2, 64, BQ);
@@ -418,18 +436,20 @@ pg_status launch_bwd_sm100(const AttnArgs& a, const void* q, const void* k, cons
     st = make_tmap_2d_bf16(&tk, k, (uint64_t)a.Hkv * D, T, (uint64_t)a.Hkv * D * 2, 64, BKV);
   if (st == PG_OK)
     st = make_tmap_2d_bf16(&tv, v, (uint64_t)a.Hkv * D, T, (uint64_t)a.Hkv * D * 2, 64, BKV);
+  if (st == PG_OK) st = make_tmap_2d_b32(&tl2, lse2, true, Tp, a.Hq, Tp * 4, BQ, 1);
+  if (st == PG_OK) st = make_tmap_2d_b32(&tds, Dbuf, true, Tp, a.Hq, Tp * 4, BQ, 1);
+  if (st == PG_OK) st = make_tmap_2d_b32(&ttok, tokens(L), false, 4, T, 16, 4, BQ);
   if (st != PG_OK) return st;
   const size_t smem = sizeof(BwdSmem) + 1024;
   st = cuda_check(cudaFuncSetAttribute(attn_bwd_sm100_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
                   "bwd smem attribute");
   if (st != PG_OK) return st;
-  const double l2t = a.theta > 0.f ? log2((double)a.theta) : 0.0;
   prof_begin(PG_KERNEL_BWD_DKDV, a.stream);
   attn_bwd_sm100_kernel<<<(unsigned)(L->n_tiles[BWD128] * a.Hkv), NTHREADS, smem, a.stream>>>(
-      tq, tk, tv, tdo, lse, Dbuf, dq_acc, static_cast<__nv_bfloat16*>(dk),
+      tq, tk, tv, tdo, tl2, tds, ttok, dq_acc, static_cast<__nv_bfloat16*>(dk),
       static_cast<__nv_bfloat16*>(dv), tokens(L), tiles<BwdTile>(L, BWD128), a.Hq, a.Hkv, (int)T,
-      a.scale * kLog2e, a.scale, l2t, 2000000000ull);
+      a.scale * kLog2e, a.scale, rope_tab, 2000000000ull);
   prof_end(PG_KERNEL_BWD_DKDV, a.stream);
   return cuda_check(cudaGetLastError(), "bwd sm100 launch");
 }

@@ -35,6 +35,10 @@ static_assert(sizeof(BwdTile) == 32, "BwdTile layout");
 
 enum TileList { FWD64 = 0, FWD128 = 1, BWD64 = 2, BWD128 = 3 };
 
+// Row stride (elements) of the per-head fp32 rows the backward keeps for LSE and rowsum(dO * O):
+// T rounded up to a multiple of 4, so every row starts 16-byte aligned (a TMA requirement).
+inline int64_t padded_tokens(const pg_layout* L) { return (L->total_tokens + 3) & ~int64_t(3); }
+
 inline const int4* tokens(const pg_layout* L) {
   return reinterpret_cast<const int4*>(static_cast<const char*>(L->tables) + L->off_tokens);
 }
@@ -81,19 +85,26 @@ pg_status launch_fwd_sm100(const AttnArgs& a, const void* q, const void* k, cons
                            float* lse);
 bool bwd_sm100_supported(const AttnArgs& a);
 pg_status launch_bwd_sm100(const AttnArgs& a, const void* q, const void* k, const void* v,
-                           const void* dO, const float* lse, const float* Dbuf, float* dq_acc,
-                           void* dk, void* dv);
+                           const void* dO, const float* lse2, const float* Dbuf, float* dq_acc,
+                           void* dk, void* dv, const float2* rope_tab);
 pg_status cuda_check(cudaError_t e, const char* what);
+
+// RoPE inverse frequencies theta^(-2k/d), k < d/2, computed on the host in fp64.
+struct RopeFreq {
+  double inv[64];
+  double inv_two_pi;
+};
 
 // SIMT kernels (pg_simt.cu).
 pg_status launch_rope(const AttnArgs& a, const void* x0, void* y0, int heads0, const void* x1,
-                      void* y1, int heads1, bool inverse, bool in_fp32);
+                      void* y1, int heads1, bool inverse, bool in_fp32, float2* table_out,
+                      const float2* table_in);
 pg_status launch_fwd_simt(const AttnArgs& a, const void* q, const void* k, const void* v, void* o,
                           float* lse);
 pg_status launch_bwd_simt(const AttnArgs& a, const void* q, const void* k, const void* v,
                           const void* o, const float* lse, const void* dO, float* Dbuf,
                           float* dq_acc, float* dk_acc, void* dv);
-pg_status launch_bwd_preprocess(const AttnArgs& a, const void* o, const void* dO, float* Dbuf,
-                                float* dq_acc);
+pg_status launch_bwd_preprocess(const AttnArgs& a, const void* o, const void* dO, const float* lse,
+                                float* Dbuf, float* lse2, float* dq_acc);
 
 }  // namespace pg

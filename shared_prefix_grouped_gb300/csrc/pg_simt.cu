@@ -81,25 +81,35 @@ __device__ __forceinline__ bool visible(int t, int s, int4 ti) {
 
 // ---------------------------------------------------------------------------------------------
 // RoPE: rotate (or inverse-rotate) the pairs (x[k], x[k + d/2]) of every head of a token by the
-// angle pos * theta^(-2k/d).  The angle is formed and reduced to [-pi, pi] in fp64, then sin/cos
-// are taken in fp32.  theta == 0 only converts (used to cast the fp32 gradient accumulators).
+// angle pos * theta^(-2k/d).  The inverse frequencies come from the host in fp64; the angle is
+// formed and reduced to [-pi, pi] in fp64 (two multiplies and a rounding), then sin/cos are taken
+// in fp32.  With a table_out the (cos, sin) pairs are also stored ([T][d/2] float2) for later
+// passes of the same call; with a table_in they are read from it instead of recomputed.
+// `rope` false only converts (used to cast the fp32 gradient accumulators).
 // One block per token; two tensors (q and k) per launch.
 // ---------------------------------------------------------------------------------------------
 template <typename Tin, typename Tout>
 __global__ void rope_kernel(const Tin* __restrict__ x0, Tout* __restrict__ y0, int h0,
                             const Tin* __restrict__ x1, Tout* __restrict__ y1, int h1, int d,
-                            const int32_t* __restrict__ pos_ids, double log2_theta, float sgn) {
+                            const int32_t* __restrict__ pos_ids, RopeFreq f, int rope, float sgn,
+                            float2* __restrict__ table_out, const float2* __restrict__ table_in) {
   __shared__ float cs[64], sn[64];
   const int t = blockIdx.x;
   const int half = d >> 1;
   if (threadIdx.x < half) {
     float c = 1.f, s = 0.f;
-    if (log2_theta > 0.0) {
-      const double two_pi = 6.283185307179586476925;
-      double inv = exp2(-(2.0 * threadIdx.x / d) * log2_theta);
-      double a = (double)pos_ids[t] * inv;
-      double r = a - two_pi * rint(a / two_pi);
-      sincosf((float)r, &s, &c);
+    if (rope) {
+      if (table_in) {
+        const float2 e = table_in[(size_t)t * half + threadIdx.x];
+        c = e.x;
+        s = e.y;
+      } else {
+        const double two_pi = 6.283185307179586476925;
+        const double a = (double)pos_ids[t] * f.inv[threadIdx.x];
+        const double r = fma(-two_pi, rint(a * f.inv_two_pi), a);
+        sincosf((float)r, &s, &c);
+        if (table_out) table_out[(size_t)t * half + threadIdx.x] = make_float2(c, s);
+      }
     }
     cs[threadIdx.x] = c;
     sn[threadIdx.x] = sgn * s;
@@ -220,16 +230,26 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
 }
 
 // ---------------------------------------------------------------------------------------------
-// Backward preprocess: Dv[h][t] = sum_j dO[t,h,j] * O[t,h,j] (fp32).  One warp per (t, h).
+// Backward preprocess: Dbuf[h][t] = sum_j dO[t,h,j] * O[t,h,j] and lse2[h][t] = lse[h][t] * log2 e
+// (fp32 rows of stride ldd >= T, padding zeroed), and zero the fp32 dQ accumulator.
+// One warp per (t, h).
 // ---------------------------------------------------------------------------------------------
 template <typename T>
 __global__ void bwd_pre_kernel(const T* __restrict__ o, const T* __restrict__ dO,
-                               float* __restrict__ Dbuf, float* __restrict__ dq_acc, int Hq, int D,
-                               int Ttot) {
+                               const float* __restrict__ lse, float* __restrict__ Dbuf,
+                               float* __restrict__ lse2, float* __restrict__ dq_acc, int Hq, int D,
+                               int Ttot, int ldd) {
   const int lane = threadIdx.x & 31;
   const size_t warp = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (warp >= (size_t)Ttot * Hq) return;
+  if (warp >= (size_t)ldd * Hq) return;
   const int t = (int)(warp / Hq), h = (int)(warp % Hq);
+  if (t >= Ttot) {
+    if (lane == 0) {
+      Dbuf[(size_t)h * ldd + t] = 0.f;
+      lse2[(size_t)h * ldd + t] = 0.f;
+    }
+    return;
+  }
   const size_t base = ((size_t)t * Hq + h) * D;
   float acc = 0.f;
   for (int c = lane * 4; c < D; c += 128) {
@@ -239,7 +259,10 @@ __global__ void bwd_pre_kernel(const T* __restrict__ o, const T* __restrict__ dO
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) Dbuf[(size_t)h * Ttot + t] = acc;
+  if (lane == 0) {
+    Dbuf[(size_t)h * ldd + t] = acc;
+    lse2[(size_t)h * ldd + t] = lse[(size_t)h * Ttot + t] * kLog2e;
+  }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -254,7 +277,7 @@ dkdv_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
                  const T* __restrict__ dO, const float* __restrict__ lse,
                  const float* __restrict__ Dbuf, float* __restrict__ dk_acc, T* __restrict__ dv,
                  const int4* __restrict__ tok, const BwdTile* __restrict__ tiles, int Hq, int Hkv,
-                 int Ttot, float scale_log2, float scale) {
+                 int Ttot, int ldd, float scale_log2, float scale) {
   constexpr int BM = 64, NV = D / 16;
   extern __shared__ float4 smem4[];
   float* Qs = reinterpret_cast<float*>(smem4);
@@ -303,7 +326,7 @@ dkdv_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
         int qr = qt + tid;
         bool in = qr < tl.q_hi;
         Ls[tid] = in ? lse[(size_t)h * Ttot + qr] * kLog2e : 0.f;
-        Ds[tid] = in ? Dbuf[(size_t)h * Ttot + qr] : 0.f;
+        Ds[tid] = in ? Dbuf[(size_t)h * ldd + qr] : 0.f;
         Ts[tid] = in ? tok[qr] : make_int4(0, 0, 0, 0);
       }
       __syncthreads();
@@ -354,7 +377,7 @@ dq_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __rest
                const T* __restrict__ dO, const float* __restrict__ lse,
                const float* __restrict__ Dbuf, float* __restrict__ dq_acc,
                const int4* __restrict__ tok, const FwdTile* __restrict__ tiles, int Hq, int Hkv,
-               int Ttot, float scale_log2, float scale) {
+               int Ttot, int ldd, float scale_log2, float scale) {
   constexpr int BN = 64, NV = D / 16;
   extern __shared__ float4 smem4[];
   float* Ks = reinterpret_cast<float*>(smem4);
@@ -381,7 +404,7 @@ dq_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __rest
     dq[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   const float L2 = lse[(size_t)h * Ttot + rowc] * kLog2e;
-  const float Dr = Dbuf[(size_t)h * Ttot + rowc];
+  const float Dr = Dbuf[(size_t)h * ldd + rowc];
   for (int range = 0; range < 2; ++range) {
     const int lo = range ? tl.s_lo : tl.g0, hi = range ? tl.s_hi : tl.p_end;
     for (int kt = lo; kt < hi; kt += BN) {
@@ -470,7 +493,8 @@ pg_status bwd_simt_t(const AttnArgs& a, const void* q, const void* k, const void
     kern<<<(unsigned)(L->n_tiles[BWD64] * a.Hkv), 256, smem, a.stream>>>(
         static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
         static_cast<const T*>(dO), lse, Dbuf, dk_acc, static_cast<T*>(dv), tokens(L),
-        tiles<BwdTile>(L, BWD64), a.Hq, a.Hkv, Ttot, a.scale * kLog2e, a.scale);
+        tiles<BwdTile>(L, BWD64), a.Hq, a.Hkv, Ttot, (int)padded_tokens(L), a.scale * kLog2e,
+        a.scale);
     prof_end(PG_KERNEL_BWD_DKDV, a.stream);
     st = cuda_check(cudaGetLastError(), "dkdv_simt launch");
     if (st != PG_OK) return st;
@@ -484,7 +508,7 @@ pg_status bwd_simt_t(const AttnArgs& a, const void* q, const void* k, const void
     kern<<<(unsigned)(L->n_tiles[FWD64] * a.Hq), 256, smem, a.stream>>>(
         static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
         static_cast<const T*>(dO), lse, Dbuf, dq_acc, tokens(L), tiles<FwdTile>(L, FWD64), a.Hq,
-        a.Hkv, Ttot, a.scale * kLog2e, a.scale);
+        a.Hkv, Ttot, (int)padded_tokens(L), a.scale * kLog2e, a.scale);
     prof_end(PG_KERNEL_BWD_DQ, a.stream);
     return cuda_check(cudaGetLastError(), "dq_simt launch");
   }
@@ -492,10 +516,20 @@ pg_status bwd_simt_t(const AttnArgs& a, const void* q, const void* k, const void
 
 }  // namespace
 
+RopeFreq rope_freq(const AttnArgs& a) {
+  RopeFreq f{};
+  for (int k = 0; k < a.d / 2 && k < 64; ++k)
+    f.inv[k] = a.theta > 0.f ? pow((double)a.theta, -2.0 * k / a.d) : 0.0;
+  f.inv_two_pi = 1.0 / 6.283185307179586476925;
+  return f;
+}
+
 pg_status launch_rope(const AttnArgs& a, const void* x0, void* y0, int heads0, const void* x1,
-                      void* y1, int heads1, bool inverse, bool in_fp32) {
+                      void* y1, int heads1, bool inverse, bool in_fp32, float2* table_out,
+                      const float2* table_in) {
   const int T = (int)a.layout->total_tokens;
-  const double l2t = a.theta > 0.f ? log2((double)a.theta) : 0.0;
+  const int rope = a.theta > 0.f ? 1 : 0;
+  const RopeFreq f = rope_freq(a);
   const float sgn = inverse ? -1.f : 1.f;
   const int32_t* pos = a.layout->position_ids;
   dim3 grid(T), block(128);
@@ -504,17 +538,18 @@ pg_status launch_rope(const AttnArgs& a, const void* x0, void* y0, int heads0, c
   if (a.dtype == PG_F32) {
     rope_kernel<float, float><<<grid, block, 0, a.stream>>>(
         static_cast<const float*>(x0), static_cast<float*>(y0), heads0,
-        static_cast<const float*>(x1), static_cast<float*>(y1), heads1, a.d, pos, l2t, sgn);
+        static_cast<const float*>(x1), static_cast<float*>(y1), heads1, a.d, pos, f, rope, sgn,
+        table_out, table_in);
   } else if (in_fp32) {
     rope_kernel<float, __nv_bfloat16><<<grid, block, 0, a.stream>>>(
         static_cast<const float*>(x0), static_cast<__nv_bfloat16*>(y0), heads0,
-        static_cast<const float*>(x1), static_cast<__nv_bfloat16*>(y1), heads1, a.d, pos, l2t,
-        sgn);
+        static_cast<const float*>(x1), static_cast<__nv_bfloat16*>(y1), heads1, a.d, pos, f, rope,
+        sgn, table_out, table_in);
   } else {
     rope_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, block, 0, a.stream>>>(
         static_cast<const __nv_bfloat16*>(x0), static_cast<__nv_bfloat16*>(y0), heads0,
         static_cast<const __nv_bfloat16*>(x1), static_cast<__nv_bfloat16*>(y1), heads1, a.d, pos,
-        l2t, sgn);
+        f, rope, sgn, table_out, table_in);
   }
   prof_end(kid, a.stream);
   return cuda_check(cudaGetLastError(), "rope launch");
@@ -529,19 +564,21 @@ pg_status launch_fwd_simt(const AttnArgs& a, const void* q, const void* k, const
                    : fwd_simt_t<__nv_bfloat16, 128>(a, q, k, v, o, lse);
 }
 
-pg_status launch_bwd_preprocess(const AttnArgs& a, const void* o, const void* dO, float* Dbuf,
-                                float* dq_acc) {
+pg_status launch_bwd_preprocess(const AttnArgs& a, const void* o, const void* dO, const float* lse,
+                                float* Dbuf, float* lse2, float* dq_acc) {
   const int T = (int)a.layout->total_tokens;
-  const size_t warps = (size_t)T * a.Hq;
+  const int ldd = (int)padded_tokens(a.layout);
+  const size_t warps = (size_t)ldd * a.Hq;
   const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
   prof_begin(PG_KERNEL_BWD_PREPROCESS, a.stream);
   if (a.dtype == PG_F32)
     bwd_pre_kernel<float><<<blocks, 256, 0, a.stream>>>(
-        static_cast<const float*>(o), static_cast<const float*>(dO), Dbuf, dq_acc, a.Hq, a.d, T);
+        static_cast<const float*>(o), static_cast<const float*>(dO), lse, Dbuf, lse2, dq_acc,
+        a.Hq, a.d, T, ldd);
   else
     bwd_pre_kernel<__nv_bfloat16><<<blocks, 256, 0, a.stream>>>(
-        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), Dbuf, dq_acc,
-        a.Hq, a.d, T);
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, Dbuf,
+        lse2, dq_acc, a.Hq, a.d, T, ldd);
   prof_end(PG_KERNEL_BWD_PREPROCESS, a.stream);
   return cuda_check(cudaGetLastError(), "bwd preprocess launch");
 }

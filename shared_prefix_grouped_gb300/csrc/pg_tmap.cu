@@ -50,4 +50,31 @@ pg_status make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, 
   return PG_OK;
 }
 
+pg_status make_tmap_2d_b32(CUtensorMap* map, const void* base, bool is_float, uint64_t inner,
+                           uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
+                           uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) {
+    set_error("cuTensorMapEncodeTiled is not available from the driver");
+    return PG_ERR_CUDA;
+  }
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) || (row_stride_bytes & 15u)) {
+    set_error("TMA needs 16-byte aligned base and row stride");
+    return PG_ERR_INVALID_ARG;
+  }
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, is_float ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_INT32,
+                  2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled (32-bit) failed (%d)", (int)r);
+    return PG_ERR_CUDA;
+  }
+  return PG_OK;
+}
+
 }  // namespace pg

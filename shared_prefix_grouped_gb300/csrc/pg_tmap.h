@@ -11,4 +11,10 @@ namespace pg {
 pg_status make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                             uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
 
+// 2-D tensor map without swizzle (fp32 or int32 elements, 4 bytes each): `inner` elements per row,
+// `outer` rows `row_stride_bytes` apart, boxes of box_inner x box_outer; out-of-range reads are 0.
+pg_status make_tmap_2d_b32(CUtensorMap* map, const void* base, bool is_float, uint64_t inner,
+                           uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
+                           uint32_t box_outer);
+
 }  // namespace pg
