@@ -6,11 +6,11 @@
 // group, so the prefix dK / dV -- the sum over the G baseline copies of the shared prefix (Pith
 // review of Prefix Grouper, Appendix A.1 objection: the shared prefix's gradient equals the sum of
 // the copies' gradients) -- is accumulated in TMEM by one CTA in a fixed order: bitwise
-// reproducible, no atomics.  dQ is accumulated across key blocks with fp32 atomics (its summation
-// order is not fixed).
+// reproducible, no atomics.  dQ is accumulated across key blocks by TMA reduce-adds into an fp32
+// buffer (its summation order is not fixed).
 //
 // Per query block (64 rows), with K, V resident in shared memory and Q, dO, the blocks' LSE (log2
-// units), rowsum(dO * O) and visibility entries arriving by TMA in a 3-stage ring:
+// units), rowsum(dO * O) and visibility entries arriving by TMA in a 2-stage ring:
 //   S^T  = K Q^T          M 128 keys x N 64 queries x K 128   (TMEM cols [0, 64))
 //   dP^T = V dO^T         M 128 x N 64 x K 128                 (TMEM cols [64, 128))
 //   P^T  = exp2(S^T * scale * log2 e - LSE_2[q]),  dS^T = P^T * (dP^T - Dsum[q])   (registers,
@@ -18,7 +18,8 @@
 //   dV  += P^T dO         M 128 x N 128 dims x K 64           (TMEM cols [256, 384))
 //   dK  += dS^T Q         M 128 x N 128 x K 64                 (TMEM cols [384, 512))
 //   dQ^T = K^T dS^T       M 128 dims x N 64 queries x K 128    (TMEM cols [128, 192)),
-//          drained by four warps (one thread per head-dim lane) as coalesced fp32 atomics.
+//          drained by four warps (one thread per head-dim lane) into a [64 x 128] fp32 block in
+//          shared memory, which one TMA bulk reduce-add adds into the global dQ accumulator.
 // The MMA thread issues S^T / dP^T of block i before the gradient products of block i-1, so the
 // tensor core computes the next scores while the softmax warps work on the current ones.
 // The epilogue applies the softmax scale and the inverse RoPE rotation to dK in registers (a
@@ -43,7 +44,7 @@ namespace {
 constexpr int D = 128;
 constexpr int BKV = 128;        // keys per CTA
 constexpr int BQ = 64;          // query rows per block
-constexpr int NSQ = 3;          // Q / dO stages
+constexpr int NSQ = 2;          // Q / dO stages
 constexpr uint32_t KHALF = BKV * 64 * 2;   // 16 KiB: [128 rows][64 cols] bf16
 constexpr uint32_t QHALF = BQ * 64 * 2;    // 8 KiB:  [64 rows][64 cols] bf16
 constexpr int NTHREADS = 448;
@@ -58,12 +59,13 @@ struct BwdSmem {
   uint8_t dO[NSQ][2 * QHALF];
   uint8_t p[KHALF];         // P^T  [128 keys][64 queries] bf16, SW128
   uint8_t ds[KHALF];        // dS^T [128 keys][64 queries]
+  alignas(1024) float dqs[BQ][D];   // dQ block staged for the bulk reduce-add
   alignas(128) float lse2[NSQ][BQ];
   alignas(128) float dsum[NSQ][BQ];
   alignas(128) int4 tokq[NSQ][BQ];   // per-token {g0, pe, own_lo, pos} of the block's queries
   uint64_t kv_full;
   uint64_t qd_full[NSQ], qd_empty[NSQ];
-  uint64_t s_full, s_free, p_full, pds_free, dq_full, dq_free, mma_done;
+  uint64_t s_full, s_free, p_full, pds_free, dq_full, dq_free, dqs_full, dqs_free, mma_done;
   uint32_t tmem;
 };
 
@@ -84,7 +86,7 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                       const __grid_constant__ CUtensorMap tl2, const __grid_constant__ CUtensorMap tds,
                       const __grid_constant__ CUtensorMap ttok,
-                      float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dk,
+                      const __grid_constant__ CUtensorMap tdq, __nv_bfloat16* __restrict__ dk,
                       __nv_bfloat16* __restrict__ dv, const int4* __restrict__ tok,
                       const BwdTile* __restrict__ tiles, int Hq, int Hkv, int Ttot,
                       float scale_log2, float scale, const float2* __restrict__ rope_tab,
@@ -119,6 +121,8 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     mbar_init(&sm.pds_free, 1);
     mbar_init(&sm.dq_full, 1);
     mbar_init(&sm.dq_free, 128);
+    mbar_init(&sm.dqs_full, 128);
+    mbar_init(&sm.dqs_free, 1);
     mbar_init(&sm.mma_done, 1);
     fence_mbar_init();
   }
@@ -391,6 +395,7 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     const int quarter = warp & 3;
     const int dd = quarter * 32 + lane;            // head-dim index = TMEM lane
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    const bool issuer = (warp == 10 && lane == 0);
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int h = kh * rep + it / nqt;
@@ -403,11 +408,26 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&sm.dq_free);
-      const int cn = min(BQ, tl.q_hi - qt);
-      float* dst = dq_acc + ((size_t)qt * Hq + h) * D + dd;
-#pragma unroll 4
-      for (int c = 0; c < cn; ++c) red_add(dst + (size_t)c * Hq * D, __uint_as_float(g[c]) * scale);
+      // The previous block's reduce must have finished reading the staging buffer.
+      if (it > 0 && !warp_wait(&sm.dqs_free, (it - 1) & 1, wait_ns)) { ok = false; break; }
+#pragma unroll
+      for (int c = 0; c < BQ; ++c) sm.dqs[c][dd] = __uint_as_float(g[c]) * scale;
+      fence_proxy_async_smem();
+      mbar_arrive(&sm.dqs_full);
+      if (issuer) {
+        if (!mbar_wait(&sm.dqs_full, it & 1, wait_ns)) {
+          ok = false;
+        } else {
+          // Rows past the group receive +0; rows past the tensor are clipped by the TMA unit.
+          tma_reduce_add_2d(&tdq, &sm.dqs[0][0], h * D, qt);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+          mbar_arrive(&sm.dqs_free);
+        }
+      }
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
     }
+    if (issuer) bulk_wait_group0();
     if (!ok) fail(PG_ERR_TIMEOUT);
   }
   tc_fence_before();
@@ -428,7 +448,7 @@ pg_status launch_bwd_sm100(const AttnArgs& a, const void* q, const void* k, cons
   const pg_layout* L = a.layout;
   const int64_t T = L->total_tokens;
   const int64_t Tp = padded_tokens(L);
-  CUtensorMap tq, tk, tv, tdo, tl2, tds, ttok;
+  CUtensorMap tq, tk, tv, tdo, tl2, tds, ttok, tdq;
   pg_status st = make_tmap_2d_bf16(&tq, q, (uint64_t)a.Hq * D, T, (uint64_t)a.Hq * D * 2, 64, BQ);
   if (st == PG_OK)
     st = make_tmap_2d_bf16(&tdo, dO, (uint64_t)a.Hq * D, T, (uint64_t)a.Hq * D * 2, 64, BQ);
@@ -439,6 +459,8 @@ pg_status launch_bwd_sm100(const AttnArgs& a, const void* q, const void* k, cons
   if (st == PG_OK) st = make_tmap_2d_b32(&tl2, lse2, true, Tp, a.Hq, Tp * 4, BQ, 1);
   if (st == PG_OK) st = make_tmap_2d_b32(&tds, Dbuf, true, Tp, a.Hq, Tp * 4, BQ, 1);
   if (st == PG_OK) st = make_tmap_2d_b32(&ttok, tokens(L), false, 4, T, 16, 4, BQ);
+  if (st == PG_OK)
+    st = make_tmap_2d_b32(&tdq, dq_acc, true, (uint64_t)a.Hq * D, T, (uint64_t)a.Hq * D * 4, D, BQ);
   if (st != PG_OK) return st;
   const size_t smem = sizeof(BwdSmem) + 1024;
   st = cuda_check(cudaFuncSetAttribute(attn_bwd_sm100_kernel,
@@ -447,7 +469,7 @@ pg_status launch_bwd_sm100(const AttnArgs& a, const void* q, const void* k, cons
   if (st != PG_OK) return st;
   prof_begin(PG_KERNEL_BWD_DKDV, a.stream);
   attn_bwd_sm100_kernel<<<(unsigned)(L->n_tiles[BWD128] * a.Hkv), NTHREADS, smem, a.stream>>>(
-      tq, tk, tv, tdo, tl2, tds, ttok, dq_acc, static_cast<__nv_bfloat16*>(dk),
+      tq, tk, tv, tdo, tl2, tds, ttok, tdq, static_cast<__nv_bfloat16*>(dk),
       static_cast<__nv_bfloat16*>(dv), tokens(L), tiles<BwdTile>(L, BWD128), a.Hq, a.Hkv, (int)T,
       a.scale * kLog2e, a.scale, rope_tab, 2000000000ull);
   prof_end(PG_KERNEL_BWD_DKDV, a.stream);
