@@ -80,8 +80,9 @@ typedef struct pg_layout {
   int64_t total_tokens;    /* T */
   int64_t max_position;    /* 1 + the largest position id */
   int64_t pairs;           /* visible (query, key) pairs per head, summed over groups */
-  int64_t n_tiles[4];      /* work-list lengths: fwd 64-row, fwd 128-row, bwd 64-key, bwd 128-key */
-  int64_t off_tiles[4];    /* byte offsets of those lists in the tables */
+  int64_t n_tiles[6];      /* work-list lengths: fwd 64-row, fwd 128-row, bwd 64-key, bwd 128-key,
+                              fwd 256-row, (unused) */
+  int64_t off_tiles[6];    /* byte offsets of those lists in the tables */
   int64_t off_tokens;      /* byte offset of the per-token table (16 bytes per token) */
   int64_t table_bytes;     /* bytes of the tables buffer in use */
   const int32_t* position_ids; /* [T] */

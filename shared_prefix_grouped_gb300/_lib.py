@@ -19,8 +19,8 @@ class PgLayout(C.Structure):
         ("total_tokens", C.c_int64),
         ("max_position", C.c_int64),
         ("pairs", C.c_int64),
-        ("n_tiles", C.c_int64 * 4),
-        ("off_tiles", C.c_int64 * 4),
+        ("n_tiles", C.c_int64 * 6),
+        ("off_tiles", C.c_int64 * 6),
         ("off_tokens", C.c_int64),
         ("table_bytes", C.c_int64),
         ("position_ids", C.c_void_p),

@@ -45,8 +45,8 @@ pg_status read_kernel_status(bool clear, int32_t* code) {
 
 struct Plan {
   int64_t T = 0, segs = 0, max_pos = 0, pairs = 0;
-  int64_t n[4] = {0, 0, 0, 0};
-  int64_t off[4] = {0, 0, 0, 0};
+  int64_t n[NUM_LISTS] = {0, 0, 0, 0, 0, 0};
+  int64_t off[NUM_LISTS] = {0, 0, 0, 0, 0, 0};
   int64_t off_tokens = 0, bytes = 0;
 };
 
@@ -92,20 +92,22 @@ static pg_status check_lengths(int32_t B, const int32_t* lp, const int32_t* gs, 
   p->max_pos = maxpos;
   p->pairs = pairs;
   // Work-list lengths: one tile per started block of rows in each group.
-  int64_t n64 = 0, n128 = 0;
+  int64_t n64 = 0, n128 = 0, n256 = 0;
   int64_t s = 0;
   for (int32_t b = 0; b < B; ++b) {
     int64_t len = lp[b];
     for (int32_t i = 0; i < gs[b]; ++i) len += rs[s++];
     n64 += (len + 63) / 64;
     n128 += (len + 127) / 128;
+    n256 += (len + 255) / 256;
   }
   p->n[FWD64] = p->n[BWD64] = n64;
   p->n[FWD128] = p->n[BWD128] = n128;
+  p->n[FWD256] = n256;
   int64_t off = 0;
   p->off_tokens = off;
   off = align_up(off + 16 * T, 256);
-  for (int w = 0; w < 4; ++w) {
+  for (int w = 0; w < NUM_LISTS; ++w) {
     p->off[w] = off;
     off = align_up(off + 32 * p->n[w], 256);
   }
@@ -145,8 +147,9 @@ static void build_tables(int32_t B, const int32_t* lp, const int32_t* gs, const 
       }
     }
   }
-  // Work lists, per group, for 64- and 128-row tiles; heaviest first.
-  for (int bm = 64, wi = 0; bm <= 128; bm *= 2, ++wi) {
+  // Work lists, per group, for 64-, 128- and 256-row tiles (no key-major list for 256); heaviest
+  // first.
+  for (int bm = 64, wi = 0; bm <= 256; bm *= 2, ++wi) {
     std::vector<FwdTile> ft;
     std::vector<BwdTile> bt;
     std::vector<int64_t> fc, bc;
@@ -188,9 +191,12 @@ static void build_tables(int32_t B, const int32_t* lp, const int32_t* gs, const 
     }
     sort_by_cost(ft, fc);
     sort_by_cost(bt, bc);
-    int fw = wi == 0 ? FWD64 : FWD128, bw = wi == 0 ? BWD64 : BWD128;
+    const int fw = wi == 0 ? FWD64 : wi == 1 ? FWD128 : FWD256;
     memcpy(tables + p.off[fw], ft.data(), ft.size() * sizeof(FwdTile));
-    memcpy(tables + p.off[bw], bt.data(), bt.size() * sizeof(BwdTile));
+    if (wi < 2) {
+      const int bw = wi == 0 ? BWD64 : BWD128;
+      memcpy(tables + p.off[bw], bt.data(), bt.size() * sizeof(BwdTile));
+    }
   }
 }
 
@@ -202,7 +208,7 @@ static void fill_layout(int32_t B, const Plan& p, const int32_t* pos, const void
   L->total_tokens = p.T;
   L->max_position = p.max_pos;
   L->pairs = p.pairs;
-  for (int w = 0; w < 4; ++w) {
+  for (int w = 0; w < NUM_LISTS; ++w) {
     L->n_tiles[w] = p.n[w];
     L->off_tiles[w] = p.off[w];
   }

@@ -10,16 +10,19 @@
 // buffer (its summation order is not fixed).
 //
 // Per query block (64 rows), with K, V resident in shared memory and Q, dO, the blocks' LSE (log2
-// units), rowsum(dO * O) and visibility entries arriving by TMA in a 2-stage ring:
+// units), rowsum(dO * O) and visibility entries arriving by TMA in a 3-stage ring (and fetched
+// into L2 two blocks before that):
 //   S^T  = K Q^T          M 128 keys x N 64 queries x K 128   (TMEM cols [0, 64))
 //   dP^T = V dO^T         M 128 x N 64 x K 128                 (TMEM cols [64, 128))
 //   P^T  = exp2(S^T * scale * log2 e - LSE_2[q]),  dS^T = P^T * (dP^T - Dsum[q])   (registers,
 //          one thread per key row, rounded to bf16 into shared memory)
 //   dV  += P^T dO         M 128 x N 128 dims x K 64           (TMEM cols [256, 384))
 //   dK  += dS^T Q         M 128 x N 128 x K 64                 (TMEM cols [384, 512))
-//   dQ^T = K^T dS^T       M 128 dims x N 64 queries x K 128    (TMEM cols [128, 192)),
-//          drained by four warps (one thread per head-dim lane) into a [64 x 128] fp32 block in
-//          shared memory, which one TMA bulk reduce-add adds into the global dQ accumulator.
+//   dQ^T = K^T dS^T       M 128 dims x N 64 queries x K 128    (TMEM cols [128, 256), two
+//          buffers used alternately), drained by four warps (one thread per head-dim lane): each
+//          warp stages its 32 head dims of the block, 32 query rows at a time ([32 x 32] fp32),
+//          in its own shared-memory buffer and adds them into the global dQ accumulator with TMA
+//          bulk reduce-adds.
 // The MMA thread issues S^T / dP^T of block i before the gradient products of block i-1, so the
 // tensor core computes the next scores while the softmax warps work on the current ones.
 // The epilogue applies the softmax scale and the inverse RoPE rotation to dK in registers (a
@@ -44,7 +47,8 @@ namespace {
 constexpr int D = 128;
 constexpr int BKV = 128;        // keys per CTA
 constexpr int BQ = 64;          // query rows per block
-constexpr int NSQ = 2;          // Q / dO stages
+constexpr int NSQ = 3;          // Q / dO stages
+constexpr int PREFETCH = 2;     // Q / dO blocks fetched into L2 this far ahead of their load
 constexpr uint32_t KHALF = BKV * 64 * 2;   // 16 KiB: [128 rows][64 cols] bf16
 constexpr uint32_t QHALF = BQ * 64 * 2;    // 8 KiB:  [64 rows][64 cols] bf16
 constexpr int NTHREADS = 448;
@@ -59,13 +63,13 @@ struct BwdSmem {
   uint8_t dO[NSQ][2 * QHALF];
   uint8_t p[KHALF];         // P^T  [128 keys][64 queries] bf16, SW128
   uint8_t ds[KHALF];        // dS^T [128 keys][64 queries]
-  alignas(1024) float dqs[BQ][D];   // dQ block staged for the bulk reduce-add
+  alignas(1024) float dqs[4][BQ / 2][32];   // per drain warp: half its slice of a dQ block
   alignas(128) float lse2[NSQ][BQ];
   alignas(128) float dsum[NSQ][BQ];
   alignas(128) int4 tokq[NSQ][BQ];   // per-token {g0, pe, own_lo, pos} of the block's queries
   uint64_t kv_full;
   uint64_t qd_full[NSQ], qd_empty[NSQ];
-  uint64_t s_full, s_free, p_full, pds_free, dq_full, dq_free, dqs_full, dqs_free, mma_done;
+  uint64_t s_full, s_free, p_full, pds_free, dq_full[2], dq_free[2], mma_done;
   uint32_t tmem;
 };
 
@@ -119,10 +123,10 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     mbar_init(&sm.s_free, 256);
     mbar_init(&sm.p_full, 256);
     mbar_init(&sm.pds_free, 1);
-    mbar_init(&sm.dq_full, 1);
-    mbar_init(&sm.dq_free, 128);
-    mbar_init(&sm.dqs_full, 128);
-    mbar_init(&sm.dqs_free, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.dq_full[b], 1);
+      mbar_init(&sm.dq_free[b], 128);
+    }
     mbar_init(&sm.mma_done, 1);
     fence_mbar_init();
   }
@@ -135,7 +139,7 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
   tc_fence_after();
   const uint32_t tmem = sm.tmem;
   const uint32_t t_s = tmem, t_dp = tmem + 64, t_dq = tmem + 128, t_dv = tmem + 256,
-                 t_dk = tmem + 384;
+                 t_dk = tmem + 384;   // dQ^T buffer b at t_dq + 64 b
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer ---------
@@ -162,6 +166,14 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       const int qt = qt0 + (it % nqt) * BQ;
       if (!warp_wait(&sm.qd_empty[st], ((it / NSQ) & 1) ^ 1, wait_ns)) { ok = false; break; }
       if (leader) {
+        const int ip = it + PREFETCH + NSQ;
+        if (ip < n_it) {
+          const int hp = kh * rep + ip / nqt, qp = qt0 + (ip % nqt) * BQ;
+          tma_prefetch_l2_2d(&tq, hp * D, qp);
+          tma_prefetch_l2_2d(&tq, hp * D + 64, qp);
+          tma_prefetch_l2_2d(&tdo, hp * D, qp);
+          tma_prefetch_l2_2d(&tdo, hp * D + 64, qp);
+        }
         mbar_expect_tx(&sm.qd_full[st], 4 * QHALF + 2 * BQ * 4 + BQ * 16);
         tma_load_2d(sm.q[st], &tq, &sm.qd_full[st], h * D, qt);
         tma_load_2d(sm.q[st] + QHALF, &tq, &sm.qd_full[st], h * D + 64, qt);
@@ -229,14 +241,18 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                    sdesc_sw128(qa + kk * 2048, QHALF, 1024), id_g, (jp | kk) != 0);
           }
           mma_commit(&sm.qd_empty[sp]);
-          if (jp > 0 && !mbar_wait(&sm.dq_free, (jp - 1) & 1, wait_ns)) { ok = false; break; }
+          const int b = jp & 1;
+          if (jp >= 2 && !mbar_wait(&sm.dq_free[b], ((jp >> 1) & 1) ^ 1, wait_ns)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < BKV / 16; ++kk) {
-            mma_ss(t_dq, sdesc_sw128(ka + kk * 2048, KHALF, 1024),
+            mma_ss(t_dq + 64 * b, sdesc_sw128(ka + kk * 2048, KHALF, 1024),
                    sdesc_sw128(dsa + kk * 2048, QHALF, 1024), id_q, kk != 0);
           }
-          mma_commit(&sm.dq_full);
+          mma_commit(&sm.dq_full[b]);
           mma_commit(&sm.pds_free);
         }
       }
@@ -392,42 +408,41 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     if (!ok) fail(PG_ERR_TIMEOUT);
   } else {
     // ------------------------------------------------------------------ dQ drain ---------
-    const int quarter = warp & 3;
-    const int dd = quarter * 32 + lane;            // head-dim index = TMEM lane
+    const int quarter = warp & 3;                  // this warp's 32 head dims (= TMEM lanes)
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-    const bool issuer = (warp == 10 && lane == 0);
+    float (*stage)[32] = sm.dqs[quarter];
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int h = kh * rep + it / nqt;
       const int qt = qt0 + (it % nqt) * BQ;
-      if (!warp_wait(&sm.dq_full, it & 1, wait_ns)) { ok = false; break; }
+      const int b = it & 1;
+      if (!warp_wait(&sm.dq_full[b], (it >> 1) & 1, wait_ns)) { ok = false; break; }
       tc_fence_after();
       uint32_t g[64];
-      tmem_ld32(t_dq + lane_addr, *reinterpret_cast<uint32_t(*)[32]>(&g[0]));
-      tmem_ld32(t_dq + lane_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&g[32]));
+      tmem_ld32(t_dq + 64 * b + lane_addr, *reinterpret_cast<uint32_t(*)[32]>(&g[0]));
+      tmem_ld32(t_dq + 64 * b + lane_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&g[32]));
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&sm.dq_free);
-      // The previous block's reduce must have finished reading the staging buffer.
-      if (it > 0 && !warp_wait(&sm.dqs_free, (it - 1) & 1, wait_ns)) { ok = false; break; }
+      mbar_arrive(&sm.dq_free[b]);
 #pragma unroll
-      for (int c = 0; c < BQ; ++c) sm.dqs[c][dd] = __uint_as_float(g[c]) * scale;
-      fence_proxy_async_smem();
-      mbar_arrive(&sm.dqs_full);
-      if (issuer) {
-        if (!mbar_wait(&sm.dqs_full, it & 1, wait_ns)) {
-          ok = false;
-        } else {
+      for (int hf = 0; hf < 2; ++hf) {
+        // This warp's previous reduce must have finished reading its staging buffer.
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < BQ / 2; ++c)
+          stage[c][lane] = __uint_as_float(g[hf * (BQ / 2) + c]) * scale;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
           // Rows past the group receive +0; rows past the tensor are clipped by the TMA unit.
-          tma_reduce_add_2d(&tdq, &sm.dqs[0][0], h * D, qt);
+          tma_reduce_add_2d(&tdq, &stage[0][0], h * D + quarter * 32, qt + hf * (BQ / 2));
           bulk_commit_group();
-          bulk_wait_group_read0();
-          mbar_arrive(&sm.dqs_free);
         }
       }
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
     }
-    if (issuer) bulk_wait_group0();
+    if (lane == 0) bulk_wait_group0();
+    __syncwarp();
     if (!ok) fail(PG_ERR_TIMEOUT);
   }
   tc_fence_before();
@@ -460,7 +475,8 @@ pg_status launch_bwd_sm100(const AttnArgs& a, const void* q, const void* k, cons
   if (st == PG_OK) st = make_tmap_2d_b32(&tds, Dbuf, true, Tp, a.Hq, Tp * 4, BQ, 1);
   if (st == PG_OK) st = make_tmap_2d_b32(&ttok, tokens(L), false, 4, T, 16, 4, BQ);
   if (st == PG_OK)
-    st = make_tmap_2d_b32(&tdq, dq_acc, true, (uint64_t)a.Hq * D, T, (uint64_t)a.Hq * D * 4, D, BQ);
+    st = make_tmap_2d_b32(&tdq, dq_acc, true, (uint64_t)a.Hq * D, T, (uint64_t)a.Hq * D * 4, 32,
+                          BQ / 2);
   if (st != PG_OK) return st;
   const size_t smem = sizeof(BwdSmem) + 1024;
   st = cuda_check(cudaFuncSetAttribute(attn_bwd_sm100_kernel,

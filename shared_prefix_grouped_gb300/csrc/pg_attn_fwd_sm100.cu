@@ -1,23 +1,27 @@
 // Grouped-attention forward on the 5th-generation tensor cores (bf16, head_dim 128).
 //
-// One CTA owns 128 packed query rows of one group and one query head (a FwdTile), and streams the
-// key/value tiles its rows can see: the group's prefix [g0, p_end) -- every response row sees all
-// of it, prefix rows causally -- then the responses' part [s_lo, s_hi) (Pith review of Prefix
-// Grouper, "What carries the argument": prefix self-attention plus suffix attention over the
-// prefix and the row's own response).  All CTAs of a group read the same prefix K/V tiles, which
-// stay resident in L2 across the group's query tiles and heads.
+// One CTA owns up to 256 packed query rows of one group -- two 128-row query tiles -- and one
+// query head (a 256-row FwdTile), and streams the key/value tiles those rows can see: the group's
+// prefix [g0, p_end) -- every response row sees all of it, prefix rows causally -- then the
+// responses' part [s_lo, s_hi) (Pith review of Prefix Grouper, "What carries the argument": prefix
+// self-attention plus suffix attention over the prefix and the row's own response).  Both query
+// tiles share each K/V tile loaded into shared memory, and all CTAs of a group read the same
+// prefix K/V tiles, which stay resident in L2 across the group's query tiles and heads.
 //
-// Warp roles (192 threads):
-//   warp 0      TMA producer: Q once, then K and V tiles into a 2-stage ring (128-byte swizzle)
-//   warp 1      TMEM allocation and the MMA issuer (one elected thread):
-//                 S = Q K^T   (M 128 x N 128 keys x K 128, fp32 in TMEM columns [0, 128))
-//                 O += P V    (M 128 x N 128 dims x K 128 keys, fp32 in TMEM columns [128, 256))
-//   warps 2..5  softmax, one thread per query row (TMEM lane = row): S from TMEM to registers,
-//               masking, online max / sum in fp32 (exp2 with the scale folded in), P rounded to
-//               bf16 into shared memory (the A operand of P V), O rescaled in TMEM when the
-//               running max grows by more than 2^8, and the final O / l, LSE epilogue.
-// The MMA thread issues S_{j+1} as soon as the softmax has read S_j, so the tensor core computes
-// the next scores while the softmax exponentiates the current ones.
+// Warp roles (320 threads):
+//   warp 0      TMA producer: Q tiles once, then 64-key K and V tiles into a 3-stage ring
+//   warp 1      TMEM allocation and the MMA issuer (one elected thread), per key tile j and
+//               query tile i:
+//                 S_i = Q_i K_j^T   (M 128 x N 64 keys x K 128; fp32 TMEM columns [64 i, 64 i + 64))
+//                 O_i += P_i V_j    (M 128 x N 128 dims x K 64; fp32 TMEM columns [128 + 128 i, ...))
+//               issued in the order S_0(0) S_1(0) PV_0(0) S_0(1) PV_1(0) S_1(1) PV_0(1) ..., so the
+//               tensor core works on one tile's products while the other tile's softmax runs
+//   warps 2..5  softmax of query tile 0, warps 6..9 of query tile 1: one thread per query row
+//               (TMEM lane = row); S from TMEM to registers, masking, online max / sum in fp32
+//               (exp2 with the scale folded in), P rounded to bf16 into shared memory (the A
+//               operand of P V), O rescaled in TMEM only when the running max grows by more than
+//               2^8, and the final O / l, LSE epilogue.
+// A key tile that lies entirely after the last row of query tile 0 is skipped for that tile.
 //
 // Every mbarrier wait is bounded (PG_ERR_TIMEOUT in the status word, then an orderly exit: copies
 // in flight are awaited, MMAs committed, TMEM freed).
@@ -34,12 +38,13 @@ using namespace sm100;
 namespace {
 
 constexpr int D = 128;          // head_dim
-constexpr int BM = 128;         // query rows per CTA
-constexpr int BN = 128;         // keys per tile
-constexpr int NS = 2;           // K/V pipeline stages
-constexpr uint32_t HALF = BM * 64 * 2;     // one 64-column SW128 half tile: 16 KiB
-constexpr uint32_t TILE = 2 * HALF;        // a 128 x 128 bf16 tile: 32 KiB
-constexpr int NTHREADS = 192;
+constexpr int BM = 128;         // query rows per query tile (two per CTA)
+constexpr int BN = 64;          // keys per tile
+constexpr int NS = 3;           // K/V pipeline stages
+constexpr uint32_t QHALF = BM * 64 * 2;    // [128 rows][64 dims] bf16: 16 KiB
+constexpr uint32_t KHALF = BN * 64 * 2;    // [64 keys][64 dims] bf16: 8 KiB
+constexpr uint32_t PTILE = BM * BN * 2;    // [128 rows][64 keys] bf16: 16 KiB
+constexpr int NTHREADS = 320;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -47,13 +52,14 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 __device__ int s_status_fwd = 0;
 
 struct FwdSmem {
-  uint8_t q[TILE];
-  uint8_t k[NS][TILE];
-  uint8_t v[NS][TILE];
-  uint8_t p[TILE];
+  uint8_t q[2][2 * QHALF];
+  uint8_t k[NS][2 * KHALF];
+  uint8_t v[NS][2 * KHALF];
+  uint8_t p[2][PTILE];
   uint64_t q_full;
   uint64_t k_full[NS], v_full[NS], kv_empty[NS];
-  uint64_t s_full, s_free, p_full, o_ready, mma_done;
+  uint64_t s_full[2], s_free[2], p_full[2], o_ready[2];
+  uint64_t mma_done;
   uint32_t tmem;
 };
 
@@ -65,16 +71,23 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 __device__ __forceinline__ void fail(int code) { atomicCAS(&s_status_fwd, 0, code); }
 
-// Key tile j of a CTA: tiles of the prefix range first, then of the responses' range.
-struct KeyTiles {
+// Key tile j of a CTA: tiles of the prefix range first, then of the responses' range; and which
+// query tiles need it.
+struct Plan {
   int g0, p_end, s_lo, s_hi, n_a, n;
-  __device__ KeyTiles(const FwdTile& t) {
+  int q0, q1;
+  int last[2];      // last query row of each query tile (-1: tile empty)
+  __device__ Plan(const FwdTile& t) {
     g0 = t.g0;
     p_end = t.p_end;
     s_lo = t.s_lo;
     s_hi = t.s_hi;
+    q0 = t.q0;
+    q1 = t.q1;
     n_a = (p_end - g0 + BN - 1) / BN;
     n = n_a + (s_hi - s_lo + BN - 1) / BN;
+    last[0] = min(q0 + BM, q1) - 1;
+    last[1] = (q1 > q0 + BM) ? q1 - 1 : -1;
   }
   __device__ void get(int j, int& kt, int& hi) const {
     if (j < n_a) {
@@ -84,6 +97,11 @@ struct KeyTiles {
       kt = s_lo + (j - n_a) * BN;
       hi = s_hi;
     }
+  }
+  __device__ bool rel(int i, int j) const {
+    int kt, hi;
+    get(j, kt, hi);
+    return last[i] >= 0 && kt <= last[i];
   }
 };
 
@@ -100,13 +118,14 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
   const int tile_id = blockIdx.x / Hq, h = blockIdx.x % Hq;
   const int kh = h / (Hq / Hkv);
   const FwdTile tl = tiles[tile_id];
-  if (tl.q0 < 0 || tl.q1 > Ttot || tl.q0 >= tl.q1 || tl.q1 - tl.q0 > BM || tl.g0 < 0 ||
+  if (tl.q0 < 0 || tl.q1 > Ttot || tl.q0 >= tl.q1 || tl.q1 - tl.q0 > 2 * BM || tl.g0 < 0 ||
       tl.s_hi > Ttot) {
     if (threadIdx.x == 0) fail(PG_ERR_DEVICE);
     return;
   }
-  const KeyTiles kts(tl);
-  const int n = kts.n;
+  const Plan pl(tl);
+  const int n = pl.n;
+  const int nq = pl.last[1] >= 0 ? 2 : 1;
 
   if (threadIdx.x == 0) {
     mbar_init(&sm.q_full, 1);
@@ -115,22 +134,23 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       mbar_init(&sm.v_full[s], 1);
       mbar_init(&sm.kv_empty[s], 1);
     }
-    mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.s_free, 128);
-    mbar_init(&sm.p_full, 128);
-    mbar_init(&sm.o_ready, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.s_full[i], 1);
+      mbar_init(&sm.s_free[i], 128);
+      mbar_init(&sm.p_full[i], 128);
+      mbar_init(&sm.o_ready[i], 1);
+    }
     mbar_init(&sm.mma_done, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&sm.tmem, 256);
+    tmem_alloc(&sm.tmem, 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem;
-  const uint32_t tmem_s = tmem, tmem_o = tmem + 128;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer -----
@@ -139,25 +159,26 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
       const int xq = h * D, xk = kh * D;
-      mbar_expect_tx(&sm.q_full, TILE);
-      tma_load_2d(sm.q, &tq, &sm.q_full, xq, tl.q0);
-      tma_load_2d(sm.q + HALF, &tq, &sm.q_full, xq + 64, tl.q0);
+      mbar_expect_tx(&sm.q_full, nq * 2 * QHALF);
+      for (int i = 0; i < nq; ++i) {
+        tma_load_2d(sm.q[i], &tq, &sm.q_full, xq, tl.q0 + i * BM);
+        tma_load_2d(sm.q[i] + QHALF, &tq, &sm.q_full, xq + 64, tl.q0 + i * BM);
+      }
       int issued = 0;
       for (int j = 0; j < n; ++j) {
         const int s = j % NS;
-        const uint32_t ph = (j / NS) & 1;
-        if (!mbar_wait(&sm.kv_empty[s], ph ^ 1, wait_ns)) {
+        if (!mbar_wait(&sm.kv_empty[s], ((j / NS) & 1) ^ 1, wait_ns)) {
           fail(PG_ERR_TIMEOUT);
           break;
         }
         int kt, hi;
-        kts.get(j, kt, hi);
-        mbar_expect_tx(&sm.k_full[s], TILE);
+        pl.get(j, kt, hi);
+        mbar_expect_tx(&sm.k_full[s], 2 * KHALF);
         tma_load_2d(sm.k[s], &tk, &sm.k_full[s], xk, kt);
-        tma_load_2d(sm.k[s] + HALF, &tk, &sm.k_full[s], xk + 64, kt);
-        mbar_expect_tx(&sm.v_full[s], TILE);
+        tma_load_2d(sm.k[s] + KHALF, &tk, &sm.k_full[s], xk + 64, kt);
+        mbar_expect_tx(&sm.v_full[s], 2 * KHALF);
         tma_load_2d(sm.v[s], &tv, &sm.v_full[s], xk, kt);
-        tma_load_2d(sm.v[s] + HALF, &tv, &sm.v_full[s], xk + 64, kt);
+        tma_load_2d(sm.v[s] + KHALF, &tv, &sm.v_full[s], xk + 64, kt);
         ++issued;
       }
       // Leave no copy in flight: the last stages' loads must have landed before exit.
@@ -173,38 +194,52 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     if (elect_one()) {
       constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16(BM, D, 0, 1);
-      const uint32_t q0a = smem_u32(sm.q), pa = smem_u32(sm.p);
+      int cnt[2] = {0, 0};        // products of each query tile issued so far (= its tiles done)
+      bool s_issued[2] = {false, false};
       bool ok = mbar_wait(&sm.q_full, 0, wait_ns);
-      for (int j = 0; ok && j <= n; ++j) {
-        if (j < n) {
-          const int s = j % NS;
-          if (!mbar_wait(&sm.k_full[s], (j / NS) & 1, wait_ns)) { ok = false; break; }
-          if (j > 0 && !mbar_wait(&sm.s_free, (j - 1) & 1, wait_ns)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t ka = smem_u32(sm.k[s]);
+      // S_i(j): scores of query tile i against key tile j (needs the K tile and a free S_i).
+      auto issue_s = [&](int i, int j) -> bool {
+        if (!mbar_wait(&sm.k_full[j % NS], (j / NS) & 1, wait_ns)) return false;
+        if (cnt[i] > 0 && !mbar_wait(&sm.s_free[i], (cnt[i] - 1) & 1, wait_ns)) return false;
+        tc_fence_after();
+        const uint32_t qa = smem_u32(sm.q[i]), ka = smem_u32(sm.k[j % NS]);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
-            mma_ss(tmem_s, sdesc_sw128(q0a + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                   idesc_s, kk != 0);
-          }
-          mma_commit(&sm.s_full);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t qo = (kk >> 2) * QHALF + (kk & 3) * 32;
+          const uint32_t ko = (kk >> 2) * KHALF + (kk & 3) * 32;
+          mma_ss(tmem + 64 * i, sdesc_sw128(qa + qo, 16, 1024), sdesc_sw128(ka + ko, 16, 1024),
+                 idesc_s, kk != 0);
         }
-        if (j > 0) {
-          const int jp = j - 1, s = jp % NS;
-          if (!mbar_wait(&sm.p_full, jp & 1, wait_ns)) { ok = false; break; }
-          if (!mbar_wait(&sm.v_full[s], (jp / NS) & 1, wait_ns)) { ok = false; break; }
+        mma_commit(&sm.s_full[i]);
+        return true;
+      };
+      for (int j = 0; ok && j < n; ++j) {
+        for (int i = 0; i < nq && ok; ++i)
+          if (pl.rel(i, j) && !s_issued[i]) {
+            ok = issue_s(i, j);
+            s_issued[i] = true;
+          }
+        if (!ok) break;
+        if (!mbar_wait(&sm.v_full[j % NS], (j / NS) & 1, wait_ns)) { ok = false; break; }
+        for (int i = 0; i < nq && ok; ++i) {
+          if (!pl.rel(i, j)) continue;
+          if (!mbar_wait(&sm.p_full[i], cnt[i] & 1, wait_ns)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t va = smem_u32(sm.v[s]);
+          const uint32_t pa = smem_u32(sm.p[i]), va = smem_u32(sm.v[j % NS]);
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint32_t poff = (kk >> 2) * HALF + (kk & 3) * 32;
-            mma_ss(tmem_o, sdesc_sw128(pa + poff, 16, 1024),
-                   sdesc_sw128(va + kk * 2048, HALF, 1024), idesc_pv, (jp | kk) != 0);
+            mma_ss(tmem + 128 + 128 * i, sdesc_sw128(pa + kk * 32, 16, 1024),
+                   sdesc_sw128(va + kk * 2048, KHALF, 1024), idesc_pv, (cnt[i] | kk) != 0);
           }
-          mma_commit(&sm.kv_empty[s]);
-          mma_commit(&sm.o_ready);
+          mma_commit(&sm.o_ready[i]);
+          ++cnt[i];
+          s_issued[i] = false;
+          if (j + 1 < n && pl.rel(i, j + 1)) {
+            ok = issue_s(i, j + 1);
+            s_issued[i] = true;
+          }
         }
+        mma_commit(&sm.kv_empty[j % NS]);
       }
       if (!ok) fail(PG_ERR_TIMEOUT);
       // Every MMA issued above completes before TMEM is released.
@@ -214,46 +249,51 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ softmax ----------
+    const int i = (warp - 2) >> 2;                // query tile of this warpgroup
     const int quarter = warp & 3;                 // TMEM lanes this warp may access
     const int r = quarter * 32 + lane;            // query row within the tile
-    const int row = tl.q0 + r;
-    const bool valid = row < tl.q1;
-    const int rowc = valid ? row : tl.q1 - 1;
+    const int row = tl.q0 + i * BM + r;
+    const int qlast = pl.last[i];
+    const bool active = qlast >= 0;
+    const bool valid = active && row <= qlast;
+    const int rowc = valid ? row : (active ? qlast : tl.q0);
     const int4 ti = tok[rowc];                    // {g0, pe, own_lo, pos}
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    const uint32_t t_s = tmem + 64 * i, t_o = tmem + 128 + 128 * i;
+    const int first_row = tl.q0 + i * BM;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    uint8_t* prow = sm.p;
-    for (int j = 0; j < n; ++j) {
+    int c = 0;
+    uint8_t* prow = sm.p[i];
+    for (int j = 0; active && j < n; ++j) {
+      if (!pl.rel(i, j)) continue;
       int kt, hi;
-      kts.get(j, kt, hi);
-      if (!warp_wait(&sm.s_full, j & 1, wait_ns)) { ok = false; break; }
+      pl.get(j, kt, hi);
+      if (!warp_wait(&sm.s_full[i], c & 1, wait_ns)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sr[128];
-      tmem_ld32(tmem_s + lane_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(tmem_s + lane_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tmem_ld32(tmem_s + lane_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
-      tmem_ld32(tmem_s + lane_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+      uint32_t sr[64];
+      tmem_ld32(t_s + lane_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(t_s + lane_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&sm.s_free);
+      mbar_arrive(&sm.s_free[i]);
       // Scores in log2 units; mask where the tile is not entirely visible to every row.
-      const bool full_tile = (j < kts.n_a) && (kt + BN <= hi) && (kt + BN - 1 <= tl.q0);
+      const bool full_tile = (j < pl.n_a) && (kt + BN <= hi) && (kt + BN - 1 <= first_row);
       float mx = -INFINITY;
       if (full_tile) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const float x = __uint_as_float(sr[c]) * scale_log2;
-          sr[c] = __float_as_uint(x);
+        for (int cc = 0; cc < BN; ++cc) {
+          const float x = __uint_as_float(sr[cc]) * scale_log2;
+          sr[cc] = __float_as_uint(x);
           mx = fmaxf(mx, x);
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const int s = kt + c;
+        for (int cc = 0; cc < BN; ++cc) {
+          const int s = kt + cc;
           const bool vis = s < hi && s <= rowc && s >= ti.x && (s < ti.y || s >= ti.z);
-          const float x = vis ? __uint_as_float(sr[c]) * scale_log2 : -INFINITY;
-          sr[c] = __float_as_uint(x);
+          const float x = vis ? __uint_as_float(sr[cc]) * scale_log2 : -INFINITY;
+          sr[cc] = __float_as_uint(x);
           mx = fmaxf(mx, x);
         }
       }
@@ -266,66 +306,68 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
         l *= corr;
       }
       const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-      // P V of the previous tile must be complete before O is rescaled or P is overwritten.
-      if (j > 0) {
-        if (!warp_wait(&sm.o_ready, (j - 1) & 1, wait_ns)) { ok = false; break; }
+      // P = exp2(s - m), rounded to bf16.
+      uint32_t pw[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const float p0 = fast_exp2(__uint_as_float(sr[2 * e]) - mref);
+        const float p1 = fast_exp2(__uint_as_float(sr[2 * e + 1]) - mref);
+        l += p0 + p1;
+        pw[e] = pack_bf16x2(p0, p1);
+      }
+      // P V of this tile's previous key tile must be complete before O is rescaled or P is
+      // overwritten.
+      if (c > 0) {
+        if (!warp_wait(&sm.o_ready[i], (c - 1) & 1, wait_ns)) { ok = false; break; }
         tc_fence_after();
         if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t orr[32];
-            tmem_ld32(tmem_o + lane_addr + c * 32, orr);
+            tmem_ld32(t_o + lane_addr + q4 * 32, orr);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * corr);
-            tmem_st32(tmem_o + lane_addr + c * 32, orr);
+            for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * corr);
+            tmem_st32(t_o + lane_addr + q4 * 32, orr);
           }
           tmem_st_wait();
         }
       }
-      // P = exp2(s - m), rounded to bf16, written as the SW128 K-major A operand.
 #pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        uint32_t w4[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = fast_exp2(__uint_as_float(sr[ch * 8 + 2 * e]) - mref);
-          const float p1 = fast_exp2(__uint_as_float(sr[ch * 8 + 2 * e + 1]) - mref);
-          l += p0 + p1;
-          w4[e] = pack_bf16x2(p0, p1);
-        }
-        const uint32_t off = (ch >> 3) * HALF + sw128_offset(r, ch & 7);
-        *reinterpret_cast<uint4*>(prow + off) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      for (int ch = 0; ch < 8; ++ch) {
+        *reinterpret_cast<uint4*>(prow + sw128_offset(r, ch)) =
+            make_uint4(pw[4 * ch], pw[4 * ch + 1], pw[4 * ch + 2], pw[4 * ch + 3]);
       }
+      ++c;
       if (debug & PG_DEBUG_WITHHOLD_P) continue;   // test hook: never signal P (bounded waits)
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&sm.p_full);
+      mbar_arrive(&sm.p_full[i]);
     }
     // Epilogue: O / l and the natural-log LSE.
-    if (ok && n > 0 && warp_wait(&sm.o_ready, (n - 1) & 1, wait_ns)) {
+    if (active && ok && c > 0 && warp_wait(&sm.o_ready[i], (c - 1) & 1, wait_ns)) {
       tc_fence_after();
       const float inv = 1.f / l;
       __nv_bfloat16* orow = o + ((size_t)rowc * Hq + h) * D;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t orr[32];
-        tmem_ld32(tmem_o + lane_addr + c * 32, orr);
+        tmem_ld32(t_o + lane_addr + q4 * 32, orr);
         tmem_ld_wait();
         if (valid) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 8) {
+          for (int e = 0; e < 32; e += 8) {
             uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(orr[i]) * inv, __uint_as_float(orr[i + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(orr[i + 2]) * inv, __uint_as_float(orr[i + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(orr[i + 4]) * inv, __uint_as_float(orr[i + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(orr[i + 6]) * inv, __uint_as_float(orr[i + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + c * 32 + i) = w;
+            w.x = pack_bf16x2(__uint_as_float(orr[e]) * inv, __uint_as_float(orr[e + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(orr[e + 2]) * inv, __uint_as_float(orr[e + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(orr[e + 4]) * inv, __uint_as_float(orr[e + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(orr[e + 6]) * inv, __uint_as_float(orr[e + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + q4 * 32 + e) = w;
           }
         }
       }
       if (valid) lse[(size_t)h * Ttot + row] = (m_used + log2f(l)) * kLn2;
-    } else if (n > 0) {
+    } else if (active && c > 0) {
       ok = false;
     }
     if (!ok) fail(PG_ERR_TIMEOUT);
@@ -334,7 +376,7 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -360,8 +402,8 @@ pg_status launch_fwd_sm100(const AttnArgs& a, const void* q, const void* k, cons
   if (st != PG_OK) return st;
   const uint64_t wait_ns = (a.debug & PG_DEBUG_WITHHOLD_P) ? 50000000ull : 2000000000ull;
   prof_begin(PG_KERNEL_ATTN_FWD, a.stream);
-  attn_fwd_sm100_kernel<<<(unsigned)(L->n_tiles[FWD128] * a.Hq), NTHREADS, smem, a.stream>>>(
-      tq, tk, tv, static_cast<__nv_bfloat16*>(o), lse, tokens(L), tiles<FwdTile>(L, FWD128),
+  attn_fwd_sm100_kernel<<<(unsigned)(L->n_tiles[FWD256] * a.Hq), NTHREADS, smem, a.stream>>>(
+      tq, tk, tv, static_cast<__nv_bfloat16*>(o), lse, tokens(L), tiles<FwdTile>(L, FWD256),
       a.Hq, a.Hkv, (int)T, a.scale * kLog2e, wait_ns, a.debug);
   prof_end(PG_KERNEL_ATTN_FWD, a.stream);
   return cuda_check(cudaGetLastError(), "fwd sm100 launch");

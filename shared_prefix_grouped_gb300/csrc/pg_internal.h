@@ -33,7 +33,7 @@ struct BwdTile {
 static_assert(sizeof(FwdTile) == 32, "FwdTile layout");
 static_assert(sizeof(BwdTile) == 32, "BwdTile layout");
 
-enum TileList { FWD64 = 0, FWD128 = 1, BWD64 = 2, BWD128 = 3 };
+enum TileList { FWD64 = 0, FWD128 = 1, BWD64 = 2, BWD128 = 3, FWD256 = 4, NUM_LISTS = 6 };
 
 // Row stride (elements) of the per-head fp32 rows the backward keeps for LSE and rowsum(dO * O):
 // T rounded up to a multiple of 4, so every row starts 16-byte aligned (a TMA requirement).

@@ -62,7 +62,7 @@ def unpack(tab, struct):
     tok = torch.frombuffer(bytearray(raw[struct.off_tokens: struct.off_tokens + 16 * T]),
                            dtype=torch.int32).view(T, 4).clone()
     lists = []
-    for w in range(4):
+    for w in range(6):
         n = struct.n_tiles[w]
         o = struct.off_tiles[w]
         lists.append(torch.frombuffer(bytearray(raw[o: o + 32 * n]), dtype=torch.int32)
@@ -83,7 +83,7 @@ def test_pack_host_matches_oracle_bit_exactly(case):
     assert torch.equal(expand_mask(tok), mask)
     assert st.pairs == int(mask.sum()) == flops.total_pairs(plens, gsz, rs)
     T = lay.total_tokens
-    for w, bm in [(0, 64), (1, 128)]:
+    for w, bm in [(0, 64), (1, 128), (4, 256)]:
         ft = lists[w]
         # forward tiles: cover every row once; their key ranges cover every visible key
         covered = torch.zeros(T, dtype=torch.int32)
