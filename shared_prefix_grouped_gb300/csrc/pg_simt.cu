@@ -39,6 +39,14 @@ struct Vec<float> {
   }
   static __device__ __forceinline__ float load(const float* p) { return *p; }
   static __device__ __forceinline__ void store(float* p, float v) { *p = v; }
+  static __device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+  static __device__ __forceinline__ void store8(float* p, const float (&v)[8]) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
 };
 
 template <>
@@ -63,6 +71,25 @@ struct Vec<__nv_bfloat16> {
   }
   static __device__ __forceinline__ void store(__nv_bfloat16* p, float v) {
     *p = __float2bfloat16_rn(v);
+  }
+  static __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  }
+  static __device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&v)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 };
 
@@ -115,18 +142,27 @@ __global__ void rope_kernel(const Tin* __restrict__ x0, Tout* __restrict__ y0, i
     sn[threadIdx.x] = sgn * s;
   }
   __syncthreads();
+  // Each thread rotates 8 consecutive pairs (16-byte loads of bf16, 32-byte of fp32).
+  const int chunks = half >> 3;
   for (int which = 0; which < 2; ++which) {
     const Tin* x = which ? x1 : x0;
     Tout* y = which ? y1 : y0;
     const int heads = which ? h1 : h0;
     const size_t base = (size_t)t * heads * d;
-    for (int idx = threadIdx.x; idx < heads * half; idx += blockDim.x) {
-      int h = idx / half, k = idx - h * half;
-      size_t i1 = base + (size_t)h * d + k;
-      float a = Vec<Tin>::load(x + i1), b = Vec<Tin>::load(x + i1 + half);
-      float c = cs[k], s = sn[k];
-      Vec<Tout>::store(y + i1, a * c - b * s);
-      Vec<Tout>::store(y + i1 + half, b * c + a * s);
+    for (int idx = threadIdx.x; idx < heads * chunks; idx += blockDim.x) {
+      const int h = idx / chunks, k0 = (idx - h * chunks) * 8;
+      const size_t i1 = base + (size_t)h * d + k0;
+      float a[8], b[8], lo[8], hi[8];
+      Vec<Tin>::load8(x + i1, a);
+      Vec<Tin>::load8(x + i1 + half, b);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float c = cs[k0 + e], s = sn[k0 + e];
+        lo[e] = a[e] * c - b[e] * s;
+        hi[e] = b[e] * c + a[e] * s;
+      }
+      Vec<Tout>::store8(y + i1, lo);
+      Vec<Tout>::store8(y + i1 + half, hi);
     }
   }
 }
