@@ -14,8 +14,8 @@
 //               query tile i:
 //                 S_i = Q_i K_j^T   (M 128 x N 64 keys x K 128; fp32 TMEM columns [64 i, 64 i + 64))
 //                 O_i += P_i V_j    (M 128 x N 128 dims x K 64; fp32 TMEM columns [128 + 128 i, ...))
-//               issued in the order S_0(0) S_1(0) PV_0(0) S_0(1) PV_1(0) S_1(1) PV_0(1) ..., so the
-//               tensor core works on one tile's products while the other tile's softmax runs
+//               issued in the order S_0(0) S_1(0), then per key tile S_0(j+1) S_1(j+1) PV_0(j)
+//               PV_1(j): the next scores are computed while both softmax warpgroups work
 //   warps 2..5  softmax of query tile 0, warps 6..9 of query tile 1: one thread per query row
 //               (TMEM lane = row); S from TMEM to registers, masking, online max / sum in fp32
 //               (exp2 with the scale folded in), P rounded to bf16 into shared memory (the A
@@ -55,10 +55,12 @@ struct FwdSmem {
   uint8_t q[2][2 * QHALF];
   uint8_t k[NS][2 * KHALF];
   uint8_t v[NS][2 * KHALF];
-  uint8_t p[2][PTILE];
+  uint8_t p[2][2][PTILE];   // [query tile][buffer]
   uint64_t q_full;
   uint64_t k_full[NS], v_full[NS], kv_empty[NS];
-  uint64_t s_full[2], s_free[2], p_full[2], o_ready[2];
+  uint64_t s_full[2], s_free[2];
+  uint64_t p_full[2][2];    // P of [query tile][buffer] written
+  uint64_t pv_done[2][2];   // the P V product reading [query tile][buffer] has completed
   uint64_t mma_done;
   uint32_t tmem;
 };
@@ -137,8 +139,10 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.s_full[i], 1);
       mbar_init(&sm.s_free[i], 128);
-      mbar_init(&sm.p_full[i], 128);
-      mbar_init(&sm.o_ready[i], 1);
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&sm.p_full[i][b], 128);
+        mbar_init(&sm.pv_done[i][b], 1);
+      }
     }
     mbar_init(&sm.mma_done, 1);
     fence_mbar_init();
@@ -194,13 +198,14 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     if (elect_one()) {
       constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16(BM, D, 0, 1);
-      int cnt[2] = {0, 0};        // products of each query tile issued so far (= its tiles done)
-      bool s_issued[2] = {false, false};
+      int n_s[2] = {0, 0};        // S products issued per query tile
+      int n_pv[2] = {0, 0};       // P V products issued per query tile
       bool ok = mbar_wait(&sm.q_full, 0, wait_ns);
-      // S_i(j): scores of query tile i against key tile j (needs the K tile and a free S_i).
+      // S_i(j): scores of query tile i against key tile j.  Needs the K tile and the softmax of
+      // tile i to have read its previous scores out of TMEM (S_i is single-buffered).
       auto issue_s = [&](int i, int j) -> bool {
         if (!mbar_wait(&sm.k_full[j % NS], (j / NS) & 1, wait_ns)) return false;
-        if (cnt[i] > 0 && !mbar_wait(&sm.s_free[i], (cnt[i] - 1) & 1, wait_ns)) return false;
+        if (n_s[i] > 0 && !mbar_wait(&sm.s_free[i], (n_s[i] - 1) & 1, wait_ns)) return false;
         tc_fence_after();
         const uint32_t qa = smem_u32(sm.q[i]), ka = smem_u32(sm.k[j % NS]);
 #pragma unroll
@@ -211,33 +216,31 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                  idesc_s, kk != 0);
         }
         mma_commit(&sm.s_full[i]);
+        ++n_s[i];
         return true;
       };
+      // Order: S_0(0) S_1(0), then per key tile j: S_0(j+1) S_1(j+1) PV_0(j) PV_1(j).  The next
+      // scores are computed while the softmax warps turn the current ones into P.
+      for (int i = 0; i < nq && ok; ++i)
+        if (pl.rel(i, 0)) ok = issue_s(i, 0);
       for (int j = 0; ok && j < n; ++j) {
         for (int i = 0; i < nq && ok; ++i)
-          if (pl.rel(i, j) && !s_issued[i]) {
-            ok = issue_s(i, j);
-            s_issued[i] = true;
-          }
+          if (j + 1 < n && pl.rel(i, j + 1)) ok = issue_s(i, j + 1);
         if (!ok) break;
         if (!mbar_wait(&sm.v_full[j % NS], (j / NS) & 1, wait_ns)) { ok = false; break; }
         for (int i = 0; i < nq && ok; ++i) {
           if (!pl.rel(i, j)) continue;
-          if (!mbar_wait(&sm.p_full[i], cnt[i] & 1, wait_ns)) { ok = false; break; }
+          const int b = n_pv[i] & 1;
+          if (!mbar_wait(&sm.p_full[i][b], (n_pv[i] >> 1) & 1, wait_ns)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t pa = smem_u32(sm.p[i]), va = smem_u32(sm.v[j % NS]);
+          const uint32_t pa = smem_u32(sm.p[i][b]), va = smem_u32(sm.v[j % NS]);
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
             mma_ss(tmem + 128 + 128 * i, sdesc_sw128(pa + kk * 32, 16, 1024),
-                   sdesc_sw128(va + kk * 2048, KHALF, 1024), idesc_pv, (cnt[i] | kk) != 0);
+                   sdesc_sw128(va + kk * 2048, KHALF, 1024), idesc_pv, (n_pv[i] | kk) != 0);
           }
-          mma_commit(&sm.o_ready[i]);
-          ++cnt[i];
-          s_issued[i] = false;
-          if (j + 1 < n && pl.rel(i, j + 1)) {
-            ok = issue_s(i, j + 1);
-            s_issued[i] = true;
-          }
+          mma_commit(&sm.pv_done[i][b]);
+          ++n_pv[i];
         }
         mma_commit(&sm.kv_empty[j % NS]);
       }
@@ -264,7 +267,6 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     int c = 0;
-    uint8_t* prow = sm.p[i];
     for (int j = 0; active && j < n; ++j) {
       if (!pl.rel(i, j)) continue;
       int kt, hi;
@@ -315,12 +317,23 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
         l += p0 + p1;
         pw[e] = pack_bf16x2(p0, p1);
       }
-      // P V of this tile's previous key tile must be complete before O is rescaled or P is
-      // overwritten.
-      if (c > 0) {
-        if (!warp_wait(&sm.o_ready[i], (c - 1) & 1, wait_ns)) { ok = false; break; }
+      // P is double-buffered: the product that read this buffer two key tiles ago must be done.
+      // Rescaling O needs the previous key tile's product done too.
+      const int b = c & 1;
+      const bool any_rescale = __any_sync(0xffffffffu, rescale) && c > 0;
+      if (any_rescale) {
+        if (!warp_wait(&sm.pv_done[i][(c - 1) & 1], ((c - 1) >> 1) & 1, wait_ns)) {
+          ok = false;
+          break;
+        }
+      }
+      if (c >= 2 && !warp_wait(&sm.pv_done[i][b], ((c >> 1) - 1) & 1, wait_ns)) {
+        ok = false;
+        break;
+      }
+      if (any_rescale) {
         tc_fence_after();
-        if (__any_sync(0xffffffffu, rescale)) {
+        {
 #pragma unroll 1
           for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t orr[32];
@@ -333,6 +346,7 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
           tmem_st_wait();
         }
       }
+      uint8_t* prow = sm.p[i][b];
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
         *reinterpret_cast<uint4*>(prow + sw128_offset(r, ch)) =
@@ -342,10 +356,11 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       if (debug & PG_DEBUG_WITHHOLD_P) continue;   // test hook: never signal P (bounded waits)
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&sm.p_full[i]);
+      mbar_arrive(&sm.p_full[i][b]);
     }
     // Epilogue: O / l and the natural-log LSE.
-    if (active && ok && c > 0 && warp_wait(&sm.o_ready[i], (c - 1) & 1, wait_ns)) {
+    if (active && ok && c > 0 &&
+        warp_wait(&sm.pv_done[i][(c - 1) & 1], ((c - 1) >> 1) & 1, wait_ns)) {
       tc_fence_after();
       const float inv = 1.f / l;
       __nv_bfloat16* orow = o + ((size_t)rowc * Hq + h) * D;
