@@ -35,6 +35,24 @@ METRIC = "grouped-attn fwd+bwd TFLOP/s, tokens/s & % BF16 peak vs repeated-prefi
 DEFAULT_WORKLOAD = workloads.WORKLOADS[1].name
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 L2_BYTES = 129 * 2 ** 20
+# DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu capture summarised
+# in profiles/attn_bwd_sm100_bf16_mha_h32_d128_p4096_g8_r512.md.  Reported only while the kernel
+# source still has the hash it had when the counters were taken, and only for that workload.
+TRAFFIC = {"file": "shared_prefix_grouped_gb300/csrc/pg_attn_bwd_sm100.cu",
+           "sha256": "7085307c4268dac09cb156abb56f4ba12e2df383166876872dac39ce0518d997",
+           "workload": "bf16_mha_h32_d128_p4096_g8_r512", "bytes": 2637393924}
+
+
+def measured_traffic(workload: str):
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, TRAFFIC["file"]), "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    if sha != TRAFFIC["sha256"] or workload != TRAFFIC["workload"]:
+        return None
+    return TRAFFIC["bytes"]
 
 
 def load_peaks():
@@ -348,7 +366,9 @@ def run_ours(args):
             "roofline": {"bound": "tensor", "kernel": "bwd dK/dV (+dQ)",
                          "achieved": dom_flops / dom_sec / 1e12, "peak": peak,
                          "unit": "TFLOP/s", "frac": dom_flops / dom_sec / 1e12 / peak,
-                         "traffic": None, "peak_source": f"bf16 dense burst, {peak_src}"},
+                         "traffic": measured_traffic(w.name),
+                         "traffic_unit": "bytes per launch (ncu dram read + write)",
+                         "peak_source": f"bf16 dense burst, {peak_src}"},
             "clocks": clocks, "gpu_launches": int(prof.launches)}
     if rank == 0 and not args.skip_extras:
         line["e2e"] = e2e_leg(step, prob, device, args, step_flops, world)
