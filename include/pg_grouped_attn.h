@@ -170,7 +170,8 @@ typedef enum pg_kernel {
   PG_KERNEL_BWD_DKDV = 4,        /* key-major dK/dV (and dQ where fused) */
   PG_KERNEL_BWD_DQ = 5,          /* query-major dQ */
   PG_KERNEL_ROPE_BWD = 6,        /* inverse RoPE of dQ/dK and the cast to the output dtype */
-  PG_KERNEL_GEMM = 7             /* the bf16 tensor-core GEMM (decoder-layer path) */
+  PG_KERNEL_GEMM = 7,            /* the bf16 tensor-core GEMM (decoder-layer path) */
+  PG_KERNEL_LAYER = 8            /* RMSNorm / SwiGLU kernels of the decoder-layer path */
 } pg_kernel;
 
 /*

@@ -16,18 +16,56 @@ extern "C" {
 #endif
 
 /*
- * C[m, n] = sum_k A(m, k) * B(n, k) on the tensor cores (bf16 inputs, fp32 accumulation).
+ * C[m, n] (+)= sum_k A(m, k) * B(n, k) on the tensor cores (bf16 inputs, fp32 accumulation).
  *   A(m, k) = A[m * lda + k] if a_mn == 0 (row-major [M, K]), A[k * lda + m] if a_mn == 1
  *   B(n, k) = B[n * ldb + k] if b_mn == 0 (row-major [N, K]), B[k * ldb + n] if b_mn == 1
- * C is row-major [M, ldc] of c_dtype (PG_F32 or PG_BF16), overwritten.  With a_mn = b_mn = 0 this
- * is X W^T of a linear layer; b_mn = 1 gives dY W (input gradient); a_mn = 1, b_mn = 1 gives
- * dY^T X (weight gradient).  Requirements: device pointers, A and B 16-byte aligned, lda and ldb
+ * C is row-major [M, ldc] of c_dtype (PG_F32 or PG_BF16): overwritten when accumulate == 0,
+ * C + A B^T (added in fp32, then stored) when accumulate == 1.  With a_mn = b_mn = 0 this is X W^T
+ * of a linear layer; b_mn = 1 gives dY W (input gradient); a_mn = 1, b_mn = 1 gives dY^T X
+ * (weight gradient).  Requirements: device pointers, A and B 16-byte aligned, lda and ldb
  * multiples of 8 covering their rows, ldc >= N.
  * Errors: PG_ERR_INVALID_ARG (host check, nothing launched); PG_ERR_CUDA on a launch failure.
  */
 pg_status pg_gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, int32_t a_mn, int64_t lda,
                        const void* B, int32_t b_mn, int64_t ldb, void* C, pg_dtype c_dtype,
-                       int64_t ldc, pg_stream_t stream);
+                       int64_t ldc, int32_t accumulate, pg_stream_t stream);
+
+/*
+ * RMSNorm forward over T rows of `hidden` bf16 values (Llama style: no mean subtraction):
+ *   y = x + residual (stored to sum_out in bf16, when residual is not NULL), else y = x;
+ *   out = y / sqrt(mean(y^2) + eps) * gamma  (bf16);  rstd[t] = 1 / sqrt(mean(y_t^2) + eps) (fp32).
+ * x, residual, sum_out, out: [T, hidden] bf16; gamma: [hidden] bf16.  sum_out may alias neither
+ * x nor residual.  Errors: PG_ERR_INVALID_ARG for bad sizes or pointers.
+ */
+pg_status pg_rmsnorm_fwd(int64_t T, int32_t hidden, const void* x, const void* residual,
+                         const void* gamma, float eps, void* out, void* sum_out, float* rstd,
+                         pg_stream_t stream);
+
+/* Workspace bytes pg_rmsnorm_bwd needs for T rows of width hidden. */
+size_t pg_rmsnorm_bwd_workspace(int64_t T, int32_t hidden);
+
+/*
+ * RMSNorm backward: with yhat = y * rstd,
+ *   dx = dres + rstd * (gamma * dout - yhat * mean(yhat * gamma * dout))   (dres optional, bf16)
+ *   dgamma = sum over rows of dout * yhat   (fp32 [hidden], summed in a fixed order)
+ * y is the forward's normalised input (sum_out, or x), rstd its fp32 rows; dout and dx are
+ * [T, hidden] in the stated dtypes.  workspace: device, >= pg_rmsnorm_bwd_workspace(T, hidden).
+ */
+pg_status pg_rmsnorm_bwd(int64_t T, int32_t hidden, const void* y, const void* gamma,
+                         const float* rstd, const void* dout, pg_dtype dout_dtype,
+                         const void* dres, void* dx, pg_dtype dx_dtype, float* dgamma,
+                         void* workspace, size_t workspace_bytes, pg_stream_t stream);
+
+/*
+ * SwiGLU: gate_up is [T, 2 * inter] bf16 (gate columns first, then up); out[t, i] =
+ * silu(gate[t, i]) * up[t, i], silu(g) = g / (1 + exp(-g)), bf16 [T, inter].
+ */
+pg_status pg_swiglu_fwd(int64_t T, int32_t inter, const void* gate_up, void* out,
+                        pg_stream_t stream);
+
+/* SwiGLU backward: dgate_up [T, 2 * inter] bf16 from gate_up and dout [T, inter]. */
+pg_status pg_swiglu_bwd(int64_t T, int32_t inter, const void* gate_up, const void* dout,
+                        void* dgate_up, pg_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -48,7 +48,7 @@ class PgProfile(C.Structure):
 
 
 (PG_KERNEL_NONE, PG_KERNEL_ROPE, PG_KERNEL_ATTN_FWD, PG_KERNEL_BWD_PREPROCESS, PG_KERNEL_BWD_DKDV,
- PG_KERNEL_BWD_DQ, PG_KERNEL_ROPE_BWD, PG_KERNEL_GEMM) = range(8)
+ PG_KERNEL_BWD_DQ, PG_KERNEL_ROPE_BWD, PG_KERNEL_GEMM, PG_KERNEL_LAYER) = range(9)
 
 I32P = C.POINTER(C.c_int32)
 I64P = C.POINTER(C.c_int64)
@@ -75,7 +75,13 @@ SIGNATURES = {
                                               C.POINTER(PgOpts), VP]),
     "pg_set_profile": (C.c_int, [C.POINTER(PgProfile)]),
     "pg_gemm_bf16": (C.c_int, [C.c_int64, C.c_int64, C.c_int64, VP, C.c_int32, C.c_int64, VP,
-                               C.c_int32, C.c_int64, VP, C.c_int, C.c_int64, VP]),
+                               C.c_int32, C.c_int64, VP, C.c_int, C.c_int64, C.c_int32, VP]),
+    "pg_rmsnorm_fwd": (C.c_int, [C.c_int64, C.c_int32, VP, VP, VP, C.c_float, VP, VP, VP, VP]),
+    "pg_rmsnorm_bwd_workspace": (C.c_size_t, [C.c_int64, C.c_int32]),
+    "pg_rmsnorm_bwd": (C.c_int, [C.c_int64, C.c_int32, VP, VP, VP, VP, C.c_int, VP, VP, C.c_int,
+                                 VP, VP, C.c_size_t, VP]),
+    "pg_swiglu_fwd": (C.c_int, [C.c_int64, C.c_int32, VP, VP, VP]),
+    "pg_swiglu_bwd": (C.c_int, [C.c_int64, C.c_int32, VP, VP, VP, VP]),
     "pg_device_status": (C.c_int, [C.c_int32]),
     "pg_status_string": (C.c_char_p, [C.c_int]),
     "pg_last_error_message": (C.c_char_p, []),

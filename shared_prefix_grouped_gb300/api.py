@@ -160,7 +160,8 @@ def device_status(clear: bool = True) -> int:
 
 
 def gemm_bf16(a: torch.Tensor, b: torch.Tensor, *, a_mn: bool = False, b_mn: bool = False,
-              out_dtype: torch.dtype = torch.float32, out: Optional[torch.Tensor] = None):
+              out_dtype: torch.dtype = torch.float32, out: Optional[torch.Tensor] = None,
+              accumulate: bool = False):
     """C[m, n] = sum_k A(m, k) B(n, k) on the tensor cores (pg_gemm_bf16).
 
     a is [M, K] (a_mn False) or [K, M] (a_mn True); b is [N, K] (b_mn False) or [K, N] (True).
@@ -174,9 +175,57 @@ def gemm_bf16(a: torch.Tensor, b: torch.Tensor, *, a_mn: bool = False, b_mn: boo
         raise ValueError("inner dimensions differ")
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=a.device)
-    _contig(out)
+    if out.dim() != 2 or out.stride(1) != 1 or not out.is_cuda or out.shape != (M, N):
+        raise ValueError("out must be a [M, N] CUDA matrix with unit column stride")
     with torch.cuda.device(a.device):
         check("pg_gemm_bf16", _lib.lib().pg_gemm_bf16(
             M, N, K, _ptr(a), int(a_mn), a.shape[1], _ptr(b), int(b_mn), b.shape[1], _ptr(out),
-            _DT[out.dtype], out.shape[1], _stream_ptr(a.device)))
+            _DT[out.dtype], out.stride(0), int(accumulate), _stream_ptr(a.device)))
     return out
+
+
+def rmsnorm_fwd(x: torch.Tensor, gamma: torch.Tensor, eps: float, residual=None):
+    """out = rmsnorm(x [+ residual]) * gamma; returns (out, y, rstd) with y the normalised input."""
+    _contig(x, gamma)
+    T, H = x.shape
+    out = torch.empty_like(x)
+    y = torch.empty_like(x) if residual is not None else x
+    rstd = torch.empty(T, dtype=torch.float32, device=x.device)
+    with torch.cuda.device(x.device):
+        check("pg_rmsnorm_fwd", _lib.lib().pg_rmsnorm_fwd(
+            T, H, _ptr(x), _ptr(residual), _ptr(gamma), float(eps), _ptr(out),
+            _ptr(y if residual is not None else None), _ptr(rstd), _stream_ptr(x.device)))
+    return out, y, rstd
+
+
+def rmsnorm_bwd(y, gamma, rstd, dout, dres=None, dx_dtype=torch.bfloat16):
+    """Returns (dx, dgamma)."""
+    T, H = y.shape
+    dx = torch.empty((T, H), dtype=dx_dtype, device=y.device)
+    dgamma = torch.empty(H, dtype=torch.float32, device=y.device)
+    L = _lib.lib()
+    nws = L.pg_rmsnorm_bwd_workspace(T, H)
+    ws = _workspace(nws, y.device)
+    with torch.cuda.device(y.device):
+        check("pg_rmsnorm_bwd", L.pg_rmsnorm_bwd(
+            T, H, _ptr(y), _ptr(gamma), _ptr(rstd), _ptr(dout), _DT[dout.dtype], _ptr(dres),
+            _ptr(dx), _DT[dx_dtype], _ptr(dgamma), _ptr(ws), ws.numel(), _stream_ptr(y.device)))
+    return dx, dgamma
+
+
+def swiglu_fwd(gate_up: torch.Tensor):
+    T, I2 = gate_up.shape
+    out = torch.empty((T, I2 // 2), dtype=gate_up.dtype, device=gate_up.device)
+    with torch.cuda.device(gate_up.device):
+        check("pg_swiglu_fwd", _lib.lib().pg_swiglu_fwd(T, I2 // 2, _ptr(gate_up), _ptr(out),
+                                                         _stream_ptr(gate_up.device)))
+    return out
+
+
+def swiglu_bwd(gate_up: torch.Tensor, dout: torch.Tensor):
+    T, I2 = gate_up.shape
+    dgu = torch.empty_like(gate_up)
+    with torch.cuda.device(gate_up.device):
+        check("pg_swiglu_bwd", _lib.lib().pg_swiglu_bwd(T, I2 // 2, _ptr(gate_up), _ptr(dout),
+                                                         _ptr(dgu), _stream_ptr(gate_up.device)))
+    return dgu

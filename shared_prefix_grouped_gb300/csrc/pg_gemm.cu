@@ -36,7 +36,7 @@ struct GemmSmem {
 template <int A_MN, int B_MN, typename OutT>
 __global__ void __launch_bounds__(128, 1)
 gemm_bf16_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
-                 OutT* __restrict__ C, int M, int N, int K, long long ldc) {
+                 OutT* __restrict__ C, int M, int N, int K, long long ldc, int accumulate) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   GemmSmem& sm = *reinterpret_cast<GemmSmem*>(base);
@@ -129,7 +129,8 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__
         OutT* dst = C + (long long)row * ldc + col0;
         for (int j = 0; j < 32; ++j) {
           if (col0 + j < N) {
-            const float x = __uint_as_float(r[j]);
+            float x = __uint_as_float(r[j]);
+            if (accumulate) x += (float)dst[j];
             if constexpr (sizeof(OutT) == 4) dst[j] = x;
             else dst[j] = __float2bfloat16_rn(x);
           }
@@ -148,7 +149,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__
 
 template <int A_MN, int B_MN, typename OutT>
 pg_status launch(const CUtensorMap& ta, const CUtensorMap& tb, void* C, int M, int N, int K,
-                 long long ldc, cudaStream_t s) {
+                 long long ldc, int acc, cudaStream_t s) {
   auto kern = gemm_bf16_kernel<A_MN, B_MN, OutT>;
   const size_t smem = sizeof(GemmSmem) + 1024;
   pg_status st = cuda_check(
@@ -157,7 +158,7 @@ pg_status launch(const CUtensorMap& ta, const CUtensorMap& tb, void* C, int M, i
   if (st != PG_OK) return st;
   dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
   prof_begin(PG_KERNEL_GEMM, s);
-  kern<<<grid, 128, smem, s>>>(ta, tb, static_cast<OutT*>(C), M, N, K, ldc);
+  kern<<<grid, 128, smem, s>>>(ta, tb, static_cast<OutT*>(C), M, N, K, ldc, acc);
   prof_end(PG_KERNEL_GEMM, s);
   return cuda_check(cudaGetLastError(), "gemm launch");
 }
@@ -183,10 +184,11 @@ using namespace pg;
 
 extern "C" pg_status pg_gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, int32_t a_mn,
                                   int64_t lda, const void* B, int32_t b_mn, int64_t ldb, void* C,
-                                  pg_dtype c_dtype, int64_t ldc, pg_stream_t stream) {
+                                  pg_dtype c_dtype, int64_t ldc, int32_t accumulate,
+                                  pg_stream_t stream) {
   if (M < 1 || N < 1 || K < 1 || M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 31) ||
       !A || !B || !C || (a_mn != 0 && a_mn != 1) || (b_mn != 0 && b_mn != 1) ||
-      (c_dtype != PG_F32 && c_dtype != PG_BF16)) {
+      (c_dtype != PG_F32 && c_dtype != PG_BF16) || (accumulate != 0 && accumulate != 1)) {
     set_error("pg_gemm_bf16: bad sizes, NULL pointer or bad layout flag");
     return PG_ERR_INVALID_ARG;
   }
@@ -204,13 +206,13 @@ extern "C" pg_status pg_gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int m = (int)M, n = (int)N, k = (int)K;
   if (c_dtype == PG_F32) {
-    if (!a_mn && !b_mn) return launch<0, 0, float>(ta, tb, C, m, n, k, ldc, s);
-    if (!a_mn && b_mn) return launch<0, 1, float>(ta, tb, C, m, n, k, ldc, s);
-    if (a_mn && !b_mn) return launch<1, 0, float>(ta, tb, C, m, n, k, ldc, s);
-    return launch<1, 1, float>(ta, tb, C, m, n, k, ldc, s);
+    if (!a_mn && !b_mn) return launch<0, 0, float>(ta, tb, C, m, n, k, ldc, accumulate, s);
+    if (!a_mn && b_mn) return launch<0, 1, float>(ta, tb, C, m, n, k, ldc, accumulate, s);
+    if (a_mn && !b_mn) return launch<1, 0, float>(ta, tb, C, m, n, k, ldc, accumulate, s);
+    return launch<1, 1, float>(ta, tb, C, m, n, k, ldc, accumulate, s);
   }
-  if (!a_mn && !b_mn) return launch<0, 0, __nv_bfloat16>(ta, tb, C, m, n, k, ldc, s);
-  if (!a_mn && b_mn) return launch<0, 1, __nv_bfloat16>(ta, tb, C, m, n, k, ldc, s);
-  if (a_mn && !b_mn) return launch<1, 0, __nv_bfloat16>(ta, tb, C, m, n, k, ldc, s);
-  return launch<1, 1, __nv_bfloat16>(ta, tb, C, m, n, k, ldc, s);
+  if (!a_mn && !b_mn) return launch<0, 0, __nv_bfloat16>(ta, tb, C, m, n, k, ldc, accumulate, s);
+  if (!a_mn && b_mn) return launch<0, 1, __nv_bfloat16>(ta, tb, C, m, n, k, ldc, accumulate, s);
+  if (a_mn && !b_mn) return launch<1, 0, __nv_bfloat16>(ta, tb, C, m, n, k, ldc, accumulate, s);
+  return launch<1, 1, __nv_bfloat16>(ta, tb, C, m, n, k, ldc, accumulate, s);
 }

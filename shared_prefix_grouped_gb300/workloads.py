@@ -149,3 +149,62 @@ def small_variant(w: Workload, *, prefix_len: int, suffix_lens: List[int], num_g
         suffix_lens=tuple(suffix_lens), suffix_range=None,
         heads_q=heads_q or w.heads_q, heads_kv=heads_kv or w.heads_kv,
         seed=w.seed if seed is None else seed)
+
+
+@dataclasses.dataclass
+class LayerProblem:
+    """Host tensors of one decoder-layer problem (packed token order)."""
+
+    workload: LayerWorkload
+    prefix_lens: List[int]
+    group_sizes: List[int]
+    suffix_lens: List[int]
+    x: torch.Tensor        # [T, hidden] bf16
+    dy: torch.Tensor       # [T, hidden] bf16
+    w_qkv: torch.Tensor    # [(Hq + 2 Hkv) d, hidden] bf16 (q rows, then k rows, then v rows)
+    w_o: torch.Tensor      # [hidden, Hq d]
+    w_gu: torch.Tensor     # [2 mlp, hidden] (gate rows, then up rows)
+    w_d: torch.Tensor      # [hidden, mlp]
+    g1: torch.Tensor       # [hidden] RMSNorm gains (ones)
+    g2: torch.Tensor
+
+    @property
+    def total_tokens(self) -> int:
+        return sum(self.prefix_lens) + sum(self.suffix_lens)
+
+
+def make_layer_problem(w: LayerWorkload, *, prefix_lens=None, group_sizes=None, suffix_lens=None,
+                       seed: Optional[int] = None) -> LayerProblem:
+    """Weights N(0, weight_std) in bf16, RMSNorm gains one, inputs x and upstream dy N(0, 1)."""
+    gen = torch.Generator().manual_seed(w.seed if seed is None else seed)
+    if group_sizes is None:
+        group_sizes = [w.group_size] * w.num_groups
+    if prefix_lens is None:
+        prefix_lens = [w.prefix_len] * len(group_sizes)
+    if suffix_lens is None:
+        suffix_lens = [w.suffix_len] * sum(group_sizes)
+    T = sum(prefix_lens) + sum(suffix_lens)
+    bf = torch.bfloat16
+
+    def rnd(shape, std=1.0):
+        x = torch.randn(shape, generator=gen, dtype=torch.float32)
+        return (x * std if std != 1.0 else x).to(bf)
+
+    qkv = (w.heads_q + 2 * w.heads_kv) * w.head_dim
+    w_qkv = rnd((qkv, w.hidden), w.weight_std)
+    w_o = rnd((w.hidden, w.heads_q * w.head_dim), w.weight_std)
+    w_gu = rnd((2 * w.mlp, w.hidden), w.weight_std)
+    w_d = rnd((w.hidden, w.mlp), w.weight_std)
+    x = rnd((T, w.hidden))
+    dy = rnd((T, w.hidden))
+    ones = torch.ones(w.hidden, dtype=bf)
+    return LayerProblem(w, list(prefix_lens), list(group_sizes), list(suffix_lens), x, dy, w_qkv,
+                        w_o, w_gu, w_d, ones, ones.clone())
+
+
+def small_layer(**kw) -> LayerWorkload:
+    """A decoder layer small enough for the CPU oracle (head_dim stays 128)."""
+    base = dict(hidden=256, heads_q=2, heads_kv=1, head_dim=128, mlp=384, num_groups=2,
+                group_size=3, prefix_len=150, suffix_len=70, rope_theta=5e5, seed=1104)
+    base.update(kw)
+    return LayerWorkload(name="llama_layer_small", **base)
