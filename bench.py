@@ -443,6 +443,59 @@ def repeated_leg(prob, device, flags, grouped_sec, args):
                 flops.total_pairs(prob.prefix_lens, prob.group_sizes, prob.suffix_lens) / rep_pairs}
 
 
+def run_layer_bench(args):
+    """The decoder-layer workload: forward + backward of one layer over the packed groups."""
+    from shared_prefix_grouped_gb300 import layer
+    world, rank, local = dist_setup()
+    device = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(device)
+    w = workloads.LayerWorkload()
+    prob = workloads.make_layer_problem(w, seed=w.seed + rank)
+    lay = api.pack(prob.prefix_lens, prob.group_sizes, prob.suffix_lens, device)
+    W = [t.to(device) for t in (prob.w_qkv, prob.w_o, prob.w_gu, prob.w_d, prob.g1, prob.g2)]
+    x, dy = prob.x.to(device), prob.dy.to(device)
+    kw = dict(heads_q=w.heads_q, heads_kv=w.heads_kv, head_dim=w.head_dim,
+              rope_theta=w.rope_theta, eps=w.rms_eps)
+
+    def step():
+        y, saved = layer.layer_fwd(lay, x, *W, **kw)
+        layer.layer_bwd(lay, x, *W, saved, dy, **kw)
+
+    for _ in range(args.warmup):
+        step()
+    L = _lib.lib()
+    prof = _lib.PgProfile(0, 0, None, None, 0)
+    sampler = ClockSampler(device.index)
+    sampler.start()
+    barrier(world, device)
+    L.pg_set_profile(prof)
+    sec = time_steps(step, args.steps, device)
+    L.pg_set_profile(None)
+    barrier(world, device)
+    clocks = sampler.stop()
+    sec = max_over_ranks(sec, world, device)
+    T, H, I = prob.total_tokens, w.hidden, w.mlp
+    qkv = (w.heads_q + 2 * w.heads_kv) * w.head_dim
+    gemm = 2.0 * T * H * (qkv + w.heads_q * w.head_dim + 3 * I) * 3    # forward + 2x backward
+    attn = flops.attn_flops(lay.pairs, w.heads_q, w.head_dim, "fwdbwd")
+    peaks, peak_src = load_peaks()
+    value = (gemm + attn) * world / sec / 1e12
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) inputs, N(0,0.02) weights; no checkpoint)",
+            "config": {"workload": w.name, "groups": w.num_groups,
+                       "responses_per_group": w.group_size, "prefix_len": w.prefix_len,
+                       "suffix_len": w.suffix_len, "total_tokens": T, "hidden": H, "mlp": I,
+                       "heads_q": w.heads_q, "heads_kv": w.heads_kv, "head_dim": w.head_dim,
+                       "rope_theta": w.rope_theta, "l2": "activations far larger than L2"},
+            "tokens_per_s": T * world / sec, "pct_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
+            "peak_source": peak_src, "counted_tflop": {"gemm": gemm / 1e12, "attention": attn / 1e12},
+            "clocks": clocks, "gpu_launches": int(prof.launches)}
+    if rank == 0:
+        print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -450,7 +503,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=[w.name for w in workloads.WORKLOADS])
+                    choices=[w.name for w in workloads.WORKLOADS] + [workloads.LayerWorkload().name])
     ap.add_argument("--simt", action="store_true", help="force the fp32 SIMT kernels")
     ap.add_argument("--skip-extras", action="store_true",
                     help="skip the e2e, repeated-prefix and CPU legs (profiling runs)")
@@ -459,6 +512,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == workloads.LayerWorkload().name:
+        run_layer_bench(args)
     else:
         run_ours(args)
 
