@@ -9,18 +9,20 @@
 // prefix K/V tiles, which stay resident in L2 across the group's query tiles and heads.
 //
 // Warp roles (320 threads):
-//   warp 0      TMA producer: Q tiles once, then 64-key K and V tiles into a 3-stage ring
+//   warp 0      TMA producer: Q tiles once, then 64-key K and V tiles into a 4-stage ring
 //   warp 1      TMEM allocation and the MMA issuer (one elected thread), per key tile j and
 //               query tile i:
 //                 S_i = Q_i K_j^T   (M 128 x N 64 keys x K 128; fp32 TMEM columns [64 i, 64 i + 64))
-//                 O_i += P_i V_j    (M 128 x N 128 dims x K 64; fp32 TMEM columns [128 + 128 i, ...))
+//                 O_i += P_i V_j    (M 128 x N 128 dims x K 64; fp32 TMEM columns [128 + 128 i, ...)),
+//                                   with P_i read from TMEM (bf16, columns [384 + 64 i + 32 b, ...)
+//                                   for buffer b) and V from shared memory
 //               issued in the order S_0(0) S_1(0), then per key tile S_0(j+1) S_1(j+1) PV_0(j)
 //               PV_1(j): the next scores are computed while both softmax warpgroups work
 //   warps 2..5  softmax of query tile 0, warps 6..9 of query tile 1: one thread per query row
 //               (TMEM lane = row); S from TMEM to registers, masking, online max / sum in fp32
-//               (exp2 with the scale folded in), P rounded to bf16 into shared memory (the A
-//               operand of P V), O rescaled in TMEM only when the running max grows by more than
-//               2^8, and the final O / l, LSE epilogue.
+//               (exp2 with the scale folded in), P rounded to bf16 and stored into TMEM (the A
+//               operand of P V, double-buffered), O rescaled in TMEM only when the running max
+//               grows by more than 2^8, and the final O / l, LSE epilogue.
 // A key tile that lies entirely after the last row of query tile 0 is skipped for that tile.
 //
 // Every mbarrier wait is bounded (PG_ERR_TIMEOUT in the status word, then an orderly exit: copies
@@ -40,10 +42,9 @@ namespace {
 constexpr int D = 128;          // head_dim
 constexpr int BM = 128;         // query rows per query tile (two per CTA)
 constexpr int BN = 64;          // keys per tile
-constexpr int NS = 3;           // K/V pipeline stages
+constexpr int NS = 4;           // K/V pipeline stages
 constexpr uint32_t QHALF = BM * 64 * 2;    // [128 rows][64 dims] bf16: 16 KiB
 constexpr uint32_t KHALF = BN * 64 * 2;    // [64 keys][64 dims] bf16: 8 KiB
-constexpr uint32_t PTILE = BM * BN * 2;    // [128 rows][64 keys] bf16: 16 KiB
 constexpr int NTHREADS = 320;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -55,7 +56,6 @@ struct FwdSmem {
   uint8_t q[2][2 * QHALF];
   uint8_t k[NS][2 * KHALF];
   uint8_t v[NS][2 * KHALF];
-  uint8_t p[2][2][PTILE];   // [query tile][buffer]
   uint64_t q_full;
   uint64_t k_full[NS], v_full[NS], kv_empty[NS];
   uint64_t s_full[2], s_free[2];
@@ -233,11 +233,11 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
           const int b = n_pv[i] & 1;
           if (!mbar_wait(&sm.p_full[i][b], (n_pv[i] >> 1) & 1, wait_ns)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t pa = smem_u32(sm.p[i][b]), va = smem_u32(sm.v[j % NS]);
+          const uint32_t pt = tmem + 384 + 64 * i + 32 * b, va = smem_u32(sm.v[j % NS]);
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
-            mma_ss(tmem + 128 + 128 * i, sdesc_sw128(pa + kk * 32, 16, 1024),
-                   sdesc_sw128(va + kk * 2048, KHALF, 1024), idesc_pv, (n_pv[i] | kk) != 0);
+            mma_ts(tmem + 128 + 128 * i, pt + kk * 8, sdesc_sw128(va + kk * 2048, KHALF, 1024),
+                   idesc_pv, (n_pv[i] | kk) != 0);
           }
           mma_commit(&sm.pv_done[i][b]);
           ++n_pv[i];
@@ -317,7 +317,8 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
         l += p0 + p1;
         pw[e] = pack_bf16x2(p0, p1);
       }
-      // P is double-buffered: the product that read this buffer two key tiles ago must be done.
+      // P is double-buffered in TMEM: the product that read this buffer two key tiles ago must
+      // be done.
       // Rescaling O needs the previous key tile's product done too.
       const int b = c & 1;
       const bool any_rescale = __any_sync(0xffffffffu, rescale) && c > 0;
@@ -331,6 +332,7 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
         ok = false;
         break;
       }
+      tc_fence_after();
       if (any_rescale) {
         tc_fence_after();
         {
@@ -346,15 +348,10 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
           tmem_st_wait();
         }
       }
-      uint8_t* prow = sm.p[i][b];
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        *reinterpret_cast<uint4*>(prow + sw128_offset(r, ch)) =
-            make_uint4(pw[4 * ch], pw[4 * ch + 1], pw[4 * ch + 2], pw[4 * ch + 3]);
-      }
+      tmem_st32(tmem + 384 + 64 * i + 32 * b + lane_addr, pw);
+      tmem_st_wait();
       ++c;
       if (debug & PG_DEBUG_WITHHOLD_P) continue;   // test hook: never signal P (bounded waits)
-      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&sm.p_full[i][b]);
     }
