@@ -199,8 +199,17 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       constexpr uint32_t id_s = idesc_bf16(BKV, BQ, 0, 0);     // S^T, dP^T
       constexpr uint32_t id_g = idesc_bf16(BKV, D, 0, 1);      // dV, dK
       constexpr uint32_t id_q = idesc_bf16(D, BQ, 1, 1);       // dQ^T
-      const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v);
-      const uint32_t pa = smem_u32(sm.p), dsa = smem_u32(sm.ds);
+      // Descriptor bases (K-major use: LBO unused; MN-major use: LBO = the 64-column half).
+      const uint64_t kd = sdesc_sw128(smem_u32(sm.k), 16, 1024);
+      const uint64_t vd = sdesc_sw128(smem_u32(sm.v), 16, 1024);
+      const uint64_t kmn = sdesc_sw128(smem_u32(sm.k), KHALF, 1024);
+      const uint64_t pd = sdesc_sw128(smem_u32(sm.p), 16, 1024);
+      const uint64_t dsd = sdesc_sw128(smem_u32(sm.ds), 16, 1024);
+      const uint64_t dsmn = sdesc_sw128(smem_u32(sm.ds), QHALF, 1024);
+      const uint64_t qd0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
+      const uint64_t dod0 = sdesc_sw128(smem_u32(sm.dO[0]), 16, 1024);
+      const uint64_t qmn0 = sdesc_sw128(smem_u32(sm.q[0]), QHALF, 1024);
+      const uint64_t domn0 = sdesc_sw128(smem_u32(sm.dO[0]), QHALF, 1024);
       bool ok = mbar_wait(&sm.kv_full, 0, wait_ns);
       for (int it = 0; ok && it <= n_it; ++it) {
         if (it < n_it) {
@@ -208,20 +217,18 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
           if (!mbar_wait(&sm.qd_full[st], (it / NSQ) & 1, wait_ns)) { ok = false; break; }
           if (it > 0 && !mbar_wait(&sm.s_free, (it - 1) & 1, wait_ns)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t qa = smem_u32(sm.q[st]), doa = smem_u32(sm.dO[st]);
+          const uint64_t qd = desc_add(qd0, st * 2 * QHALF), dod = desc_add(dod0, st * 2 * QHALF);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t ko = (kk >> 2) * KHALF + (kk & 3) * 32;
             const uint32_t qo = (kk >> 2) * QHALF + (kk & 3) * 32;
-            mma_ss(t_s, sdesc_sw128(ka + ko, 16, 1024), sdesc_sw128(qa + qo, 16, 1024), id_s,
-                   kk != 0);
+            mma_ss(t_s, desc_add(kd, ko), desc_add(qd, qo), id_s, kk != 0);
           }
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t ko = (kk >> 2) * KHALF + (kk & 3) * 32;
             const uint32_t qo = (kk >> 2) * QHALF + (kk & 3) * 32;
-            mma_ss(t_dp, sdesc_sw128(va + ko, 16, 1024), sdesc_sw128(doa + qo, 16, 1024), id_s,
-                   kk != 0);
+            mma_ss(t_dp, desc_add(vd, ko), desc_add(dod, qo), id_s, kk != 0);
           }
           mma_commit(&sm.s_full);
         }
@@ -229,17 +236,17 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
           const int jp = it - 1, sp = jp % NSQ;
           if (!mbar_wait(&sm.p_full, jp & 1, wait_ns)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t qa = smem_u32(sm.q[sp]), doa = smem_u32(sm.dO[sp]);
+          const uint64_t qmn = desc_add(qmn0, sp * 2 * QHALF);
+          const uint64_t domn = desc_add(domn0, sp * 2 * QHALF);
+          const uint32_t acc0 = jp != 0;
 #pragma unroll
-          for (int kk = 0; kk < BQ / 16; ++kk) {
-            mma_ss(t_dv, sdesc_sw128(pa + kk * 32, 16, 1024),
-                   sdesc_sw128(doa + kk * 2048, QHALF, 1024), id_g, (jp | kk) != 0);
-          }
+          for (int kk = 0; kk < BQ / 16; ++kk)
+            mma_ss(t_dv, desc_add(pd, kk * 32), desc_add(domn, kk * 2048), id_g,
+                   kk == 0 ? acc0 : 1u);
 #pragma unroll
-          for (int kk = 0; kk < BQ / 16; ++kk) {
-            mma_ss(t_dk, sdesc_sw128(dsa + kk * 32, 16, 1024),
-                   sdesc_sw128(qa + kk * 2048, QHALF, 1024), id_g, (jp | kk) != 0);
-          }
+          for (int kk = 0; kk < BQ / 16; ++kk)
+            mma_ss(t_dk, desc_add(dsd, kk * 32), desc_add(qmn, kk * 2048), id_g,
+                   kk == 0 ? acc0 : 1u);
           mma_commit(&sm.qd_empty[sp]);
           const int b = jp & 1;
           if (jp >= 2 && !mbar_wait(&sm.dq_free[b], ((jp >> 1) & 1) ^ 1, wait_ns)) {
@@ -248,10 +255,9 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
           }
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < BKV / 16; ++kk) {
-            mma_ss(t_dq + 64 * b, sdesc_sw128(ka + kk * 2048, KHALF, 1024),
-                   sdesc_sw128(dsa + kk * 2048, QHALF, 1024), id_q, kk != 0);
-          }
+          for (int kk = 0; kk < BKV / 16; ++kk)
+            mma_ss(t_dq + 64 * b, desc_add(kmn, kk * 2048), desc_add(dsmn, kk * 2048), id_q,
+                   kk != 0);
           mma_commit(&sm.dq_full[b]);
           mma_commit(&sm.pds_free);
         }

@@ -201,19 +201,22 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       int n_s[2] = {0, 0};        // S products issued per query tile
       int n_pv[2] = {0, 0};       // P V products issued per query tile
       bool ok = mbar_wait(&sm.q_full, 0, wait_ns);
+      // Descriptor bases: buffers of a kind are contiguous, so buffer n is base + n * stride.
+      const uint64_t qd0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
+      const uint64_t kd0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
+      const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0]), KHALF, 1024);
       // S_i(j): scores of query tile i against key tile j.  Needs the K tile and the softmax of
       // tile i to have read its previous scores out of TMEM (S_i is single-buffered).
       auto issue_s = [&](int i, int j) -> bool {
         if (!mbar_wait(&sm.k_full[j % NS], (j / NS) & 1, wait_ns)) return false;
         if (n_s[i] > 0 && !mbar_wait(&sm.s_free[i], (n_s[i] - 1) & 1, wait_ns)) return false;
         tc_fence_after();
-        const uint32_t qa = smem_u32(sm.q[i]), ka = smem_u32(sm.k[j % NS]);
+        const uint64_t qd = desc_add(qd0, i * 2 * QHALF), kd = desc_add(kd0, (j % NS) * 2 * KHALF);
+        const uint32_t ts = tmem + 64 * i;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t qo = (kk >> 2) * QHALF + (kk & 3) * 32;
-          const uint32_t ko = (kk >> 2) * KHALF + (kk & 3) * 32;
-          mma_ss(tmem + 64 * i, sdesc_sw128(qa + qo, 16, 1024), sdesc_sw128(ka + ko, 16, 1024),
-                 idesc_s, kk != 0);
+          mma_ss(ts, desc_add(qd, (kk >> 2) * QHALF + (kk & 3) * 32),
+                 desc_add(kd, (kk >> 2) * KHALF + (kk & 3) * 32), idesc_s, kk != 0);
         }
         mma_commit(&sm.s_full[i]);
         ++n_s[i];
@@ -233,12 +236,12 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
           const int b = n_pv[i] & 1;
           if (!mbar_wait(&sm.p_full[i][b], (n_pv[i] >> 1) & 1, wait_ns)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t pt = tmem + 384 + 64 * i + 32 * b, va = smem_u32(sm.v[j % NS]);
+          const uint32_t pt = tmem + 384 + 64 * i + 32 * b, to = tmem + 128 + 128 * i;
+          const uint64_t vd = desc_add(vd0, (j % NS) * 2 * KHALF);
+          const uint32_t acc0 = n_pv[i] != 0;
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            mma_ts(tmem + 128 + 128 * i, pt + kk * 8, sdesc_sw128(va + kk * 2048, KHALF, 1024),
-                   idesc_pv, (n_pv[i] | kk) != 0);
-          }
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(to, pt + kk * 8, desc_add(vd, kk * 2048), idesc_pv, kk == 0 ? acc0 : 1u);
           mma_commit(&sm.pv_done[i][b]);
           ++n_pv[i];
         }

@@ -256,6 +256,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo
   return d;
 }
 
+// A descriptor whose start address is `bytes` further (the start address field is the low 14
+// bits in 16-byte units and shared memory is below 256 KiB, so the add never carries out of it).
+// Descriptors are built once per buffer and advanced with compile-time offsets, which keeps the
+// single MMA-issuing thread from spending tens of cycles per MMA on descriptor arithmetic.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) {
+  return d + (uint64_t)(bytes >> 4);
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 D, M x N tile.
 // a_mn / b_mn: operand is MN-major (1) or K-major (0).
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
