@@ -8,16 +8,15 @@
 // tiles share each K/V tile loaded into shared memory, and all CTAs of a group read the same
 // prefix K/V tiles, which stay resident in L2 across the group's query tiles and heads.
 //
-// Warp roles (320 threads):
+// Warp roles (352 threads):
 //   warp 0      TMA producer: Q tiles once, then 64-key K and V tiles into a 4-stage ring
-//   warp 1      TMEM allocation and the MMA issuer (one elected thread), per key tile j and
+//   warp 1      TMEM allocation and the score MMAs, warp 10 the P V MMAs (one elected thread
+//               each, so both kinds are queued on the tensor core at once), per key tile j and
 //               query tile i:
 //                 S_i = Q_i K_j^T   (M 128 x N 64 keys x K 128; fp32 TMEM columns [64 i, 64 i + 64))
 //                 O_i += P_i V_j    (M 128 x N 128 dims x K 64; fp32 TMEM columns [128 + 128 i, ...)),
 //                                   with P_i read from TMEM (bf16, columns [384 + 64 i + 32 b, ...)
 //                                   for buffer b) and V from shared memory
-//               issued in the order S_0(0) S_1(0), then per key tile S_0(j+1) S_1(j+1) PV_0(j)
-//               PV_1(j): the next scores are computed while both softmax warpgroups work
 //   warps 2..5  softmax of query tile 0, warps 6..9 of query tile 1: one thread per query row
 //               (TMEM lane = row); S from TMEM to registers, masking, online max / sum in fp32
 //               (exp2 with the scale folded in), P rounded to bf16 and stored into TMEM (the A
@@ -45,7 +44,7 @@ constexpr int BN = 64;          // keys per tile
 constexpr int NS = 4;           // K/V pipeline stages
 constexpr uint32_t QHALF = BM * 64 * 2;    // [128 rows][64 dims] bf16: 16 KiB
 constexpr uint32_t KHALF = BN * 64 * 2;    // [64 keys][64 dims] bf16: 8 KiB
-constexpr int NTHREADS = 320;
+constexpr int NTHREADS = 352;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -61,7 +60,7 @@ struct FwdSmem {
   uint64_t s_full[2], s_free[2];
   uint64_t p_full[2][2];    // P of [query tile][buffer] written
   uint64_t pv_done[2][2];   // the P V product reading [query tile][buffer] has completed
-  uint64_t mma_done;
+  uint64_t mma_done, mma_done2;
   uint32_t tmem;
 };
 
@@ -145,6 +144,7 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       }
     }
     mbar_init(&sm.mma_done, 1);
+    mbar_init(&sm.mma_done2, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -194,42 +194,54 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer -------
+    // ------------------------------------------------------------------ score MMAs -------
     if (elect_one()) {
       constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
-      constexpr uint32_t idesc_pv = idesc_bf16(BM, D, 0, 1);
       int n_s[2] = {0, 0};        // S products issued per query tile
-      int n_pv[2] = {0, 0};       // P V products issued per query tile
       bool ok = mbar_wait(&sm.q_full, 0, wait_ns);
       // Descriptor bases: buffers of a kind are contiguous, so buffer n is base + n * stride.
       const uint64_t qd0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
       const uint64_t kd0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
-      const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0]), KHALF, 1024);
       // S_i(j): scores of query tile i against key tile j.  Needs the K tile and the softmax of
       // tile i to have read its previous scores out of TMEM (S_i is single-buffered).
-      auto issue_s = [&](int i, int j) -> bool {
-        if (!mbar_wait(&sm.k_full[j % NS], (j / NS) & 1, wait_ns)) return false;
-        if (n_s[i] > 0 && !mbar_wait(&sm.s_free[i], (n_s[i] - 1) & 1, wait_ns)) return false;
-        tc_fence_after();
-        const uint64_t qd = desc_add(qd0, i * 2 * QHALF), kd = desc_add(kd0, (j % NS) * 2 * KHALF);
-        const uint32_t ts = tmem + 64 * i;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          mma_ss(ts, desc_add(qd, (kk >> 2) * QHALF + (kk & 3) * 32),
-                 desc_add(kd, (kk >> 2) * KHALF + (kk & 3) * 32), idesc_s, kk != 0);
-        }
-        mma_commit(&sm.s_full[i]);
-        ++n_s[i];
-        return true;
-      };
-      // Order: S_0(0) S_1(0), then per key tile j: S_0(j+1) S_1(j+1) PV_0(j) PV_1(j).  The next
-      // scores are computed while the softmax warps turn the current ones into P.
-      for (int i = 0; i < nq && ok; ++i)
-        if (pl.rel(i, 0)) ok = issue_s(i, 0);
       for (int j = 0; ok && j < n; ++j) {
-        for (int i = 0; i < nq && ok; ++i)
-          if (j + 1 < n && pl.rel(i, j + 1)) ok = issue_s(i, j + 1);
-        if (!ok) break;
+        for (int i = 0; i < nq; ++i) {
+          if (!pl.rel(i, j)) continue;
+          if (!mbar_wait(&sm.k_full[j % NS], (j / NS) & 1, wait_ns)) { ok = false; break; }
+          if (n_s[i] > 0 && !mbar_wait(&sm.s_free[i], (n_s[i] - 1) & 1, wait_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t qd = desc_add(qd0, i * 2 * QHALF);
+          const uint64_t kd = desc_add(kd0, (j % NS) * 2 * KHALF);
+          const uint32_t ts = tmem + 64 * i;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            mma_ss(ts, desc_add(qd, (kk >> 2) * QHALF + (kk & 3) * 32),
+                   desc_add(kd, (kk >> 2) * KHALF + (kk & 3) * 32), idesc_s, kk != 0);
+          }
+          mma_commit(&sm.s_full[i]);
+          ++n_s[i];
+        }
+      }
+      if (!ok) fail(PG_ERR_TIMEOUT);
+      // Every MMA issued above completes before TMEM is released.
+      mma_commit(&sm.mma_done);
+      mbar_wait(&sm.mma_done, 0, wait_ns);
+    }
+    __syncwarp();
+  } else if (warp == 10) {
+    // ------------------------------------------------------------------ P V MMAs ---------
+    // A second issuing thread: the products of P with V are queued while the next scores are
+    // still being issued.  Ordering with the score MMAs goes through the barriers (a key tile's
+    // scores completed before its P was written).
+    if (elect_one()) {
+      constexpr uint32_t idesc_pv = idesc_bf16(BM, D, 0, 1);
+      int n_pv[2] = {0, 0};       // P V products issued per query tile
+      const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0]), KHALF, 1024);
+      bool ok = true;
+      for (int j = 0; ok && j < n; ++j) {
         if (!mbar_wait(&sm.v_full[j % NS], (j / NS) & 1, wait_ns)) { ok = false; break; }
         for (int i = 0; i < nq && ok; ++i) {
           if (!pl.rel(i, j)) continue;
@@ -248,9 +260,8 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
         mma_commit(&sm.kv_empty[j % NS]);
       }
       if (!ok) fail(PG_ERR_TIMEOUT);
-      // Every MMA issued above completes before TMEM is released.
-      mma_commit(&sm.mma_done);
-      mbar_wait(&sm.mma_done, 0, wait_ns);
+      mma_commit(&sm.mma_done2);
+      mbar_wait(&sm.mma_done2, 0, wait_ns);
     }
     __syncwarp();
   } else {
