@@ -15,11 +15,12 @@
 //   S^T  = K Q^T          M 128 keys x N 64 queries x K 128   (TMEM cols [0, 64))
 //   dP^T = V dO^T         M 128 x N 64 x K 128                 (TMEM cols [64, 128))
 //   P^T  = exp2(S^T * scale * log2 e - LSE_2[q]),  dS^T = P^T * (dP^T - Dsum[q])   (registers,
-//          one thread per key row, rounded to bf16 into shared memory)
-//   dV  += P^T dO         M 128 x N 128 dims x K 64           (TMEM cols [256, 384))
-//   dK  += dS^T Q         M 128 x N 128 x K 64                 (TMEM cols [384, 512))
-//   dQ^T = K^T dS^T       M 128 dims x N 64 queries x K 128    (TMEM cols [128, 256), two
-//          buffers used alternately), drained by four warps (one thread per head-dim lane): each
+//          one thread per key row, rounded to bf16 and stored into TMEM cols [192, 224) and
+//          [224, 256); dS^T also into shared memory, the B operand of dQ^T)
+//   dV  += P^T dO         M 128 x N 128 dims x K 64, A = P^T from TMEM  (TMEM cols [256, 384))
+//   dK  += dS^T Q         M 128 x N 128 x K 64, A = dS^T from TMEM      (TMEM cols [384, 512))
+//   dQ^T = K^T dS^T       M 128 dims x N 64 queries x K 128    (TMEM cols [128, 192)),
+//          drained by four warps (one thread per head-dim lane): each
 //          warp stages its 32 head dims of the block, 32 query rows at a time ([32 x 32] fp32),
 //          in its own shared-memory buffer and adds them into the global dQ accumulator with TMA
 //          bulk reduce-adds.
@@ -61,15 +62,14 @@ struct BwdSmem {
   uint8_t v[2 * KHALF];
   uint8_t q[NSQ][2 * QHALF];
   uint8_t dO[NSQ][2 * QHALF];
-  uint8_t p[KHALF];         // P^T  [128 keys][64 queries] bf16, SW128
-  uint8_t ds[KHALF];        // dS^T [128 keys][64 queries]
+  uint8_t ds[KHALF];        // dS^T [128 keys][64 queries] bf16, SW128
   alignas(1024) float dqs[4][BQ / 2][32];   // per drain warp: half its slice of a dQ block
   alignas(128) float lse2[NSQ][BQ];
   alignas(128) float dsum[NSQ][BQ];
   alignas(128) int4 tokq[NSQ][BQ];   // per-token {g0, pe, own_lo, pos} of the block's queries
   uint64_t kv_full;
   uint64_t qd_full[NSQ], qd_empty[NSQ];
-  uint64_t s_full, s_free, p_full, pds_free, dq_full[2], dq_free[2], mma_done;
+  uint64_t s_full, s_free, p_full, pds_free, dq_full, dq_free, mma_done;
   uint32_t tmem;
 };
 
@@ -123,10 +123,8 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     mbar_init(&sm.s_free, 256);
     mbar_init(&sm.p_full, 256);
     mbar_init(&sm.pds_free, 1);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&sm.dq_full[b], 1);
-      mbar_init(&sm.dq_free[b], 128);
-    }
+    mbar_init(&sm.dq_full, 1);
+    mbar_init(&sm.dq_free, 128);
     mbar_init(&sm.mma_done, 1);
     fence_mbar_init();
   }
@@ -138,8 +136,8 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem;
-  const uint32_t t_s = tmem, t_dp = tmem + 64, t_dq = tmem + 128, t_dv = tmem + 256,
-                 t_dk = tmem + 384;   // dQ^T buffer b at t_dq + 64 b
+  const uint32_t t_s = tmem, t_dp = tmem + 64, t_dq = tmem + 128, t_p = tmem + 192,
+                 t_ds = tmem + 224, t_dv = tmem + 256, t_dk = tmem + 384;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer ---------
@@ -203,8 +201,6 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       const uint64_t kd = sdesc_sw128(smem_u32(sm.k), 16, 1024);
       const uint64_t vd = sdesc_sw128(smem_u32(sm.v), 16, 1024);
       const uint64_t kmn = sdesc_sw128(smem_u32(sm.k), KHALF, 1024);
-      const uint64_t pd = sdesc_sw128(smem_u32(sm.p), 16, 1024);
-      const uint64_t dsd = sdesc_sw128(smem_u32(sm.ds), 16, 1024);
       const uint64_t dsmn = sdesc_sw128(smem_u32(sm.ds), QHALF, 1024);
       const uint64_t qd0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
       const uint64_t dod0 = sdesc_sw128(smem_u32(sm.dO[0]), 16, 1024);
@@ -241,24 +237,17 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
           const uint32_t acc0 = jp != 0;
 #pragma unroll
           for (int kk = 0; kk < BQ / 16; ++kk)
-            mma_ss(t_dv, desc_add(pd, kk * 32), desc_add(domn, kk * 2048), id_g,
-                   kk == 0 ? acc0 : 1u);
+            mma_ts(t_dv, t_p + kk * 8, desc_add(domn, kk * 2048), id_g, kk == 0 ? acc0 : 1u);
 #pragma unroll
           for (int kk = 0; kk < BQ / 16; ++kk)
-            mma_ss(t_dk, desc_add(dsd, kk * 32), desc_add(qmn, kk * 2048), id_g,
-                   kk == 0 ? acc0 : 1u);
+            mma_ts(t_dk, t_ds + kk * 8, desc_add(qmn, kk * 2048), id_g, kk == 0 ? acc0 : 1u);
           mma_commit(&sm.qd_empty[sp]);
-          const int b = jp & 1;
-          if (jp >= 2 && !mbar_wait(&sm.dq_free[b], ((jp >> 1) & 1) ^ 1, wait_ns)) {
-            ok = false;
-            break;
-          }
+          if (jp >= 1 && !mbar_wait(&sm.dq_free, (jp - 1) & 1, wait_ns)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < BKV / 16; ++kk)
-            mma_ss(t_dq + 64 * b, desc_add(kmn, kk * 2048), desc_add(dsmn, kk * 2048), id_q,
-                   kk != 0);
-          mma_commit(&sm.dq_full[b]);
+            mma_ss(t_dq, desc_add(kmn, kk * 2048), desc_add(dsmn, kk * 2048), id_q, kk != 0);
+          mma_commit(&sm.dq_full);
           mma_commit(&sm.pds_free);
         }
       }
@@ -333,14 +322,16 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       }
       // The previous block's gradient products must be done with P^T / dS^T.
       if (it > 0 && !warp_wait(&sm.pds_free, (it - 1) & 1, wait_ns)) { ok = false; break; }
+      tc_fence_after();
+      tmem_st16(t_p + half * 16 + lane_addr, pw);
+      tmem_st16(t_ds + half * 16 + lane_addr, dw);
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         const uint32_t off = sw128_offset(r, half * 4 + ch);
-        *reinterpret_cast<uint4*>(sm.p + off) =
-            make_uint4(pw[4 * ch], pw[4 * ch + 1], pw[4 * ch + 2], pw[4 * ch + 3]);
         *reinterpret_cast<uint4*>(sm.ds + off) =
             make_uint4(dw[4 * ch], dw[4 * ch + 1], dw[4 * ch + 2], dw[4 * ch + 3]);
       }
+      tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&sm.p_full);
@@ -421,15 +412,14 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     for (int it = 0; it < n_it; ++it) {
       const int h = kh * rep + it / nqt;
       const int qt = qt0 + (it % nqt) * BQ;
-      const int b = it & 1;
-      if (!warp_wait(&sm.dq_full[b], (it >> 1) & 1, wait_ns)) { ok = false; break; }
+      if (!warp_wait(&sm.dq_full, it & 1, wait_ns)) { ok = false; break; }
       tc_fence_after();
       uint32_t g[64];
-      tmem_ld32(t_dq + 64 * b + lane_addr, *reinterpret_cast<uint32_t(*)[32]>(&g[0]));
-      tmem_ld32(t_dq + 64 * b + lane_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&g[32]));
+      tmem_ld32(t_dq + lane_addr, *reinterpret_cast<uint32_t(*)[32]>(&g[0]));
+      tmem_ld32(t_dq + lane_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&g[32]));
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&sm.dq_free[b]);
+      mbar_arrive(&sm.dq_free);
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         // This warp's previous reduce must have finished reading its staging buffer.
