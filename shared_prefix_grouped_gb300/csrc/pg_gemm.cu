@@ -5,9 +5,10 @@
 //   A(m, k) = A[m * lda + k] (K-major)  or  A[k * lda + m] (MN-major, "transposed")
 //   B(n, k) = B[n * ldb + k] (K-major)  or  B[k * ldb + n] (MN-major)
 //
-// One CTA computes a 128 x 128 tile of C; 4 warps: warp 0 issues TMA loads into a 4-stage ring,
-// warp 1 issues the MMAs (K = 16 each, 4 per 64-wide K block), then all four warps drain TMEM
-// (warp w owns accumulator lanes / C rows 32w .. 32w + 31).
+// One CTA computes a 128 x 256 tile of C; 4 warps: warp 0 issues TMA loads into a 4-stage ring,
+// warp 1 issues the MMAs (128 x 256 x 16 each, 4 per 64-wide K block, descriptors built once and
+// advanced by constant offsets), then all four warps drain TMEM (warp w owns accumulator lanes /
+// C rows 32w .. 32w + 31) with 16-byte stores where the tile is in bounds and aligned.
 #include "pg_internal.h"
 #include "pg_sm100.cuh"
 #include "pg_tmap.h"
@@ -18,15 +19,17 @@ using namespace sm100;
 
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 64, STAGES = 4;
-constexpr uint32_t TILE_BYTES = BM * BK * 2;   // 16 KiB per operand per stage
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int GROUP_M = 16;
+constexpr uint32_t A_BYTES = BM * BK * 2;      // 16 KiB per stage
+constexpr uint32_t B_BYTES = BN * BK * 2;      // 32 KiB per stage
 constexpr uint64_t WAIT_NS = 2000000000ull;    // 2 s bound on every wait
 
 __device__ int s_status_gemm = 0;
 
 struct GemmSmem {
-  uint8_t a[STAGES][TILE_BYTES];
-  uint8_t b[STAGES][TILE_BYTES];
+  uint8_t a[STAGES][A_BYTES];
+  uint8_t b[STAGES][B_BYTES];
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
   uint64_t done;
@@ -36,12 +39,22 @@ struct GemmSmem {
 template <int A_MN, int B_MN, typename OutT>
 __global__ void __launch_bounds__(128, 1)
 gemm_bf16_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
-                 OutT* __restrict__ C, int M, int N, int K, long long ldc, int accumulate) {
+                 OutT* __restrict__ C, int M, int N, int K, long long ldc, int accumulate,
+                 int vec_ok) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   GemmSmem& sm = *reinterpret_cast<GemmSmem*>(base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  // Grouped rasterisation: consecutive CTAs walk down GROUP_M row blocks before moving to the
+  // next column block, so a wave of CTAs touches a compact block of A rows and B columns that
+  // stays in L2.
+  const int num_m = (M + BM - 1) / BM, num_n = (N + BN - 1) / BN;
+  const int tile = blockIdx.x;
+  const int group = tile / (GROUP_M * num_n);
+  const int first_m = group * GROUP_M;
+  const int gm = min(num_m - first_m, GROUP_M);
+  const int in_group = tile - group * GROUP_M * num_n;
+  const int m0 = (first_m + in_group % gm) * BM, n0 = (in_group / gm) * BN;
   const int nk = (K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
@@ -71,18 +84,19 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__
         const int s = kb % STAGES;
         const uint32_t ph = (kb / STAGES) & 1;
         if (!mbar_wait(&sm.empty[s], ph ^ 1, WAIT_NS)) { ok = false; break; }
-        mbar_expect_tx(&sm.full[s], 2 * TILE_BYTES);
+        mbar_expect_tx(&sm.full[s], A_BYTES + B_BYTES);
         if (!A_MN) {
           tma_load_2d(sm.a[s], &ta, &sm.full[s], kb * BK, m0);
         } else {
           tma_load_2d(sm.a[s], &ta, &sm.full[s], m0, kb * BK);
-          tma_load_2d(sm.a[s] + TILE_BYTES / 2, &ta, &sm.full[s], m0 + 64, kb * BK);
+          tma_load_2d(sm.a[s] + A_BYTES / 2, &ta, &sm.full[s], m0 + 64, kb * BK);
         }
         if (!B_MN) {
           tma_load_2d(sm.b[s], &tb, &sm.full[s], kb * BK, n0);
         } else {
-          tma_load_2d(sm.b[s], &tb, &sm.full[s], n0, kb * BK);
-          tma_load_2d(sm.b[s] + TILE_BYTES / 2, &tb, &sm.full[s], n0 + 64, kb * BK);
+#pragma unroll
+          for (int q4 = 0; q4 < BN / 64; ++q4)
+            tma_load_2d(sm.b[s] + q4 * (BK * 64 * 2), &tb, &sm.full[s], n0 + 64 * q4, kb * BK);
         }
         ++issued;
       }
@@ -94,19 +108,21 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__
   } else if (warp == 1) {
     if (elect_one()) {
       constexpr uint32_t idesc = idesc_bf16(BM, BN, A_MN, B_MN);
+      // MN-major: the next 64-wide M/N block is LBO further (the next TMA box).
+      const uint64_t ad0 = A_MN ? sdesc_sw128(smem_u32(sm.a[0]), A_BYTES / 2, 1024)
+                                : sdesc_sw128(smem_u32(sm.a[0]), 16, 1024);
+      const uint64_t bd0 = B_MN ? sdesc_sw128(smem_u32(sm.b[0]), BK * 64 * 2, 1024)
+                                : sdesc_sw128(smem_u32(sm.b[0]), 16, 1024);
       for (int kb = 0; kb < nk; ++kb) {
         const int s = kb % STAGES;
         if (!mbar_wait(&sm.full[s], (kb / STAGES) & 1, WAIT_NS)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t a0 = smem_u32(sm.a[s]), b0 = smem_u32(sm.b[s]);
+        const uint64_t ad = desc_add(ad0, s * A_BYTES), bd = desc_add(bd0, s * B_BYTES);
+        const uint32_t acc0 = kb != 0;
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint64_t ad = A_MN ? sdesc_sw128(a0 + kk * 2048, TILE_BYTES / 2, 1024)
-                                   : sdesc_sw128(a0 + kk * 32, 16, 1024);
-          const uint64_t bd = B_MN ? sdesc_sw128(b0 + kk * 2048, TILE_BYTES / 2, 1024)
-                                   : sdesc_sw128(b0 + kk * 32, 16, 1024);
-          mma_ss(tmem, ad, bd, idesc, (kb | kk) != 0);
-        }
+        for (int kk = 0; kk < BK / 16; ++kk)
+          mma_ss(tmem, desc_add(ad, A_MN ? kk * 2048 : kk * 32),
+                 desc_add(bd, B_MN ? kk * 2048 : kk * 32), idesc, kk == 0 ? acc0 : 1u);
         mma_commit(&sm.empty[s]);
       }
       mma_commit(&sm.done);
@@ -119,20 +135,56 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__
   tc_fence_after();
   const int row = m0 + warp * 32 + lane;
   if (ok) {
+    // 16-byte stores need the row start aligned: ldc * sizeof(OutT) a multiple of 16 and an
+    // aligned C (checked on the host: vec_ok).
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       uint32_t r[32];
       tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c * 32, r);
       tmem_ld_wait();
       const int col0 = n0 + c * 32;
-      if (row < M) {
+      if (row < M && col0 < N) {
         OutT* dst = C + (long long)row * ldc + col0;
-        for (int j = 0; j < 32; ++j) {
-          if (col0 + j < N) {
-            float x = __uint_as_float(r[j]);
-            if (accumulate) x += (float)dst[j];
-            if constexpr (sizeof(OutT) == 4) dst[j] = x;
-            else dst[j] = __float2bfloat16_rn(x);
+        if (vec_ok && col0 + 32 <= N) {
+          if constexpr (sizeof(OutT) == 4) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              float4 v = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                                     __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+              if (accumulate) {
+                const float4 o = *reinterpret_cast<const float4*>(dst + j);
+                v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+              }
+              *reinterpret_cast<float4*>(dst + j) = v;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+              float f[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(r[j + e]);
+              if (accumulate) {
+                const uint4 o = *reinterpret_cast<const uint4*>(dst + j);
+                const __nv_bfloat16* ob = reinterpret_cast<const __nv_bfloat16*>(&o);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] += __bfloat162float(ob[e]);
+              }
+              uint4 w;
+              w.x = pack_bf16x2(f[0], f[1]);
+              w.y = pack_bf16x2(f[2], f[3]);
+              w.z = pack_bf16x2(f[4], f[5]);
+              w.w = pack_bf16x2(f[6], f[7]);
+              *reinterpret_cast<uint4*>(dst + j) = w;
+            }
+          }
+        } else {
+          for (int j = 0; j < 32; ++j) {
+            if (col0 + j < N) {
+              float x = __uint_as_float(r[j]);
+              if (accumulate) x += (float)dst[j];
+              if constexpr (sizeof(OutT) == 4) dst[j] = x;
+              else dst[j] = __float2bfloat16_rn(x);
+            }
           }
         }
       }
@@ -156,9 +208,11 @@ pg_status launch(const CUtensorMap& ta, const CUtensorMap& tb, void* C, int M, i
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
       "gemm smem attribute");
   if (st != PG_OK) return st;
-  dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
+  dim3 grid((unsigned)(((N + BN - 1) / BN) * ((M + BM - 1) / BM)));
   prof_begin(PG_KERNEL_GEMM, s);
-  kern<<<grid, 128, smem, s>>>(ta, tb, static_cast<OutT*>(C), M, N, K, ldc, acc);
+  const int vec_ok = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0) &&
+                     ((ldc * (long long)sizeof(OutT)) % 16 == 0);
+  kern<<<grid, 128, smem, s>>>(ta, tb, static_cast<OutT*>(C), M, N, K, ldc, acc, vec_ok);
   prof_end(PG_KERNEL_GEMM, s);
   return cuda_check(cudaGetLastError(), "gemm launch");
 }
@@ -201,7 +255,7 @@ extern "C" pg_status pg_gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A
                       : make_tmap_2d_bf16(&ta, A, K, M, lda * 2, 64, 128);
   if (st != PG_OK) return st;
   st = b_mn ? make_tmap_2d_bf16(&tb, B, N, K, ldb * 2, 64, 64)
-            : make_tmap_2d_bf16(&tb, B, K, N, ldb * 2, 64, 128);
+            : make_tmap_2d_bf16(&tb, B, K, N, ldb * 2, 64, BN);
   if (st != PG_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int m = (int)M, n = (int)N, k = (int)K;
