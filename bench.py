@@ -40,7 +40,7 @@ L2_BYTES = 129 * 2 ** 20
 # source still has the hash it had when the counters were taken, and only for that workload.
 TRAFFIC = {"file": "shared_prefix_grouped_gb300/csrc/pg_attn_bwd_sm100.cu",
            "sha256": "75186b0ea5aeae2567c5377e8fceb01de2abb29e46ebc42cb41700f938e58d5d",
-           "workload": "bf16_mha_h32_d128_p4096_g8_r512", "bytes": 2653527824}
+           "workload": "bf16_mha_h32_d128_p4096_g8_r512", "bytes": 2653527944}
 
 
 def measured_traffic(workload: str):
