@@ -443,6 +443,105 @@ def repeated_leg(prob, device, flags, grouped_sec, args):
                 flops.total_pairs(prob.prefix_lens, prob.group_sizes, prob.suffix_lens) / rep_pairs}
 
 
+SCORE_METRIC = ("grouped-attn responses-only forward (scoring) TFLOP/s & HBM GB/s "
+                "vs the K/V-read roofline (1 GB300)")
+
+
+def score_counts(prob):
+    """Visible pairs of the response rows and the algorithmic bytes of one responses-only call:
+    every K/V row a response can see read once per key/value head, the response rows of q read,
+    o and lse written."""
+    w = prob.workload
+    pairs, kv_rows, s = 0, 0, 0
+    for lp, G in zip(prob.prefix_lens, prob.group_sizes):
+        rs = prob.suffix_lens[s:s + G]
+        s += G
+        pairs += sum(r * lp + r * (r + 1) // 2 for r in rs)
+        kv_rows += (lp + sum(rs)) if sum(rs) else 0
+    rows = sum(prob.suffix_lens)
+    nbytes = (2 * kv_rows * w.heads_kv * w.head_dim * 2 + 2 * rows * w.heads_q * w.head_dim * 2
+              + rows * w.heads_q * 4)
+    return pairs, nbytes
+
+
+def run_score_bench(args):
+    """The forward-only scoring workload: response rows only, L2 flushed before every call and
+    outside its events."""
+    world, rank, local = dist_setup()
+    device = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(device)
+    w = workloads.by_name(args.workload)
+    prob = workloads.make_problem(w, seed=w.seed + rank)
+    flags = _lib.PG_FLAG_RESPONSES_ONLY | (_lib.PG_FLAG_SIMT if args.simt else 0)
+    lay = api.pack(prob.prefix_lens, prob.group_sizes, prob.suffix_lens, device)
+    q, k, v = (t.to(device) for t in (prob.q, prob.k, prob.v))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.heads_q, prob.total_tokens), dtype=torch.float32, device=device)
+    opts = api.make_opts(w.rope_theta, 0.0, flags)
+    ws = api._workspace(api.workspace_size(lay, q.dtype, w.heads_q, w.heads_kv, w.head_dim, opts,
+                                           0), device)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+
+    def call():
+        api.grouped_attn_fwd(lay, q, k, v, rope_theta=w.rope_theta, flags=flags, out=o, lse=lse,
+                             workspace=ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize(device)
+    L = _lib.lib()
+    n = args.steps
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    step_ev = [(mk(), mk()) for _ in range(n)]
+    kern_ev = [(mk(), mk()) for _ in range(n)]
+    for a, b in kern_ev:      # create the CUDA events before their handles are passed on
+        a.record()
+        b.record()
+    prof = _lib.PgProfile(_lib.PG_KERNEL_ATTN_FWD, 0, None, None, 0)
+    sampler = ClockSampler(device.index)
+    sampler.start()
+    barrier(world, device)
+    L.pg_set_profile(prof)
+    for i in range(n):
+        flush.zero_()
+        prof.ev_begin = kern_ev[i][0].cuda_event
+        prof.ev_end = kern_ev[i][1].cuda_event
+        step_ev[i][0].record()
+        call()
+        step_ev[i][1].record()
+    L.pg_set_profile(None)
+    barrier(world, device)
+    clocks = sampler.stop()
+    assert api.device_status() == 0, "a kernel reported an error"
+    sec = sum(a.elapsed_time(b) for a, b in step_ev) / 1e3 / n
+    sec = max_over_ranks(sec, world, device)
+    ksec = sum(a.elapsed_time(b) for a, b in kern_ev) / 1e3 / n
+    pairs, nbytes = score_counts(prob)
+    fl = flops.attn_flops(pairs, w.heads_q, w.head_dim, "fwd")
+    peaks, peak_src = load_peaks()
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    value = fl * world / sec / 1e12
+    line = {"metric": SCORE_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": n, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic (seeded N(0,1) Q/K/V; no dataset)",
+            "config": dict(workload_config(w, prob, "L2 flushed before every call (outside the "
+                                                     "events)"), responses_only=True,
+                           response_tokens=sum(prob.suffix_lens)),
+            "tokens_per_s": sum(prob.suffix_lens) * world / sec,
+            "hbm_gbs_per_call": nbytes / sec / 1e9,
+            "roofline": {"bound": "hbm", "kernel": "responses-only forward (key-split, GQA-packed)",
+                         "achieved": nbytes / ksec / 1e9, "peak": hbm, "unit": "GB/s",
+                         "frac": nbytes / ksec / 1e9 / hbm, "traffic": None,
+                         "algorithmic_bytes": nbytes, "kernel_ms": ksec * 1e3,
+                         "kernel_tflops": fl / ksec / 1e12,
+                         "peak_source": f"HBM copy bandwidth, {peak_src}"},
+            "clocks": clocks, "gpu_launches": int(prof.launches)}
+    if rank == 0:
+        print(json.dumps(line))
+
+
 def run_layer_bench(args):
     """The decoder-layer workload: forward + backward of one layer over the packed groups."""
     from shared_prefix_grouped_gb300 import layer
@@ -514,6 +613,8 @@ def main():
         run_reference(args)
     elif args.workload == workloads.LayerWorkload().name:
         run_layer_bench(args)
+    elif workloads.by_name(args.workload).responses_only:
+        run_score_bench(args)
     else:
         run_ours(args)
 

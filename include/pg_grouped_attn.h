@@ -64,6 +64,20 @@ typedef struct pg_opts {
 /* Run the fp32-arithmetic SIMT kernels even for bf16 inputs (a slower, independent path). */
 #define PG_FLAG_SIMT 1u
 
+/*
+ * Forward only: compute o and lse for the response rows alone, for scoring many short responses
+ * against one long shared context (Pith review, "Core claim": judging many short questions against
+ * one long context reuses the same sharing pattern).  Every response row still attends to its whole
+ * prefix and causally to its own response, so k and v must hold the prefix rows too (for example a
+ * cached context); the prefix rows of o and lse are not written and their q rows are not read.
+ * Rejected by pg_grouped_attn_bwd (PG_ERR_INVALID_ARG).  The bf16, head_dim 128 kernel packs the
+ * Hq / Hkv query heads that share a key/value head into one tile and splits the prefix keys across
+ * CTAs, so each prefix K/V row is read from memory about once per key/value head; the partial
+ * results are merged by their log-sum-exp in a second kernel (workspace: pg_workspace_size with
+ * this flag).
+ */
+#define PG_FLAG_RESPONSES_ONLY 2u
+
 /* Test hook for the bounded-wait error path: the tensor-core forward never signals that P is
  * ready, so its MMA thread's wait runs out (after 50 ms instead of 2 s), the kernel records
  * PG_ERR_TIMEOUT in the status word and exits cleanly; the outputs are then undefined. */
@@ -81,12 +95,13 @@ typedef struct pg_layout {
   int64_t max_position;    /* 1 + the largest position id */
   int64_t pairs;           /* visible (query, key) pairs per head, summed over groups */
   int64_t n_tiles[6];      /* work-list lengths: fwd 64-row, fwd 128-row, bwd 64-key, bwd 128-key,
-                              fwd 256-row, (unused) */
+                              fwd 256-row, response spans (one per group with response rows) */
   int64_t off_tiles[6];    /* byte offsets of those lists in the tables */
   int64_t off_tokens;      /* byte offset of the per-token table (16 bytes per token) */
   int64_t table_bytes;     /* bytes of the tables buffer in use */
   const int32_t* position_ids; /* [T] */
   const void* tables;
+  int64_t max_response_rows; /* the largest number of response rows (sum of R_bi) in one group */
 } pg_layout;
 
 /*
@@ -171,7 +186,8 @@ typedef enum pg_kernel {
   PG_KERNEL_BWD_DQ = 5,          /* query-major dQ */
   PG_KERNEL_ROPE_BWD = 6,        /* inverse RoPE of dQ/dK and the cast to the output dtype */
   PG_KERNEL_GEMM = 7,            /* the bf16 tensor-core GEMM (decoder-layer path) */
-  PG_KERNEL_LAYER = 8            /* RMSNorm / SwiGLU kernels of the decoder-layer path */
+  PG_KERNEL_LAYER = 8,           /* RMSNorm / SwiGLU kernels of the decoder-layer path */
+  PG_KERNEL_SCORE_COMBINE = 9    /* merge of the responses-only forward's key splits */
 } pg_kernel;
 
 /*

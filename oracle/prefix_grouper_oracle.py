@@ -364,6 +364,49 @@ def repeated_prefix(layout: PackedLayout, q, k, v, do=None, *, theta: float = 0.
     return AttnResult(O, LSE)
 
 
+def response_rows(layout: PackedLayout, q, k, v, rows: Sequence[int], *, theta: float = 0.0,
+                  scale: Optional[float] = None, q_heads: Optional[Sequence[int]] = None):
+    """Forward O and LSE of selected response rows, straight from the baseline's definition.
+
+    Packed row t = token j of response i of group b is row Lp + j of the baseline sequence
+    [P_b; R_bi].  Causal attention makes that row depend only on the baseline rows 0 .. Lp + j, so
+    it is computed from them alone: positions 0 .. Lp + j, RoPE, scores against those Lp + j + 1
+    keys, softmax, weighted sum of the values.  This is the quantity scored when many short
+    responses are judged against one long context (Pith review, "Core claim"), and it keeps the
+    cost per row at O(Lp d) so rows of very long prefixes can be sampled.
+    Returns (O [len(rows), len(q_heads), d], LSE [len(q_heads), len(rows)]) in float64.
+    """
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    scale = d ** -0.5 if scale is None else scale
+    q_heads = list(range(Hq)) if q_heads is None else list(q_heads)
+    O = torch.empty((len(rows), len(q_heads), d), dtype=F64)
+    LSE = torch.empty((len(q_heads), len(rows)), dtype=F64)
+    prefix_k = {}     # group -> its prefix keys rotated at positions 0 .. Lp-1 (same in every copy)
+    for n, t in enumerate(rows):
+        i = int(layout.token_segment[t])
+        assert i >= 0, "response_rows takes response rows only"
+        b = int(layout.token_group[t])
+        lp = layout.prefix_lens[b]
+        j = t - int(layout.segment_start[i])
+        seq = baseline_rows(layout, b, i)[: lp + j + 1]
+        pos = torch.arange(seq.numel())
+        if b not in prefix_k:
+            prefix_k[b] = rope_rotate(k[seq[:lp]].to(F64), pos[:lp], theta)
+        kr = torch.cat([prefix_k[b], rope_rotate(k[seq[lp:]].to(F64), pos[lp:], theta)])
+        vr = v[seq].to(F64)
+        qr = rope_rotate(q[t:t + 1].to(F64), pos[-1:], theta)[0]
+        for hn, h in enumerate(q_heads):
+            kh = _kv_head(h, Hq, Hkv)
+            s_ = (kr[:, kh] @ qr[h]) * scale
+            m = s_.max()
+            e = torch.exp(s_ - m)
+            den = e.sum()
+            O[n, hn] = (e / den) @ vr[:, kh]
+            LSE[hn, n] = m + torch.log(den)
+    return O, LSE
+
+
 # ------------------------------------------------------------------------------------------------
 # Second formulation: one attention over the packed sequence with a dense mask
 # ------------------------------------------------------------------------------------------------

@@ -10,6 +10,7 @@ LIB_PATH = os.path.join(HERE, "libpg_gb300.so")
 PG_OK, PG_ERR_INVALID_ARG, PG_ERR_UNSUPPORTED, PG_ERR_CUDA, PG_ERR_TIMEOUT, PG_ERR_DEVICE = range(6)
 PG_F32, PG_BF16 = 0, 1
 PG_FLAG_SIMT = 1
+PG_FLAG_RESPONSES_ONLY = 2
 
 
 class PgLayout(C.Structure):
@@ -25,6 +26,7 @@ class PgLayout(C.Structure):
         ("table_bytes", C.c_int64),
         ("position_ids", C.c_void_p),
         ("tables", C.c_void_p),
+        ("max_response_rows", C.c_int64),
     ]
 
 
@@ -48,7 +50,8 @@ class PgProfile(C.Structure):
 
 
 (PG_KERNEL_NONE, PG_KERNEL_ROPE, PG_KERNEL_ATTN_FWD, PG_KERNEL_BWD_PREPROCESS, PG_KERNEL_BWD_DKDV,
- PG_KERNEL_BWD_DQ, PG_KERNEL_ROPE_BWD, PG_KERNEL_GEMM, PG_KERNEL_LAYER) = range(9)
+ PG_KERNEL_BWD_DQ, PG_KERNEL_ROPE_BWD, PG_KERNEL_GEMM, PG_KERNEL_LAYER,
+ PG_KERNEL_SCORE_COMBINE) = range(10)
 
 I32P = C.POINTER(C.c_int32)
 I64P = C.POINTER(C.c_int64)

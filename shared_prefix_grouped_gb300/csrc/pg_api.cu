@@ -35,6 +35,7 @@ pg_status read_kernel_status(bool clear, int32_t* code) {
   if (st == PG_OK) st = read_status_gemm(clear, code);
   if (st == PG_OK) st = read_status_fwd_sm100(clear, code);
   if (st == PG_OK) st = read_status_bwd_sm100(clear, code);
+  if (st == PG_OK) st = read_status_score_sm100(clear, code);
   return st;
 }
 
@@ -48,6 +49,7 @@ struct Plan {
   int64_t n[NUM_LISTS] = {0, 0, 0, 0, 0, 0};
   int64_t off[NUM_LISTS] = {0, 0, 0, 0, 0, 0};
   int64_t off_tokens = 0, bytes = 0;
+  int64_t max_resp = 0;   // largest number of response rows in one group
 };
 
 static pg_status check_lengths(int32_t B, const int32_t* lp, const int32_t* gs, const int32_t* rs,
@@ -92,18 +94,22 @@ static pg_status check_lengths(int32_t B, const int32_t* lp, const int32_t* gs, 
   p->max_pos = maxpos;
   p->pairs = pairs;
   // Work-list lengths: one tile per started block of rows in each group.
-  int64_t n64 = 0, n128 = 0, n256 = 0;
+  int64_t n64 = 0, n128 = 0, n256 = 0, nspan = 0;
   int64_t s = 0;
   for (int32_t b = 0; b < B; ++b) {
-    int64_t len = lp[b];
-    for (int32_t i = 0; i < gs[b]; ++i) len += rs[s++];
+    int64_t resp = 0;
+    for (int32_t i = 0; i < gs[b]; ++i) resp += rs[s++];
+    const int64_t len = lp[b] + resp;
     n64 += (len + 63) / 64;
     n128 += (len + 127) / 128;
     n256 += (len + 255) / 256;
+    nspan += resp > 0;
+    p->max_resp = std::max(p->max_resp, resp);
   }
   p->n[FWD64] = p->n[BWD64] = n64;
   p->n[FWD128] = p->n[BWD128] = n128;
   p->n[FWD256] = n256;
+  p->n[SPANS] = nspan;
   int64_t off = 0;
   p->off_tokens = off;
   off = align_up(off + 16 * T, 256);
@@ -198,6 +204,29 @@ static void build_tables(int32_t B, const int32_t* lp, const int32_t* gs, const 
       memcpy(tables + p.off[bw], bt.data(), bt.size() * sizeof(BwdTile));
     }
   }
+  // Response spans, in group order.
+  std::vector<FwdTile> spans;
+  int32_t g0 = 0;
+  int64_t sb = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    const int32_t pe = g0 + lp[b];
+    int32_t gend = pe;
+    for (int32_t i = 0; i < gs[b]; ++i) gend += rs[sb + i];
+    sb += gs[b];
+    if (gend > pe) {
+      FwdTile t{};
+      t.q0 = pe;
+      t.q1 = gend;
+      t.g0 = g0;
+      t.p_end = pe;
+      t.s_lo = pe;
+      t.s_hi = gend;
+      t.pe = pe;
+      spans.push_back(t);
+    }
+    g0 = gend;
+  }
+  memcpy(tables + p.off[SPANS], spans.data(), spans.size() * sizeof(FwdTile));
 }
 
 static void fill_layout(int32_t B, const Plan& p, const int32_t* pos, const void* tables,
@@ -216,6 +245,7 @@ static void fill_layout(int32_t B, const Plan& p, const int32_t* pos, const void
   L->table_bytes = p.bytes;
   L->position_ids = pos;
   L->tables = tables;
+  L->max_response_rows = p.max_resp;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -223,13 +253,14 @@ static void fill_layout(int32_t B, const Plan& p, const int32_t* pos, const void
 // ---------------------------------------------------------------------------------------------
 
 struct WsPlan {
-  size_t q_rot = 0, k_rot = 0, rope_tab = 0, Dbuf = 0, lse2 = 0, dq_acc = 0, dk_acc = 0, total = 0;
+  size_t q_rot = 0, k_rot = 0, rope_tab = 0, Dbuf = 0, lse2 = 0, dq_acc = 0, dk_acc = 0;
+  size_t part_o = 0, part_lse = 0, total = 0;
 };
 
 static size_t esize(pg_dtype dt) { return dt == PG_F32 ? 4 : 2; }
 
 static WsPlan ws_plan(const pg_layout* L, pg_dtype dt, int Hq, int Hkv, int d, bool rope,
-                      int phase) {
+                      int phase, const AttnArgs& a) {
   WsPlan w;
   size_t T = (size_t)L->total_tokens;
   size_t off = 0;
@@ -240,10 +271,19 @@ static WsPlan ws_plan(const pg_layout* L, pg_dtype dt, int Hq, int Hkv, int d, b
   };
   // Offset 0 is a valid slot; record "absent" as SIZE_MAX.
   w.q_rot = w.k_rot = w.rope_tab = w.Dbuf = w.lse2 = w.dq_acc = w.dk_acc = SIZE_MAX;
+  w.part_o = w.part_lse = SIZE_MAX;
   if (rope) {
     w.q_rot = take(T * Hq * d * esize(dt));
     w.k_rot = take(T * Hkv * d * esize(dt));
     if (phase == 1) w.rope_tab = take(T * (d / 2) * sizeof(float2));
+  }
+  if (phase == 0 && (a.flags & PG_FLAG_RESPONSES_ONLY) && !(a.flags & PG_FLAG_SIMT) &&
+      score_sm100_supported(a)) {
+    const ScorePlan sp = score_plan(L, Hq, Hkv);
+    if (sp.nsplit > 1) {
+      w.part_o = take(sp.part_o_bytes);
+      w.part_lse = take(sp.part_lse_bytes);
+    }
   }
   if (phase == 1) {
     const size_t Tp = (size_t)padded_tokens(L);
@@ -386,7 +426,8 @@ pg_status pg_workspace_size(const pg_layout* layout, pg_dtype dtype, int32_t hea
                             "pg_workspace_size");
   if (st != PG_OK) return st;
   bool rope = opts && opts->rope_theta > 0.f;
-  *bytes = ws_plan(layout, dtype, heads_q, heads_kv, head_dim, rope, phase).total;
+  const AttnArgs a = make_args(layout, dtype, heads_q, heads_kv, head_dim, opts, nullptr);
+  *bytes = ws_plan(layout, dtype, heads_q, heads_kv, head_dim, rope, phase, a).total;
   return PG_OK;
 }
 
@@ -401,7 +442,7 @@ pg_status pg_grouped_attn_fwd(const pg_layout* layout, pg_dtype dtype, int32_t h
   AttnArgs a = make_args(layout, dtype, heads_q, heads_kv, head_dim, opts,
                          reinterpret_cast<cudaStream_t>(stream));
   bool rope = a.theta > 0.f;
-  WsPlan w = ws_plan(layout, dtype, heads_q, heads_kv, head_dim, rope, 0);
+  WsPlan w = ws_plan(layout, dtype, heads_q, heads_kv, head_dim, rope, 0, a);
   if (w.total > 0 && (!workspace || workspace_bytes < w.total || !aligned16(workspace))) {
     set_error("%s: workspace must be 16-byte aligned and >= %zu bytes", who, w.total);
     return PG_ERR_INVALID_ARG;
@@ -409,12 +450,22 @@ pg_status pg_grouped_attn_fwd(const pg_layout* layout, pg_dtype dtype, int32_t h
   char* ws = static_cast<char*>(workspace);
   const void* qx = q;
   const void* kx = k;
+  const bool responses_only = (a.flags & PG_FLAG_RESPONSES_ONLY) != 0;
   if (rope) {
+    // Responses only: the prefix rows of q are never read, so they are not rotated either.
     st = launch_rope(a, q, ws + w.q_rot, heads_q, k, ws + w.k_rot, heads_kv, false, false,
-                     nullptr, nullptr);
+                     nullptr, nullptr, responses_only);
     if (st != PG_OK) return st;
     qx = ws + w.q_rot;
     kx = ws + w.k_rot;
+  }
+  if (responses_only) {
+    if (!(a.flags & PG_FLAG_SIMT) && score_sm100_supported(a))
+      return launch_score_sm100(
+          a, qx, kx, v, o, lse,
+          w.part_o == SIZE_MAX ? nullptr : reinterpret_cast<float*>(ws + w.part_o),
+          w.part_lse == SIZE_MAX ? nullptr : reinterpret_cast<float*>(ws + w.part_lse));
+    return launch_fwd_simt(a, qx, kx, v, o, lse);
   }
   if (!(a.flags & PG_FLAG_SIMT) && fwd_sm100_supported(a))
     return launch_fwd_sm100(a, qx, kx, v, o, lse);
@@ -432,8 +483,12 @@ pg_status pg_grouped_attn_bwd(const pg_layout* layout, pg_dtype dtype, int32_t h
   if (st != PG_OK) return st;
   AttnArgs a = make_args(layout, dtype, heads_q, heads_kv, head_dim, opts,
                          reinterpret_cast<cudaStream_t>(stream));
+  if (a.flags & PG_FLAG_RESPONSES_ONLY) {
+    set_error("%s: PG_FLAG_RESPONSES_ONLY is a forward-only option", who);
+    return PG_ERR_INVALID_ARG;
+  }
   bool rope = a.theta > 0.f;
-  WsPlan w = ws_plan(layout, dtype, heads_q, heads_kv, head_dim, rope, 1);
+  WsPlan w = ws_plan(layout, dtype, heads_q, heads_kv, head_dim, rope, 1, a);
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) {
     set_error("%s: workspace must be 16-byte aligned and >= %zu bytes", who, w.total);
     return PG_ERR_INVALID_ARG;

@@ -305,19 +305,23 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
         const int4* tq4 = sm.tokq[st] + c0;
         const float* l2 = sm.lse2[st] + c0;
         const float* ds_ = sm.dsum[st] + c0;
+        // Branch-free visibility (bitwise, not short-circuit, so the unrolled loop stays
+        // straight-line): query t sees this key iff key <= t < q_hi and the key is a prefix key or
+        // lies in t's own response.  An invisible entry's exponent is -inf, so P = 0 and dS = 0.
+        const bool prefix_key = keyc < tl.pe;
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           const int t0 = qt + c0 + c, t1 = t0 + 1;
-          const bool v0 = kvalid && t0 < tl.q_hi && keyc <= t0 && keyc >= tl.g0 &&
-                          (keyc < tl.pe || keyc >= tq4[c].z);
-          const bool v1 = kvalid && t1 < tl.q_hi && keyc <= t1 && keyc >= tl.g0 &&
-                          (keyc < tl.pe || keyc >= tq4[c + 1].z);
-          const float p0 = v0 ? fast_exp2(fmaf(__uint_as_float(sr[c]), scale_log2, -l2[c])) : 0.f;
-          const float p1 =
-              v1 ? fast_exp2(fmaf(__uint_as_float(sr[c + 1]), scale_log2, -l2[c + 1])) : 0.f;
+          const bool v0 = kvalid & (t0 < tl.q_hi) & (keyc <= t0) & (prefix_key | (keyc >= tq4[c].z));
+          const bool v1 =
+              kvalid & (t1 < tl.q_hi) & (keyc <= t1) & (prefix_key | (keyc >= tq4[c + 1].z));
+          const float a0 = fmaf(__uint_as_float(sr[c]), scale_log2, -l2[c]);
+          const float a1 = fmaf(__uint_as_float(sr[c + 1]), scale_log2, -l2[c + 1]);
+          const float p0 = fast_exp2(v0 ? a0 : -INFINITY);
+          const float p1 = fast_exp2(v1 ? a1 : -INFINITY);
           pw[c >> 1] = pack_bf16x2(p0, p1);
-          dw[c >> 1] = pack_bf16x2(v0 ? p0 * (__uint_as_float(dr[c]) - ds_[c]) : 0.f,
-                                   v1 ? p1 * (__uint_as_float(dr[c + 1]) - ds_[c + 1]) : 0.f);
+          dw[c >> 1] = pack_bf16x2(p0 * (__uint_as_float(dr[c]) - ds_[c]),
+                                   p1 * (__uint_as_float(dr[c + 1]) - ds_[c + 1]));
         }
       }
       // The previous block's gradient products must be done with P^T / dS^T.

@@ -304,10 +304,15 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
           mx = fmaxf(mx, x);
         }
       } else {
+        // Within one key tile a row's visible keys are one contiguous run of columns: in the
+        // prefix range [kt, min(hi, row + 1)); in the responses' range the same run starting no
+        // earlier than the row's own response (prefix rows get an empty run there).  One unsigned
+        // compare per column, no branches.
+        const int lo = (j < pl.n_a) ? 0 : max(ti.z - kt, 0);
+        const int len = max(min(hi, rowc + 1) - kt - lo, 0);
 #pragma unroll
         for (int cc = 0; cc < BN; ++cc) {
-          const int s = kt + cc;
-          const bool vis = s < hi && s <= rowc && s >= ti.x && (s < ti.y || s >= ti.z);
+          const bool vis = (unsigned)(cc - lo) < (unsigned)len;
           const float x = vis ? __uint_as_float(sr[cc]) * scale_log2 : -INFINITY;
           sr[cc] = __float_as_uint(x);
           mx = fmaxf(mx, x);

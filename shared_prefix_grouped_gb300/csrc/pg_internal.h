@@ -33,7 +33,9 @@ struct BwdTile {
 static_assert(sizeof(FwdTile) == 32, "FwdTile layout");
 static_assert(sizeof(BwdTile) == 32, "BwdTile layout");
 
-enum TileList { FWD64 = 0, FWD128 = 1, BWD64 = 2, BWD128 = 3, FWD256 = 4, NUM_LISTS = 6 };
+// SPANS: one FwdTile per group with response rows: q0 = pe, q1 = the group's end, g0, p_end = pe,
+// s_lo = pe, s_hi = q1, pe.
+enum TileList { FWD64 = 0, FWD128 = 1, BWD64 = 2, BWD128 = 3, FWD256 = 4, SPANS = 5, NUM_LISTS = 6 };
 
 // Row stride (elements) of the per-head fp32 rows the backward keeps for LSE and rowsum(dO * O):
 // T rounded up to a multiple of 4, so every row starts 16-byte aligned (a TMA requirement).
@@ -89,6 +91,21 @@ pg_status launch_bwd_sm100(const AttnArgs& a, const void* q, const void* k, cons
                            void* dk, void* dv, const float2* rope_tab);
 pg_status cuda_check(cudaError_t e, const char* what);
 
+// Responses-only forward (pg_attn_score_sm100.cu): its launch shape and partial-result buffers.
+struct ScorePlan {
+  int hp;              // query heads per key/value head, packed into one CTA's rows
+  int TB;              // tokens per row block (256 / hp)
+  int nrb;             // row blocks per response span (the largest span decides)
+  int nsplit;          // prefix-key splits per row block
+  int64_t nblk;        // CTAs per split: spans x nrb x Hkv
+  size_t part_o_bytes, part_lse_bytes;   // fp32 partials (0 when nsplit == 1)
+};
+bool score_sm100_supported(const AttnArgs& a);
+ScorePlan score_plan(const pg_layout* L, int Hq, int Hkv);
+pg_status launch_score_sm100(const AttnArgs& a, const void* q, const void* k, const void* v,
+                             void* o, float* lse, float* part_o, float* part_lse);
+pg_status read_status_score_sm100(bool clear, int32_t* code);
+
 // RoPE inverse frequencies theta^(-2k/d), k < d/2, computed on the host in fp64.
 struct RopeFreq {
   double inv[64];
@@ -96,9 +113,10 @@ struct RopeFreq {
 };
 
 // SIMT kernels (pg_simt.cu).
+// skip_prefix0: leave the prefix tokens of (x0, y0) alone (responses-only forward).
 pg_status launch_rope(const AttnArgs& a, const void* x0, void* y0, int heads0, const void* x1,
                       void* y1, int heads1, bool inverse, bool in_fp32, float2* table_out,
-                      const float2* table_in);
+                      const float2* table_in, bool skip_prefix0 = false);
 pg_status launch_fwd_simt(const AttnArgs& a, const void* q, const void* k, const void* v, void* o,
                           float* lse);
 pg_status launch_bwd_simt(const AttnArgs& a, const void* q, const void* k, const void* v,

@@ -119,9 +119,12 @@ template <typename Tin, typename Tout>
 __global__ void rope_kernel(const Tin* __restrict__ x0, Tout* __restrict__ y0, int h0,
                             const Tin* __restrict__ x1, Tout* __restrict__ y1, int h1, int d,
                             const int32_t* __restrict__ pos_ids, RopeFreq f, int rope, float sgn,
-                            float2* __restrict__ table_out, const float2* __restrict__ table_in) {
+                            float2* __restrict__ table_out, const float2* __restrict__ table_in,
+                            const int4* __restrict__ skip_prefix0) {
   __shared__ float cs[64], sn[64];
   const int t = blockIdx.x;
+  // With skip_prefix0 (the per-token table), prefix tokens of the first tensor are left alone.
+  const bool skip0 = skip_prefix0 != nullptr && t < skip_prefix0[t].y;
   const int half = d >> 1;
   if (threadIdx.x < half) {
     float c = 1.f, s = 0.f;
@@ -144,7 +147,7 @@ __global__ void rope_kernel(const Tin* __restrict__ x0, Tout* __restrict__ y0, i
   __syncthreads();
   // Each thread rotates 8 consecutive pairs (16-byte loads of bf16, 32-byte of fp32).
   const int chunks = half >> 3;
-  for (int which = 0; which < 2; ++which) {
+  for (int which = skip0 ? 1 : 0; which < 2; ++which) {
     const Tin* x = which ? x1 : x0;
     Tout* y = which ? y1 : y0;
     const int heads = which ? h1 : h0;
@@ -174,7 +177,8 @@ template <typename T, int D>
 __global__ void __launch_bounds__(256)
 fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                 T* __restrict__ o, float* __restrict__ lse, const int4* __restrict__ tok,
-                const FwdTile* __restrict__ tiles, int Hq, int Hkv, int Ttot, float qscale) {
+                const FwdTile* __restrict__ tiles, int Hq, int Hkv, int Ttot, float qscale,
+                int responses_only) {
   constexpr int BN = 64, NV = D / 16;
   extern __shared__ float4 smem4[];
   float* Ks = reinterpret_cast<float*>(smem4);
@@ -185,10 +189,12 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
     report(PG_ERR_DEVICE);
     return;
   }
+  // Responses only: a tile made of prefix rows has nothing to compute (uniform exit).
+  if (responses_only && tl.q1 <= tl.pe) return;
   const int kh = h / (Hq / Hkv);
   const int tid = threadIdx.x, r = tid >> 2, ql = tid & 3;
   const int row = tl.q0 + r;
-  const bool valid = row < tl.q1;
+  const bool valid = row < tl.q1 && !(responses_only && row < tl.pe);
   const int rowc = valid ? row : tl.q1 - 1;
   const int4 ti = tok[rowc];
   float4 qv[NV], acc[NV];
@@ -509,7 +515,7 @@ pg_status fwd_simt_t(const AttnArgs& a, const void* q, const void* k, const void
   kern<<<(unsigned)(n * a.Hq), 256, smem, a.stream>>>(
       static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
       static_cast<T*>(o), lse, tokens(L), tiles<FwdTile>(L, FWD64), a.Hq, a.Hkv,
-      (int)L->total_tokens, a.scale * kLog2e);
+      (int)L->total_tokens, a.scale * kLog2e, (a.flags & PG_FLAG_RESPONSES_ONLY) ? 1 : 0);
   prof_end(PG_KERNEL_ATTN_FWD, a.stream);
   return cuda_check(cudaGetLastError(), "fwd_simt launch");
 }
@@ -562,7 +568,8 @@ RopeFreq rope_freq(const AttnArgs& a) {
 
 pg_status launch_rope(const AttnArgs& a, const void* x0, void* y0, int heads0, const void* x1,
                       void* y1, int heads1, bool inverse, bool in_fp32, float2* table_out,
-                      const float2* table_in) {
+                      const float2* table_in, bool skip_prefix0) {
+  const int4* skip = skip_prefix0 ? tokens(a.layout) : nullptr;
   const int T = (int)a.layout->total_tokens;
   const int rope = a.theta > 0.f ? 1 : 0;
   const RopeFreq f = rope_freq(a);
@@ -575,17 +582,17 @@ pg_status launch_rope(const AttnArgs& a, const void* x0, void* y0, int heads0, c
     rope_kernel<float, float><<<grid, block, 0, a.stream>>>(
         static_cast<const float*>(x0), static_cast<float*>(y0), heads0,
         static_cast<const float*>(x1), static_cast<float*>(y1), heads1, a.d, pos, f, rope, sgn,
-        table_out, table_in);
+        table_out, table_in, skip);
   } else if (in_fp32) {
     rope_kernel<float, __nv_bfloat16><<<grid, block, 0, a.stream>>>(
         static_cast<const float*>(x0), static_cast<__nv_bfloat16*>(y0), heads0,
         static_cast<const float*>(x1), static_cast<__nv_bfloat16*>(y1), heads1, a.d, pos, f, rope,
-        sgn, table_out, table_in);
+        sgn, table_out, table_in, skip);
   } else {
     rope_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, block, 0, a.stream>>>(
         static_cast<const __nv_bfloat16*>(x0), static_cast<__nv_bfloat16*>(y0), heads0,
         static_cast<const __nv_bfloat16*>(x1), static_cast<__nv_bfloat16*>(y1), heads1, a.d, pos,
-        f, rope, sgn, table_out, table_in);
+        f, rope, sgn, table_out, table_in, skip);
   }
   prof_end(kid, a.stream);
   return cuda_check(cudaGetLastError(), "rope launch");

@@ -50,6 +50,34 @@ pg_status make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, 
   return PG_OK;
 }
 
+pg_status make_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1,
+                            uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes,
+                            uint32_t box0, uint32_t box1, uint32_t box2) {
+  auto fn = encode_fn();
+  if (!fn) {
+    set_error("cuTensorMapEncodeTiled is not available from the driver");
+    return PG_ERR_CUDA;
+  }
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) || (stride1_bytes & 15u) || (stride2_bytes & 15u)) {
+    set_error("TMA needs 16-byte aligned base and strides");
+    return PG_ERR_INVALID_ARG;
+  }
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  cuuint32_t box[3] = {box0, box1, box2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled (3-D) failed (%d): dims %llu x %llu x %llu, box %u x %u x %u",
+              (int)r, (unsigned long long)d0, (unsigned long long)d1, (unsigned long long)d2,
+              box0, box1, box2);
+    return PG_ERR_CUDA;
+  }
+  return PG_OK;
+}
+
 pg_status make_tmap_2d_b32(CUtensorMap* map, const void* base, bool is_float, uint64_t inner,
                            uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
                            uint32_t box_outer) {

@@ -34,10 +34,13 @@ class Workload:
     rope_theta: float = 0.0          # 0 disables RoPE
     input_scale: float = 1.0         # Q, K, V are N(0,1) * input_scale; dO is N(0,1)
     seed: int = 1000
+    responses_only: bool = False     # forward of the response rows only (scoring)
 
 
-# The five workloads: index 0 is the small fp32 case, 1..3 the bf16 attention cases, and the
-# decoder-layer workload (index 4) is described by LayerWorkload below.
+# Index 0 is the small fp32 case, 1..3 the bf16 fwd+bwd attention cases, 4 the forward-only
+# scoring case: 16 candidate continuations of 1-4 tokens scored against one 32k-token context (the
+# short-suffix shape in which grouped attention is bound by reading K/V, Pith review "Core claim").
+# The decoder-layer workload is described by LayerWorkload below.
 WORKLOADS: List[Workload] = [
     Workload("fp32_h2_d64_p256_g4", "f32", 1, 4, 256, 2, 2, 64,
              suffix_lens=(32, 48, 64, 16), rope_theta=0.0, seed=1000),
@@ -47,6 +50,8 @@ WORKLOADS: List[Workload] = [
              suffix_range=(64, 512), rope_theta=1e4, seed=1002),
     Workload("bf16_gqa32x8_d128_p16384_g16_r256-1024", "bf16", 1, 16, 16384, 32, 8, 128,
              suffix_range=(256, 1024), rope_theta=5e5, seed=1003),
+    Workload("bf16_gqa32x8_d128_p32768_g16_r1-4_score", "bf16", 1, 16, 32768, 32, 8, 128,
+             suffix_range=(1, 4), rope_theta=5e5, seed=1005, responses_only=True),
 ]
 
 

@@ -95,6 +95,17 @@ def test_pack_host_matches_oracle_bit_exactly(case):
             keys[s_lo:s_hi] = True
             assert not bool((mask[q0:q1] & ~keys[None, :]).any())
         assert torch.equal(covered, torch.ones(T, dtype=torch.int32))
+    # response spans: one per group with response rows, in group order
+    spans, g0, s = [], 0, 0
+    for lp, g in zip(plens, gsz):
+        pe = g0 + lp
+        gend = pe + sum(rs[s:s + g])
+        s += g
+        if gend > pe:
+            spans.append([pe, gend, g0, pe, pe, gend, pe, 0])
+        g0 = gend
+    assert st.n_tiles[5] == len(spans) and lists[5].tolist() == spans
+    assert st.max_response_rows == max([sp[1] - sp[0] for sp in spans], default=0)
     for w, bm in [(2, 64), (3, 128)]:
         bt = lists[w]
         covered = torch.zeros(T, dtype=torch.int32)
@@ -144,6 +155,11 @@ def test_attention_rejects_bad_arguments_on_host():
     assert L.pg_grouped_attn_fwd(*args, p, bad, p, p, p, C.byref(opts), p, 4096, None) \
         == _lib.PG_ERR_INVALID_ARG
     assert b"16-byte" in L.pg_last_error_message()
+    # the responses-only option is forward-only
+    ro = _lib.PgOpts(0.0, 0.0, _lib.PG_FLAG_RESPONSES_ONLY, 0)
+    assert L.pg_grouped_attn_bwd(*args, p, p, p, p, p, p, p, p, p, C.byref(ro), p, 4096, None) \
+        == _lib.PG_ERR_INVALID_ARG
+    assert b"forward-only" in L.pg_last_error_message()
     neg = _lib.PgOpts(-1.0, 0.0, 0, 0)
     assert L.pg_grouped_attn_fwd(*args, p, p, p, p, p, C.byref(neg), p, 4096, None) \
         == _lib.PG_ERR_INVALID_ARG

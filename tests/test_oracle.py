@@ -293,3 +293,30 @@ def test_continuing_positions_change_outputs():
     S = (cont[:, h] @ kc[:, h].T) / math.sqrt(8)
     o = torch.softmax(S.masked_fill(~mask, float("-inf")), dim=1) @ v[:, h]
     assert (o[7:] - res.o[7:, h]).abs().max().item() > 1e-3
+
+
+# ---------------------------------------------------------------- responses-only rows -----------
+
+@pytest.mark.parametrize("case", CASES[:3])
+def test_response_rows_match_repeated_prefix(case):
+    plens, gsz, rs, Hq, Hkv, d, theta = case
+    lay, q, k, v, _ = problem(plens, gsz, rs, Hq, Hkv, d, seed=131)
+    full = orc.repeated_prefix(lay, q, k, v, theta=theta)
+    rows = [t for t in range(lay.total_tokens) if int(lay.token_segment[t]) >= 0]
+    o, lse = orc.response_rows(lay, q, k, v, rows, theta=theta)
+    assert orc.normwise_error(o, full.o[rows]) < 1e-12
+    assert orc.normwise_error(lse, full.lse[:, rows]) < 1e-12
+
+
+def test_response_rows_single_response_is_textbook_causal_attention():
+    # G = 1 with RoPE: row Lp + j of causal SDPA over [P; R] (rotated by the complex form).
+    theta, lp, r = 40.0, 11, 5
+    lay, q, k, v, _ = problem([lp], [1], [r], 4, 2, 8, seed=141)
+    pos = torch.arange(lp + r)
+    o_ref = F.scaled_dot_product_attention(
+        rope_complex_diff(q, pos, theta).transpose(0, 1)[None],
+        rope_complex_diff(k, pos, theta).repeat_interleave(2, dim=1).transpose(0, 1)[None],
+        v.repeat_interleave(2, dim=1).transpose(0, 1)[None], is_causal=True)[0].transpose(0, 1)
+    rows = list(range(lp, lp + r))
+    o, _ = orc.response_rows(lay, q, k, v, rows, theta=theta, q_heads=[1, 3])
+    assert orc.normwise_error(o, o_ref[rows][:, [1, 3]]) < 1e-12
