@@ -451,10 +451,19 @@ pg_status pg_grouped_attn_fwd(const pg_layout* layout, pg_dtype dtype, int32_t h
   const void* qx = q;
   const void* kx = k;
   const bool responses_only = (a.flags & PG_FLAG_RESPONSES_ONLY) != 0;
-  if (rope) {
-    // Responses only: the prefix rows of q are never read, so they are not rotated either.
+  if (rope && responses_only) {
+    // Every key is rotated; of q only the response rows, the only ones read.
+    st = launch_rope(a, k, ws + w.k_rot, heads_kv, nullptr, nullptr, 0, false, false, nullptr,
+                     nullptr);
+    if (st == PG_OK)
+      st = launch_rope(a, q, ws + w.q_rot, heads_q, nullptr, nullptr, 0, false, false, nullptr,
+                       nullptr, true);
+    if (st != PG_OK) return st;
+    qx = ws + w.q_rot;
+    kx = ws + w.k_rot;
+  } else if (rope) {
     st = launch_rope(a, q, ws + w.q_rot, heads_q, k, ws + w.k_rot, heads_kv, false, false,
-                     nullptr, nullptr, responses_only);
+                     nullptr, nullptr);
     if (st != PG_OK) return st;
     qx = ws + w.q_rot;
     kx = ws + w.k_rot;

@@ -463,7 +463,9 @@ attn_score_sm100_kernel(const __grid_constant__ CUtensorMap tq,
 
 // Merge of the splits: one warp per query row of a CTA slot; lane l owns dims [4 l, 4 l + 4).
 // O = sum_c 2^(lse_c - M) O_c / sum_c 2^(lse_c - M), LSE = (M + log2 sum_c 2^(lse_c - M)) ln 2,
-// with M the largest split LSE; splits that saw no key (LSE -inf) drop out.
+// with M the largest split LSE; splits that saw no key (LSE -inf) drop out.  The split LSEs are
+// read by the lanes in parallel (split c by lane c % 32), the weights reach every lane by shuffle,
+// and the split rows are accumulated four at a time so their loads overlap.
 __global__ void __launch_bounds__(256)
 score_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
                      __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
@@ -481,22 +483,39 @@ score_combine_kernel(const float* __restrict__ part_o, const float* __restrict__
   const int t_end = min(t0 + TB, sp.q1);
   if (m >= (t_end - t0) * hp) return;
   const int t = t0 + m / hp, h = kh * hp + m % hp;
-  float M = -INFINITY;
-  for (int c = 0; c < nsplit; ++c) M = fmaxf(M, part_lse[((size_t)c * nblk + blk) * ROWS + m]);
-  float W = 0.f;
+  // nsplit <= 64: lane l holds the LSEs of splits l and l + 32.
+  const size_t stride = (size_t)nblk * ROWS;
+  const float* pl = part_lse + (size_t)blk * ROWS + m;
+  const float la = lane < nsplit ? pl[lane * stride] : -INFINITY;
+  const float lb = lane + 32 < nsplit ? pl[(lane + 32) * stride] : -INFINITY;
+  float M = fmaxf(la, lb);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  const float wa = M == -INFINITY ? 0.f : exp2f(la - M);     // exp2(-inf) = 0 for empty splits
+  const float wb = M == -INFINITY ? 0.f : exp2f(lb - M);
+  float W = wa + wb;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+  const float* po = part_o + ((size_t)blk * ROWS + m) * D + 4 * lane;
+  const size_t ostride = stride * D;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (M != -INFINITY) {
-    for (int c = 0; c < nsplit; ++c) {
-      const size_t sl = (size_t)c * nblk + blk;
-      const float lc = part_lse[sl * ROWS + m];
-      if (lc == -INFINITY) continue;
-      const float w = exp2f(lc - M);
-      W += w;
-      const float4 v = *reinterpret_cast<const float4*>(part_o + (sl * ROWS + m) * D + 4 * lane);
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
+  for (int c0 = 0; c0 < nsplit; c0 += 4) {
+    float w[4];
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + u;
+      const float wc = __shfl_sync(0xffffffffu, c < 32 ? wa : wb, c & 31);
+      w[u] = c < nsplit ? wc : 0.f;
+      v[u] = (c < nsplit && w[u] > 0.f) ? *reinterpret_cast<const float4*>(po + c * ostride)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      acc.x = fmaf(w[u], v[u].x, acc.x);
+      acc.y = fmaf(w[u], v[u].y, acc.y);
+      acc.z = fmaf(w[u], v[u].z, acc.z);
+      acc.w = fmaf(w[u], v[u].w, acc.w);
     }
   }
   const float inv = W > 0.f ? 1.f / W : 0.f;

@@ -113,10 +113,10 @@ struct RopeFreq {
 };
 
 // SIMT kernels (pg_simt.cu).
-// skip_prefix0: leave the prefix tokens of (x0, y0) alone (responses-only forward).
+// responses_only: rotate the response tokens only (the layout's response spans).
 pg_status launch_rope(const AttnArgs& a, const void* x0, void* y0, int heads0, const void* x1,
                       void* y1, int heads1, bool inverse, bool in_fp32, float2* table_out,
-                      const float2* table_in, bool skip_prefix0 = false);
+                      const float2* table_in, bool responses_only = false);
 pg_status launch_fwd_simt(const AttnArgs& a, const void* q, const void* k, const void* v, void* o,
                           float* lse);
 pg_status launch_bwd_simt(const AttnArgs& a, const void* q, const void* k, const void* v,

@@ -13,6 +13,8 @@
 // and k + d/2 live in the same lane (d/2 is a multiple of 16).
 #include <math.h>
 
+#include <algorithm>
+
 #include "pg_internal.h"
 
 namespace pg {
@@ -113,54 +115,68 @@ __device__ __forceinline__ bool visible(int t, int s, int4 ti) {
 // in fp32.  With a table_out the (cos, sin) pairs are also stored ([T][d/2] float2) for later
 // passes of the same call; with a table_in they are read from it instead of recomputed.
 // `rope` false only converts (used to cast the fp32 gradient accumulators).
-// One block per token; two tensors (q and k) per launch.
+// A block handles `tpb` consecutive tokens (enough to give its 256 threads 16-byte chunks of work
+// when a token has few heads); two tensors (q and k) per launch.  With `spans` (the layout's
+// response spans) the blocks cover only the response tokens: `span_blocks` blocks per span.
 // ---------------------------------------------------------------------------------------------
+constexpr int kRopeThreads = 256;
+constexpr int kRopeMaxTokens = 8;
+
 template <typename Tin, typename Tout>
-__global__ void rope_kernel(const Tin* __restrict__ x0, Tout* __restrict__ y0, int h0,
-                            const Tin* __restrict__ x1, Tout* __restrict__ y1, int h1, int d,
-                            const int32_t* __restrict__ pos_ids, RopeFreq f, int rope, float sgn,
-                            float2* __restrict__ table_out, const float2* __restrict__ table_in,
-                            const int4* __restrict__ skip_prefix0) {
-  __shared__ float cs[64], sn[64];
-  const int t = blockIdx.x;
-  // With skip_prefix0 (the per-token table), prefix tokens of the first tensor are left alone.
-  const bool skip0 = skip_prefix0 != nullptr && t < skip_prefix0[t].y;
+__global__ void __launch_bounds__(kRopeThreads)
+rope_kernel(const Tin* __restrict__ x0, Tout* __restrict__ y0, int h0,
+            const Tin* __restrict__ x1, Tout* __restrict__ y1, int h1, int d, int Ttot, int tpb,
+            const FwdTile* __restrict__ spans, int span_blocks,
+            const int32_t* __restrict__ pos_ids, RopeFreq f, int rope, float sgn,
+            float2* __restrict__ table_out, const float2* __restrict__ table_in) {
+  __shared__ float cs[kRopeMaxTokens][64], sn[kRopeMaxTokens][64];
+  int t_first = blockIdx.x * tpb, t_limit = Ttot;
+  if (spans != nullptr) {
+    const FwdTile sp = spans[blockIdx.x / span_blocks];
+    t_first = sp.q0 + (blockIdx.x % span_blocks) * tpb;
+    t_limit = min(sp.q1, Ttot);
+    if (t_first >= t_limit) return;
+  }
   const int half = d >> 1;
-  if (threadIdx.x < half) {
+  for (int e = threadIdx.x; e < tpb * half; e += blockDim.x) {
+    const int tl = e / half, k = e - tl * half, t = t_first + tl;
     float c = 1.f, s = 0.f;
-    if (rope) {
+    if (rope && t < t_limit) {
       if (table_in) {
-        const float2 e = table_in[(size_t)t * half + threadIdx.x];
-        c = e.x;
-        s = e.y;
+        const float2 v = table_in[(size_t)t * half + k];
+        c = v.x;
+        s = v.y;
       } else {
         const double two_pi = 6.283185307179586476925;
-        const double a = (double)pos_ids[t] * f.inv[threadIdx.x];
+        const double a = (double)pos_ids[t] * f.inv[k];
         const double r = fma(-two_pi, rint(a * f.inv_two_pi), a);
         sincosf((float)r, &s, &c);
-        if (table_out) table_out[(size_t)t * half + threadIdx.x] = make_float2(c, s);
+        if (table_out) table_out[(size_t)t * half + k] = make_float2(c, s);
       }
     }
-    cs[threadIdx.x] = c;
-    sn[threadIdx.x] = sgn * s;
+    cs[tl][k] = c;
+    sn[tl][k] = sgn * s;
   }
   __syncthreads();
-  // Each thread rotates 8 consecutive pairs (16-byte loads of bf16, 32-byte of fp32).
+  // Each work item rotates 8 consecutive pairs of one head of one token (16-byte loads of bf16,
+  // 32-byte of fp32).
   const int chunks = half >> 3;
-  for (int which = skip0 ? 1 : 0; which < 2; ++which) {
+  for (int which = 0; which < 2; ++which) {
     const Tin* x = which ? x1 : x0;
     Tout* y = which ? y1 : y0;
     const int heads = which ? h1 : h0;
-    const size_t base = (size_t)t * heads * d;
-    for (int idx = threadIdx.x; idx < heads * chunks; idx += blockDim.x) {
-      const int h = idx / chunks, k0 = (idx - h * chunks) * 8;
-      const size_t i1 = base + (size_t)h * d + k0;
+    const int per_token = heads * chunks;
+    for (int idx = threadIdx.x; idx < tpb * per_token; idx += blockDim.x) {
+      const int tl = idx / per_token, rem = idx - tl * per_token, t = t_first + tl;
+      if (t >= t_limit) break;
+      const int h = rem / chunks, k0 = (rem - h * chunks) * 8;
+      const size_t i1 = ((size_t)t * heads + h) * d + k0;
       float a[8], b[8], lo[8], hi[8];
       Vec<Tin>::load8(x + i1, a);
       Vec<Tin>::load8(x + i1 + half, b);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float c = cs[k0 + e], s = sn[k0 + e];
+        const float c = cs[tl][k0 + e], s = sn[tl][k0 + e];
         lo[e] = a[e] * c - b[e] * s;
         hi[e] = b[e] * c + a[e] * s;
       }
@@ -568,31 +584,39 @@ RopeFreq rope_freq(const AttnArgs& a) {
 
 pg_status launch_rope(const AttnArgs& a, const void* x0, void* y0, int heads0, const void* x1,
                       void* y1, int heads1, bool inverse, bool in_fp32, float2* table_out,
-                      const float2* table_in, bool skip_prefix0) {
-  const int4* skip = skip_prefix0 ? tokens(a.layout) : nullptr;
+                      const float2* table_in, bool responses_only) {
   const int T = (int)a.layout->total_tokens;
   const int rope = a.theta > 0.f ? 1 : 0;
   const RopeFreq f = rope_freq(a);
   const float sgn = inverse ? -1.f : 1.f;
   const int32_t* pos = a.layout->position_ids;
-  dim3 grid(T), block(128);
+  // Tokens per block: enough 16-byte work items (heads x d/16 per token) for the block's threads.
+  const int items = (heads0 + (x1 ? heads1 : 0)) * (a.d / 16);
+  const int tpb = std::max(1, std::min(kRopeMaxTokens, kRopeThreads / std::max(items, 1)));
+  const FwdTile* spans = responses_only ? tiles<FwdTile>(a.layout, SPANS) : nullptr;
+  const int span_blocks =
+      responses_only ? (int)std::max<int64_t>(1, (a.layout->max_response_rows + tpb - 1) / tpb) : 1;
+  const int64_t nblocks =
+      responses_only ? a.layout->n_tiles[SPANS] * span_blocks : (T + tpb - 1) / tpb;
+  if (nblocks == 0) return PG_OK;
+  dim3 grid((unsigned)nblocks), block(kRopeThreads);
   const pg_kernel kid = inverse ? PG_KERNEL_ROPE_BWD : PG_KERNEL_ROPE;
   prof_begin(kid, a.stream);
   if (a.dtype == PG_F32) {
     rope_kernel<float, float><<<grid, block, 0, a.stream>>>(
         static_cast<const float*>(x0), static_cast<float*>(y0), heads0,
-        static_cast<const float*>(x1), static_cast<float*>(y1), heads1, a.d, pos, f, rope, sgn,
-        table_out, table_in, skip);
+        static_cast<const float*>(x1), static_cast<float*>(y1), heads1, a.d, T, tpb, spans, span_blocks, pos, f,
+        rope, sgn, table_out, table_in);
   } else if (in_fp32) {
     rope_kernel<float, __nv_bfloat16><<<grid, block, 0, a.stream>>>(
         static_cast<const float*>(x0), static_cast<__nv_bfloat16*>(y0), heads0,
-        static_cast<const float*>(x1), static_cast<__nv_bfloat16*>(y1), heads1, a.d, pos, f, rope,
-        sgn, table_out, table_in, skip);
+        static_cast<const float*>(x1), static_cast<__nv_bfloat16*>(y1), heads1, a.d, T, tpb, spans, span_blocks,
+        pos, f, rope, sgn, table_out, table_in);
   } else {
     rope_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, block, 0, a.stream>>>(
         static_cast<const __nv_bfloat16*>(x0), static_cast<__nv_bfloat16*>(y0), heads0,
-        static_cast<const __nv_bfloat16*>(x1), static_cast<__nv_bfloat16*>(y1), heads1, a.d, pos,
-        f, rope, sgn, table_out, table_in, skip);
+        static_cast<const __nv_bfloat16*>(x1), static_cast<__nv_bfloat16*>(y1), heads1, a.d, T, tpb,
+        spans, span_blocks, pos, f, rope, sgn, table_out, table_in);
   }
   prof_end(kid, a.stream);
   return cuda_check(cudaGetLastError(), "rope launch");
