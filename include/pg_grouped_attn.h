@@ -102,6 +102,8 @@ typedef struct pg_layout {
   const int32_t* position_ids; /* [T] */
   const void* tables;
   int64_t max_response_rows; /* the largest number of response rows (sum of R_bi) in one group */
+  int64_t n_pad_rows;      /* padded layouts (pg_pack_padded): number of padding rows, else 0 */
+  int64_t off_pad_rows;    /* byte offset of the padding rows' indices (int32) in the tables */
 } pg_layout;
 
 /*
@@ -137,6 +139,33 @@ pg_status pg_pack_host(int32_t num_groups, const int32_t* prefix_lens, const int
 pg_status pg_pack(int32_t num_groups, const int32_t* prefix_lens, const int32_t* group_sizes,
                   const int32_t* suffix_lens, int32_t* position_ids_dev, void* tables_dev,
                   int64_t table_bytes, pg_layout* layout, pg_stream_t stream);
+
+/*
+ * Padded layout (skill page "prefix-grouper-grpo", Step 3 "Restructure Input Format"): each of the
+ * num_groups groups is [P; slot_1; ...; slot_G] with prefix_len prefix tokens and group_size slots
+ * of max_response_len tokens; response i of group b fills the first response_lens[b * group_size +
+ * i] tokens of its slot and the rest of the slot is padding (where that page's attention mask is 0).
+ * Padding only ever trails a response, so causal attention never lets a real token see it: the
+ * padded buffer is run as a packed layout whose responses all have max_response_len tokens (so
+ * positions, tiles and pairs count the padding too), and the layout also lists the padding rows.
+ * With such a layout pg_grouped_attn_fwd writes o = 0 and lse = +inf on padding rows (+inf makes
+ * exp(s - lse) = 0, so in the backward a padding query has no weight: its dO must be finite but
+ * is otherwise ignored) and pg_grouped_attn_bwd writes dq = dk = dv = 0 on them.  Real rows get the
+ * results of the unpadded packing.  Padding rows still cost kernel time in proportion to their
+ * number.  Buffers and errors as pg_pack_size / pg_pack_host / pg_pack; additionally
+ * PG_ERR_INVALID_ARG if a response length is outside [0, max_response_len].
+ */
+pg_status pg_pack_padded_size(int32_t num_groups, int32_t prefix_len, int32_t group_size,
+                              int32_t max_response_len, const int32_t* response_lens,
+                              int64_t* total_tokens, int64_t* table_bytes);
+pg_status pg_pack_padded_host(int32_t num_groups, int32_t prefix_len, int32_t group_size,
+                              int32_t max_response_len, const int32_t* response_lens,
+                              int32_t* position_ids, void* tables, int64_t table_bytes,
+                              pg_layout* layout);
+pg_status pg_pack_padded(int32_t num_groups, int32_t prefix_len, int32_t group_size,
+                         int32_t max_response_len, const int32_t* response_lens,
+                         int32_t* position_ids_dev, void* tables_dev, int64_t table_bytes,
+                         pg_layout* layout, pg_stream_t stream);
 
 /*
  * Workspace bytes for pg_grouped_attn_fwd (phase 0) or pg_grouped_attn_bwd (phase 1) with this
@@ -187,7 +216,8 @@ typedef enum pg_kernel {
   PG_KERNEL_ROPE_BWD = 6,        /* inverse RoPE of dQ/dK and the cast to the output dtype */
   PG_KERNEL_GEMM = 7,            /* the bf16 tensor-core GEMM (decoder-layer path) */
   PG_KERNEL_LAYER = 8,           /* RMSNorm / SwiGLU kernels of the decoder-layer path */
-  PG_KERNEL_SCORE_COMBINE = 9    /* merge of the responses-only forward's key splits */
+  PG_KERNEL_SCORE_COMBINE = 9,   /* merge of the responses-only forward's key splits */
+  PG_KERNEL_PAD_FILL = 10        /* padded layouts: outputs / gradients of the padding rows */
 } pg_kernel;
 
 /*

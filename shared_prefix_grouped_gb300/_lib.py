@@ -27,6 +27,8 @@ class PgLayout(C.Structure):
         ("position_ids", C.c_void_p),
         ("tables", C.c_void_p),
         ("max_response_rows", C.c_int64),
+        ("n_pad_rows", C.c_int64),
+        ("off_pad_rows", C.c_int64),
     ]
 
 
@@ -51,7 +53,7 @@ class PgProfile(C.Structure):
 
 (PG_KERNEL_NONE, PG_KERNEL_ROPE, PG_KERNEL_ATTN_FWD, PG_KERNEL_BWD_PREPROCESS, PG_KERNEL_BWD_DKDV,
  PG_KERNEL_BWD_DQ, PG_KERNEL_ROPE_BWD, PG_KERNEL_GEMM, PG_KERNEL_LAYER,
- PG_KERNEL_SCORE_COMBINE) = range(10)
+ PG_KERNEL_SCORE_COMBINE, PG_KERNEL_PAD_FILL) = range(11)
 
 I32P = C.POINTER(C.c_int32)
 I64P = C.POINTER(C.c_int64)
@@ -64,6 +66,12 @@ SIGNATURES = {
                                C.POINTER(PgLayout)]),
     "pg_pack": (C.c_int, [C.c_int32, I32P, I32P, I32P, VP, VP, C.c_int64, C.POINTER(PgLayout),
                           VP]),
+    "pg_pack_padded_size": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, I32P, I64P,
+                                      I64P]),
+    "pg_pack_padded_host": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, I32P, I32P, VP,
+                                      C.c_int64, C.POINTER(PgLayout)]),
+    "pg_pack_padded": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, I32P, VP, VP,
+                                 C.c_int64, C.POINTER(PgLayout), VP]),
     "pg_workspace_size": (C.c_int, [C.POINTER(PgLayout), C.c_int, C.c_int32, C.c_int32,
                                     C.c_int32, C.POINTER(PgOpts), C.c_int32,
                                     C.POINTER(C.c_size_t)]),

@@ -78,6 +78,53 @@ def pack(prefix_lens: Sequence[int], group_sizes: Sequence[int], suffix_lens: Se
     return Layout(prefix_lens, group_sizes, suffix_lens, st, pos, tab)
 
 
+def _padded_args(num_groups, prefix_len, group_size, max_response_len, response_lens):
+    assert len(response_lens) == num_groups * group_size
+    return (int(num_groups), int(prefix_len), int(group_size), int(max_response_len),
+            int_array(response_lens))
+
+
+def pack_padded_size(num_groups: int, prefix_len: int, group_size: int, max_response_len: int,
+                     response_lens: Sequence[int]):
+    T, nb = C.c_int64(), C.c_int64()
+    check("pg_pack_padded_size", _lib.lib().pg_pack_padded_size(
+        *_padded_args(num_groups, prefix_len, group_size, max_response_len, response_lens),
+        C.byref(T), C.byref(nb)))
+    return T.value, nb.value
+
+
+def pack_padded_host(num_groups: int, prefix_len: int, group_size: int, max_response_len: int,
+                     response_lens: Sequence[int]):
+    """Host-only padded packing: (position_ids, tables, struct), as pack_host."""
+    T, nb = pack_padded_size(num_groups, prefix_len, group_size, max_response_len, response_lens)
+    pos = torch.empty(T, dtype=torch.int32)
+    tab = torch.empty(nb, dtype=torch.uint8)
+    st = PgLayout()
+    check("pg_pack_padded_host", _lib.lib().pg_pack_padded_host(
+        *_padded_args(num_groups, prefix_len, group_size, max_response_len, response_lens),
+        C.cast(pos.data_ptr(), _lib.I32P), C.c_void_p(tab.data_ptr()), nb, C.byref(st)))
+    return pos, tab, st
+
+
+def pack_padded(num_groups: int, prefix_len: int, group_size: int, max_response_len: int,
+                response_lens: Sequence[int], device="cuda") -> Layout:
+    """Layout of a padded batch [P; slot_1; ...; slot_G] per group (slots of max_response_len
+    tokens, response i in the first response_lens[i] of its slot); attention calls on it write
+    zeros (and lse = +inf) on the padding rows."""
+    device = torch.device(device)
+    T, nb = pack_padded_size(num_groups, prefix_len, group_size, max_response_len, response_lens)
+    pos = torch.empty(T, dtype=torch.int32, device=device)
+    tab = torch.empty(nb, dtype=torch.uint8, device=device)
+    st = PgLayout()
+    with torch.cuda.device(device):
+        check("pg_pack_padded", _lib.lib().pg_pack_padded(
+            *_padded_args(num_groups, prefix_len, group_size, max_response_len, response_lens),
+            C.c_void_p(pos.data_ptr()), C.c_void_p(tab.data_ptr()), nb, C.byref(st),
+            _stream_ptr(device)))
+    return Layout([prefix_len] * num_groups, [group_size] * num_groups,
+                  [max_response_len] * (num_groups * group_size), st, pos, tab)
+
+
 def make_opts(rope_theta: float = 0.0, softmax_scale: float = 0.0, flags: int = 0,
               debug: int = 0) -> PgOpts:
     return PgOpts(float(softmax_scale), float(rope_theta), int(flags), int(debug))

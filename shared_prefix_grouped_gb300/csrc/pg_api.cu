@@ -50,6 +50,7 @@ struct Plan {
   int64_t off[NUM_LISTS] = {0, 0, 0, 0, 0, 0};
   int64_t off_tokens = 0, bytes = 0;
   int64_t max_resp = 0;   // largest number of response rows in one group
+  int64_t n_pad = 0, off_pad = 0;   // padded layouts: padding-row list
 };
 
 static pg_status check_lengths(int32_t B, const int32_t* lp, const int32_t* gs, const int32_t* rs,
@@ -229,6 +230,55 @@ static void build_tables(int32_t B, const int32_t* lp, const int32_t* gs, const 
   memcpy(tables + p.off[SPANS], spans.data(), spans.size() * sizeof(FwdTile));
 }
 
+// Padded layouts: the same plan as packing every slot at its full length, plus the list of
+// padding rows appended to the tables.
+struct Padded {
+  std::vector<int32_t> lp, gs, rs;
+  const int32_t* rlen = nullptr;
+  int32_t R = 0;
+};
+
+static pg_status plan_padded(int32_t B, int32_t Lp, int32_t G, int32_t R, const int32_t* rlen,
+                             Padded* pd, Plan* p) {
+  if (B < 1 || Lp < 0 || G < 0 || R < 0 || (G > 0 && R > 0 && !rlen)) {
+    set_error("pg_pack_padded: num_groups >= 1, lengths >= 0 and response_lens non-NULL required");
+    return PG_ERR_INVALID_ARG;
+  }
+  int64_t n_pad = 0;
+  for (int64_t i = 0; i < (int64_t)B * G; ++i) {
+    const int32_t r = R > 0 ? rlen[i] : 0;
+    if (r < 0 || r > R) {
+      set_error("pg_pack_padded: response %lld has length %d outside [0, %d]", (long long)i, r, R);
+      return PG_ERR_INVALID_ARG;
+    }
+    n_pad += R - r;
+  }
+  pd->lp.assign(B, Lp);
+  pd->gs.assign(B, G);
+  pd->rs.assign((size_t)B * G, R);
+  pd->rlen = rlen;
+  pd->R = R;
+  pg_status st = check_lengths(B, pd->lp.data(), pd->gs.data(), pd->rs.data(), p);
+  if (st != PG_OK) return st;
+  p->n_pad = n_pad;
+  p->off_pad = p->bytes;
+  p->bytes = align_up(p->bytes + 4 * n_pad, 256);
+  return PG_OK;
+}
+
+static void build_pad_list(int32_t B, int32_t Lp, int32_t G, const Padded& pd, const Plan& p,
+                           char* tables) {
+  int32_t* out = reinterpret_cast<int32_t*>(tables + p.off_pad);
+  int64_t row = 0, n = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    row += Lp;
+    for (int32_t i = 0; i < G; ++i, row += pd.R) {
+      const int32_t r = pd.R > 0 ? pd.rlen[(int64_t)b * G + i] : 0;
+      for (int32_t j = r; j < pd.R; ++j) out[n++] = (int32_t)(row + j);
+    }
+  }
+}
+
 static void fill_layout(int32_t B, const Plan& p, const int32_t* pos, const void* tables,
                         pg_layout* L) {
   memset(L, 0, sizeof(*L));
@@ -246,6 +296,29 @@ static void fill_layout(int32_t B, const Plan& p, const int32_t* pos, const void
   L->position_ids = pos;
   L->tables = tables;
   L->max_response_rows = p.max_resp;
+  L->n_pad_rows = p.n_pad;
+  L->off_pad_rows = p.off_pad;
+}
+
+// Copies a host-built layout to the caller's device buffers and points *layout at them.
+static pg_status upload_layout(const std::vector<int32_t>& pos, const std::vector<char>& tab,
+                               int32_t* position_ids_dev, void* tables_dev, const pg_layout& host,
+                               pg_layout* layout, cudaStream_t s) {
+  pg_status st = cuda_check(cudaMemcpyAsync(position_ids_dev, pos.data(), pos.size() * 4,
+                                            cudaMemcpyHostToDevice, s),
+                            "pg_pack: copy position ids");
+  if (st != PG_OK) return st;
+  st = cuda_check(cudaMemcpyAsync(tables_dev, tab.data(), tab.size(), cudaMemcpyHostToDevice, s),
+                  "pg_pack: copy tables");
+  if (st != PG_OK) return st;
+  // Pageable-source copies return once the source has been staged; make that explicit so the
+  // vectors can be released whatever the runtime's staging policy.
+  st = cuda_check(cudaStreamSynchronize(s), "pg_pack: synchronize");
+  if (st != PG_OK) return st;
+  *layout = host;
+  layout->position_ids = position_ids_dev;
+  layout->tables = tables_dev;
+  return PG_OK;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -398,21 +471,66 @@ pg_status pg_pack(int32_t num_groups, const int32_t* prefix_lens, const int32_t*
   st = pg_pack_host(num_groups, prefix_lens, group_sizes, suffix_lens, pos.data(), tab.data(),
                     p.bytes, &host);
   if (st != PG_OK) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  st = cuda_check(cudaMemcpyAsync(position_ids_dev, pos.data(), pos.size() * 4,
-                                  cudaMemcpyHostToDevice, s), "pg_pack: copy position ids");
+  return upload_layout(pos, tab, position_ids_dev, tables_dev, host, layout,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+pg_status pg_pack_padded_size(int32_t num_groups, int32_t prefix_len, int32_t group_size,
+                              int32_t max_response_len, const int32_t* response_lens,
+                              int64_t* total_tokens, int64_t* table_bytes) {
+  Plan p;
+  Padded pd;
+  pg_status st = plan_padded(num_groups, prefix_len, group_size, max_response_len, response_lens,
+                             &pd, &p);
   if (st != PG_OK) return st;
-  st = cuda_check(cudaMemcpyAsync(tables_dev, tab.data(), tab.size(), cudaMemcpyHostToDevice, s),
-                  "pg_pack: copy tables");
-  if (st != PG_OK) return st;
-  // Pageable-source copies return once the source has been staged; make that explicit so the
-  // vectors can be released whatever the runtime's staging policy.
-  st = cuda_check(cudaStreamSynchronize(s), "pg_pack: synchronize");
-  if (st != PG_OK) return st;
-  *layout = host;
-  layout->position_ids = position_ids_dev;
-  layout->tables = tables_dev;
+  if (total_tokens) *total_tokens = p.T;
+  if (table_bytes) *table_bytes = p.bytes;
   return PG_OK;
+}
+
+pg_status pg_pack_padded_host(int32_t num_groups, int32_t prefix_len, int32_t group_size,
+                              int32_t max_response_len, const int32_t* response_lens,
+                              int32_t* position_ids, void* tables, int64_t table_bytes,
+                              pg_layout* layout) {
+  Plan p;
+  Padded pd;
+  pg_status st = plan_padded(num_groups, prefix_len, group_size, max_response_len, response_lens,
+                             &pd, &p);
+  if (st != PG_OK) return st;
+  if (!position_ids || !tables || !layout || table_bytes < p.bytes) {
+    set_error("pg_pack_padded_host: NULL buffer or table buffer smaller than %lld bytes",
+              (long long)p.bytes);
+    return PG_ERR_INVALID_ARG;
+  }
+  memset(tables, 0, (size_t)p.bytes);
+  build_tables(num_groups, pd.lp.data(), pd.gs.data(), pd.rs.data(), p, position_ids,
+               static_cast<char*>(tables));
+  build_pad_list(num_groups, prefix_len, group_size, pd, p, static_cast<char*>(tables));
+  fill_layout(num_groups, p, position_ids, tables, layout);
+  return PG_OK;
+}
+
+pg_status pg_pack_padded(int32_t num_groups, int32_t prefix_len, int32_t group_size,
+                         int32_t max_response_len, const int32_t* response_lens,
+                         int32_t* position_ids_dev, void* tables_dev, int64_t table_bytes,
+                         pg_layout* layout, pg_stream_t stream) {
+  int64_t T = 0, bytes = 0;
+  pg_status st = pg_pack_padded_size(num_groups, prefix_len, group_size, max_response_len,
+                                     response_lens, &T, &bytes);
+  if (st != PG_OK) return st;
+  if (!position_ids_dev || !tables_dev || !layout || table_bytes < bytes) {
+    set_error("pg_pack_padded: NULL buffer or table buffer smaller than %lld bytes",
+              (long long)bytes);
+    return PG_ERR_INVALID_ARG;
+  }
+  std::vector<int32_t> pos((size_t)T);
+  std::vector<char> tab((size_t)bytes);
+  pg_layout host;
+  st = pg_pack_padded_host(num_groups, prefix_len, group_size, max_response_len, response_lens,
+                           pos.data(), tab.data(), bytes, &host);
+  if (st != PG_OK) return st;
+  return upload_layout(pos, tab, position_ids_dev, tables_dev, host, layout,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 pg_status pg_workspace_size(const pg_layout* layout, pg_dtype dtype, int32_t heads_q,
@@ -470,15 +588,20 @@ pg_status pg_grouped_attn_fwd(const pg_layout* layout, pg_dtype dtype, int32_t h
   }
   if (responses_only) {
     if (!(a.flags & PG_FLAG_SIMT) && score_sm100_supported(a))
-      return launch_score_sm100(
+      st = launch_score_sm100(
           a, qx, kx, v, o, lse,
           w.part_o == SIZE_MAX ? nullptr : reinterpret_cast<float*>(ws + w.part_o),
           w.part_lse == SIZE_MAX ? nullptr : reinterpret_cast<float*>(ws + w.part_lse));
-    return launch_fwd_simt(a, qx, kx, v, o, lse);
+    else
+      st = launch_fwd_simt(a, qx, kx, v, o, lse);
+  } else if (!(a.flags & PG_FLAG_SIMT) && fwd_sm100_supported(a)) {
+    st = launch_fwd_sm100(a, qx, kx, v, o, lse);
+  } else {
+    st = launch_fwd_simt(a, qx, kx, v, o, lse);
   }
-  if (!(a.flags & PG_FLAG_SIMT) && fwd_sm100_supported(a))
-    return launch_fwd_sm100(a, qx, kx, v, o, lse);
-  return launch_fwd_simt(a, qx, kx, v, o, lse);
+  if (st != PG_OK || layout->n_pad_rows == 0) return st;
+  // Padded layout: o = 0 and lse = +inf on the padding rows.
+  return launch_pad_fill(a, o, heads_q, nullptr, 0, nullptr, 0, lse);
 }
 
 pg_status pg_grouped_attn_bwd(const pg_layout* layout, pg_dtype dtype, int32_t heads_q,
@@ -524,14 +647,17 @@ pg_status pg_grouped_attn_bwd(const pg_layout* layout, pg_dtype dtype, int32_t h
     // in the fp32 accumulator and is rotated back and cast here.
     st = launch_bwd_sm100(a, qx, kx, v, dO, lse2, Dbuf, dq_acc, dk, dv, rope_tab);
     if (st != PG_OK) return st;
-    return launch_rope(a, dq_acc, dq, heads_q, nullptr, nullptr, 0, true, true, nullptr,
-                       rope_tab);
+    st = launch_rope(a, dq_acc, dq, heads_q, nullptr, nullptr, 0, true, true, nullptr, rope_tab);
+  } else {
+    st = launch_bwd_simt(a, qx, kx, v, o, lse, dO, Dbuf, dq_acc, dk_acc, dv);
+    if (st != PG_OK) return st;
+    // dQ and dK of the rotated q/k back to the caller's q/k (inverse rotation) and dtype.
+    st = launch_rope(a, dq_acc, dq, heads_q, dk_acc, dk, heads_kv, true, true, nullptr, rope_tab);
   }
-  st = launch_bwd_simt(a, qx, kx, v, o, lse, dO, Dbuf, dq_acc, dk_acc, dv);
-  if (st != PG_OK) return st;
-  // dQ and dK of the rotated q/k back to the caller's q/k (inverse rotation) and dtype.
-  return launch_rope(a, dq_acc, dq, heads_q, dk_acc, dk, heads_kv, true, true, nullptr,
-                     rope_tab);
+  if (st != PG_OK || layout->n_pad_rows == 0) return st;
+  // Padded layout: the padding rows' gradients are zero (their queries had no weight; no real
+  // query sees their keys); write them as exact zeros.
+  return launch_pad_fill(a, dq, heads_q, dk, heads_kv, dv, heads_kv, nullptr);
 }
 
 pg_status pg_set_profile(pg_profile* profile) {

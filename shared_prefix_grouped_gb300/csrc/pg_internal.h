@@ -122,6 +122,10 @@ pg_status launch_fwd_simt(const AttnArgs& a, const void* q, const void* k, const
 pg_status launch_bwd_simt(const AttnArgs& a, const void* q, const void* k, const void* v,
                           const void* o, const float* lse, const void* dO, float* Dbuf,
                           float* dq_acc, float* dk_acc, void* dv);
+// Padded layouts: zero the padding rows of up to three [T, heads, d] tensors of the call's dtype
+// and, with lse, set lse[h][row] = +inf on them.
+pg_status launch_pad_fill(const AttnArgs& a, void* x0, int heads0, void* x1, int heads1, void* x2,
+                          int heads2, float* lse);
 pg_status launch_bwd_preprocess(const AttnArgs& a, const void* o, const void* dO, const float* lse,
                                 float* Dbuf, float* lse2, float* dq_acc);
 

@@ -622,6 +622,46 @@ pg_status launch_rope(const AttnArgs& a, const void* x0, void* y0, int heads0, c
   return cuda_check(cudaGetLastError(), "rope launch");
 }
 
+// Padded layouts: one block per padding row (grid-stride), 16-byte zero stores over each tensor's
+// row, and lse = +inf for every head.
+__global__ void __launch_bounds__(256)
+pad_fill_kernel(const int32_t* __restrict__ rows, int64_t n, uint4* __restrict__ x0,
+                int64_t v0, uint4* __restrict__ x1, int64_t v1, uint4* __restrict__ x2,
+                int64_t v2, float* __restrict__ lse, int Hq, int64_t Ttot) {
+  for (int64_t i = blockIdx.x; i < n; i += gridDim.x) {
+    const int64_t r = rows[i];
+    if (r < 0 || r >= Ttot) {
+      report(PG_ERR_DEVICE);
+      continue;
+    }
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    for (int64_t e = threadIdx.x; e < v0; e += blockDim.x) x0[r * v0 + e] = z;
+    if (x1)
+      for (int64_t e = threadIdx.x; e < v1; e += blockDim.x) x1[r * v1 + e] = z;
+    if (x2)
+      for (int64_t e = threadIdx.x; e < v2; e += blockDim.x) x2[r * v2 + e] = z;
+    if (lse)
+      for (int h = threadIdx.x; h < Hq; h += blockDim.x) lse[(size_t)h * Ttot + r] = INFINITY;
+  }
+}
+
+pg_status launch_pad_fill(const AttnArgs& a, void* x0, int heads0, void* x1, int heads1, void* x2,
+                          int heads2, float* lse) {
+  const pg_layout* L = a.layout;
+  if (L->n_pad_rows == 0) return PG_OK;
+  const int64_t es = a.dtype == PG_F32 ? 4 : 2;
+  const int32_t* rows = reinterpret_cast<const int32_t*>(static_cast<const char*>(L->tables) +
+                                                         L->off_pad_rows);
+  const unsigned grid = (unsigned)std::min<int64_t>(L->n_pad_rows, 152 * 8);
+  prof_begin(PG_KERNEL_PAD_FILL, a.stream);
+  pad_fill_kernel<<<grid, 256, 0, a.stream>>>(
+      rows, L->n_pad_rows, static_cast<uint4*>(x0), heads0 * a.d * es / 16,
+      static_cast<uint4*>(x1), heads1 * a.d * es / 16, static_cast<uint4*>(x2),
+      heads2 * a.d * es / 16, lse, a.Hq, L->total_tokens);
+  prof_end(PG_KERNEL_PAD_FILL, a.stream);
+  return cuda_check(cudaGetLastError(), "pad fill launch");
+}
+
 pg_status launch_fwd_simt(const AttnArgs& a, const void* q, const void* k, const void* v, void* o,
                           float* lse) {
   if (a.dtype == PG_F32)

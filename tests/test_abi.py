@@ -163,3 +163,32 @@ def test_attention_rejects_bad_arguments_on_host():
     neg = _lib.PgOpts(-1.0, 0.0, 0, 0)
     assert L.pg_grouped_attn_fwd(*args, p, p, p, p, p, C.byref(neg), p, 4096, None) \
         == _lib.PG_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("B,Lp,G,R,rl", [
+    (2, 5, 3, 4, [4, 0, 2, 1, 4, 3]),
+    (1, 0, 2, 3, [1, 3]),
+    (3, 7, 1, 0, [0, 0, 0]),
+])
+def test_padded_layout_is_full_slot_packing_plus_pad_rows(B, Lp, G, R, rl):
+    # A padded batch is the packing with every response at max_response_len tokens; the layout
+    # additionally lists exactly the slot tails beyond each response's length.
+    pos, tab, st = api.pack_padded_host(B, Lp, G, R, rl)
+    pos2, tab2, st2 = api.pack_host([Lp] * B, [G] * B, [R] * (B * G))
+    assert torch.equal(pos, pos2) and st.total_tokens == st2.total_tokens == B * (Lp + G * R)
+    assert tab.numpy().tobytes()[:st2.table_bytes] == tab2.numpy().tobytes()
+    expect = []
+    for b in range(B):
+        for i in range(G):
+            s0 = b * (Lp + G * R) + Lp + i * R
+            expect += list(range(s0 + rl[b * G + i], s0 + R))
+    assert st.n_pad_rows == len(expect)
+    raw = tab.numpy().tobytes()[st.off_pad_rows: st.off_pad_rows + 4 * len(expect)]
+    assert torch.frombuffer(bytearray(raw), dtype=torch.int32).tolist() == expect if expect else True
+
+
+def test_padded_layout_rejects_bad_lengths():
+    with pytest.raises(_lib.PgError):
+        api.pack_padded_size(1, 4, 2, 3, [4, 1])
+    with pytest.raises(_lib.PgError):
+        api.pack_padded_size(1, 4, 2, 3, [-1, 1])
