@@ -304,7 +304,8 @@ def run_ours(args):
     torch.cuda.set_device(device)
     w = workloads.by_name(args.workload)
     prob = workloads.make_problem(w, seed=w.seed + rank)   # independent batch per rank
-    flags = _lib.PG_FLAG_SIMT if args.simt else 0
+    flags = (_lib.PG_FLAG_SIMT if args.simt else 0) | \
+        (_lib.PG_FLAG_DETERMINISTIC if args.deterministic else 0)
     step = Step(prob, device, flags)
     pairs = step.layout.pairs
     step_flops = flops.attn_flops(pairs, w.heads_q, w.head_dim, "fwdbwd")
@@ -359,7 +360,8 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic (seeded N(0,1) Q/K/V/dO; no dataset)",
-            "config": workload_config(w, prob, l2_note),
+            "config": dict(workload_config(w, prob, l2_note),
+                           deterministic_backward=bool(args.deterministic)),
             "tokens_per_s": prob.total_tokens * world / sec,
             "pct_bf16_peak": 100.0 * value / world / peak,
             "peak_source": peak_src,
@@ -604,6 +606,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=[w.name for w in workloads.WORKLOADS] + [workloads.LayerWorkload().name])
     ap.add_argument("--simt", action="store_true", help="force the fp32 SIMT kernels")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="bitwise-reproducible backward (query-major dQ kernel)")
     ap.add_argument("--skip-extras", action="store_true",
                     help="skip the e2e, repeated-prefix and CPU legs (profiling runs)")
     args = ap.parse_args()

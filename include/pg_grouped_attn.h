@@ -78,6 +78,15 @@ typedef struct pg_opts {
  */
 #define PG_FLAG_RESPONSES_ONLY 2u
 
+/*
+ * Backward with dq bitwise reproducible as well: the bf16 head_dim-128 path computes dq in a
+ * query-major tensor-core kernel (each row's dq summed by one CTA in a fixed key order, then
+ * inverse-rotated and cast in its epilogue) and dk / dv in the key-major kernel without its dQ
+ * part.  Without the flag dq is accumulated across key blocks with TMA reduce-adds (fp32, summation
+ * order not fixed).  The fp32 / SIMT path is deterministic either way.
+ */
+#define PG_FLAG_DETERMINISTIC 4u
+
 /* Test hook for the bounded-wait error path: the tensor-core forward never signals that P is
  * ready, so its MMA thread's wait runs out (after 50 ms instead of 2 s), the kernel records
  * PG_ERR_TIMEOUT in the status word and exits cleanly; the outputs are then undefined. */

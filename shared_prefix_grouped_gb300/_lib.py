@@ -11,6 +11,7 @@ PG_OK, PG_ERR_INVALID_ARG, PG_ERR_UNSUPPORTED, PG_ERR_CUDA, PG_ERR_TIMEOUT, PG_E
 PG_F32, PG_BF16 = 0, 1
 PG_FLAG_SIMT = 1
 PG_FLAG_RESPONSES_ONLY = 2
+PG_FLAG_DETERMINISTIC = 4
 
 
 class PgLayout(C.Structure):

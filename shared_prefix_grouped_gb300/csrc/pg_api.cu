@@ -36,6 +36,7 @@ pg_status read_kernel_status(bool clear, int32_t* code) {
   if (st == PG_OK) st = read_status_fwd_sm100(clear, code);
   if (st == PG_OK) st = read_status_bwd_sm100(clear, code);
   if (st == PG_OK) st = read_status_score_sm100(clear, code);
+  if (st == PG_OK) st = read_status_dq_sm100(clear, code);
   return st;
 }
 
@@ -360,10 +361,13 @@ static WsPlan ws_plan(const pg_layout* L, pg_dtype dt, int Hq, int Hkv, int d, b
   }
   if (phase == 1) {
     const size_t Tp = (size_t)padded_tokens(L);
+    const bool sm100 = !(a.flags & PG_FLAG_SIMT) && bwd_sm100_supported(a);
     w.Dbuf = take(Tp * Hq * sizeof(float));
     w.lse2 = take(Tp * Hq * sizeof(float));
-    w.dq_acc = take(T * Hq * d * sizeof(float));
-    w.dk_acc = take(T * Hkv * d * sizeof(float));
+    // The query-major dQ kernel writes dq directly: no fp32 accumulator.
+    if (!(sm100 && (a.flags & PG_FLAG_DETERMINISTIC) && dq_sm100_supported(a)))
+      w.dq_acc = take(T * Hq * d * sizeof(float));
+    if (!sm100) w.dk_acc = take(T * Hkv * d * sizeof(float));
   }
   w.total = off;
   return w;
@@ -638,16 +642,21 @@ pg_status pg_grouped_attn_bwd(const pg_layout* layout, pg_dtype dtype, int32_t h
   }
   float* Dbuf = reinterpret_cast<float*>(ws + w.Dbuf);
   float* lse2 = reinterpret_cast<float*>(ws + w.lse2);
-  float* dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);
-  float* dk_acc = reinterpret_cast<float*>(ws + w.dk_acc);
+  float* dq_acc = w.dq_acc == SIZE_MAX ? nullptr : reinterpret_cast<float*>(ws + w.dq_acc);
+  float* dk_acc = w.dk_acc == SIZE_MAX ? nullptr : reinterpret_cast<float*>(ws + w.dk_acc);
   st = launch_bwd_preprocess(a, o, dO, lse, Dbuf, lse2, dq_acc);
   if (st != PG_OK) return st;
   if (!(a.flags & PG_FLAG_SIMT) && bwd_sm100_supported(a)) {
-    // dK (inverse-rotated, cast) and dV are written by the key-major kernel itself; dQ arrives
-    // in the fp32 accumulator and is rotated back and cast here.
+    // dK (inverse-rotated, cast) and dV are written by the key-major kernel itself.  dQ either
+    // comes from the query-major kernel (deterministic) or arrives in the fp32 accumulator and is
+    // rotated back and cast here.
     st = launch_bwd_sm100(a, qx, kx, v, dO, lse2, Dbuf, dq_acc, dk, dv, rope_tab);
     if (st != PG_OK) return st;
-    st = launch_rope(a, dq_acc, dq, heads_q, nullptr, nullptr, 0, true, true, nullptr, rope_tab);
+    if (dq_acc == nullptr)
+      st = launch_dq_sm100(a, qx, kx, v, dO, lse2, Dbuf, dq, rope_tab);
+    else
+      st = launch_rope(a, dq_acc, dq, heads_q, nullptr, nullptr, 0, true, true, nullptr,
+                       rope_tab);
   } else {
     st = launch_bwd_simt(a, qx, kx, v, o, lse, dO, Dbuf, dq_acc, dk_acc, dv);
     if (st != PG_OK) return st;

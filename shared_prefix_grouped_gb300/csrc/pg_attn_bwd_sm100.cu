@@ -32,8 +32,13 @@
 //
 // Warps: 0 TMA producer, 1 TMEM allocation and MMA issue, 2..9 softmax (key rows; two
 // warpgroups split the 64 query columns), 10..13 dQ drain.  Every mbarrier wait is bounded.
+//
+// Instantiated twice: with dQ as above, and without it (kDQ = false: no dQ^T product, no dS^T in
+// shared memory, no drain warps) for the deterministic backward, whose dQ comes from the
+// query-major kernel in pg_attn_dq_sm100.cu.
 #include <limits.h>
 #include <math.h>
+#include <string.h>
 
 #include "pg_internal.h"
 #include "pg_sm100.cuh"
@@ -52,7 +57,7 @@ constexpr int NSQ = 3;          // Q / dO stages
 constexpr int PREFETCH = 2;     // Q / dO blocks fetched into L2 this far ahead of their load
 constexpr uint32_t KHALF = BKV * 64 * 2;   // 16 KiB: [128 rows][64 cols] bf16
 constexpr uint32_t QHALF = BQ * 64 * 2;    // 8 KiB:  [64 rows][64 cols] bf16
-constexpr int NTHREADS = 448;
+constexpr int nthreads(bool with_dq) { return with_dq ? 448 : 320; }
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ int s_status_bwd = 0;
@@ -85,7 +90,8 @@ __device__ __forceinline__ void red_add(float* p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
-__global__ void __launch_bounds__(NTHREADS, 1)
+template <bool kDQ>
+__global__ void __launch_bounds__(nthreads(kDQ), 1)
 attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                       const __grid_constant__ CUtensorMap tl2, const __grid_constant__ CUtensorMap tds,
@@ -94,12 +100,13 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                       __nv_bfloat16* __restrict__ dv, const int4* __restrict__ tok,
                       const BwdTile* __restrict__ tiles, int Hq, int Hkv, int Ttot,
                       float scale_log2, float scale, const float2* __restrict__ rope_tab,
-                      uint64_t wait_ns) {
+                      int hc, uint64_t wait_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   BwdSmem& sm = *reinterpret_cast<BwdSmem*>(base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile_id = blockIdx.x / Hkv, kh = blockIdx.x % Hkv;
+  int tile_id, kh;
+  chunked_order(blockIdx.x, gridDim.x / Hkv, Hkv, hc, tile_id, kh);
   const BwdTile tl = tiles[tile_id];
   if (tl.k0 < 0 || tl.k1 > Ttot || tl.k0 >= tl.k1 || tl.k1 - tl.k0 > BKV || tl.q_lo < 0 ||
       tl.q_hi > Ttot || tl.q_lo >= tl.q_hi) {
@@ -242,12 +249,14 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
           for (int kk = 0; kk < BQ / 16; ++kk)
             mma_ts(t_dk, t_ds + kk * 8, desc_add(qmn, kk * 2048), id_g, kk == 0 ? acc0 : 1u);
           mma_commit(&sm.qd_empty[sp]);
-          if (jp >= 1 && !mbar_wait(&sm.dq_free, (jp - 1) & 1, wait_ns)) { ok = false; break; }
-          tc_fence_after();
+          if constexpr (kDQ) {
+            if (jp >= 1 && !mbar_wait(&sm.dq_free, (jp - 1) & 1, wait_ns)) { ok = false; break; }
+            tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < BKV / 16; ++kk)
-            mma_ss(t_dq, desc_add(kmn, kk * 2048), desc_add(dsmn, kk * 2048), id_q, kk != 0);
-          mma_commit(&sm.dq_full);
+            for (int kk = 0; kk < BKV / 16; ++kk)
+              mma_ss(t_dq, desc_add(kmn, kk * 2048), desc_add(dsmn, kk * 2048), id_q, kk != 0);
+            mma_commit(&sm.dq_full);
+          }
           mma_commit(&sm.pds_free);
         }
       }
@@ -329,14 +338,16 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       tc_fence_after();
       tmem_st16(t_p + half * 16 + lane_addr, pw);
       tmem_st16(t_ds + half * 16 + lane_addr, dw);
+      if constexpr (kDQ) {
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        const uint32_t off = sw128_offset(r, half * 4 + ch);
-        *reinterpret_cast<uint4*>(sm.ds + off) =
-            make_uint4(dw[4 * ch], dw[4 * ch + 1], dw[4 * ch + 2], dw[4 * ch + 3]);
+        for (int ch = 0; ch < 4; ++ch) {
+          const uint32_t off = sw128_offset(r, half * 4 + ch);
+          *reinterpret_cast<uint4*>(sm.ds + off) =
+              make_uint4(dw[4 * ch], dw[4 * ch + 1], dw[4 * ch + 2], dw[4 * ch + 3]);
+        }
       }
       tmem_st_wait();
-      fence_proxy_async_smem();
+      if constexpr (kDQ) fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&sm.p_full);
     }
@@ -407,7 +418,7 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       ok = false;
     }
     if (!ok) fail(PG_ERR_TIMEOUT);
-  } else {
+  } else if constexpr (kDQ) {
     // ------------------------------------------------------------------ dQ drain ---------
     const int quarter = warp & 3;                  // this warp's 32 head dims (= TMEM lanes)
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
@@ -474,20 +485,25 @@ pg_status launch_bwd_sm100(const AttnArgs& a, const void* q, const void* k, cons
   if (st == PG_OK) st = make_tmap_2d_b32(&tl2, lse2, true, Tp, a.Hq, Tp * 4, BQ, 1);
   if (st == PG_OK) st = make_tmap_2d_b32(&tds, Dbuf, true, Tp, a.Hq, Tp * 4, BQ, 1);
   if (st == PG_OK) st = make_tmap_2d_b32(&ttok, tokens(L), false, 4, T, 16, 4, BQ);
-  if (st == PG_OK)
+  // Without a dQ accumulator the kernel computes dK and dV only (dQ comes from the query-major
+  // kernel); its dQ tensor map is then never read.
+  const bool with_dq = dq_acc != nullptr;
+  memset(&tdq, 0, sizeof(tdq));
+  if (st == PG_OK && with_dq)
     st = make_tmap_2d_b32(&tdq, dq_acc, true, (uint64_t)a.Hq * D, T, (uint64_t)a.Hq * D * 4, 32,
                           BQ / 2);
   if (st != PG_OK) return st;
   const size_t smem = sizeof(BwdSmem) + 1024;
-  st = cuda_check(cudaFuncSetAttribute(attn_bwd_sm100_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+  auto kern = with_dq ? attn_bwd_sm100_kernel<true> : attn_bwd_sm100_kernel<false>;
+  st = cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem),
                   "bwd smem attribute");
   if (st != PG_OK) return st;
   prof_begin(PG_KERNEL_BWD_DKDV, a.stream);
-  attn_bwd_sm100_kernel<<<(unsigned)(L->n_tiles[BWD128] * a.Hkv), NTHREADS, smem, a.stream>>>(
+  kern<<<(unsigned)(L->n_tiles[BWD128] * a.Hkv), nthreads(with_dq), smem, a.stream>>>(
       tq, tk, tv, tdo, tl2, tds, ttok, tdq, static_cast<__nv_bfloat16*>(dk),
       static_cast<__nv_bfloat16*>(dv), tokens(L), tiles<BwdTile>(L, BWD128), a.Hq, a.Hkv, (int)T,
-      a.scale * kLog2e, a.scale, rope_tab, 2000000000ull);
+      a.scale * kLog2e, a.scale, rope_tab, order_chunk(a.Hkv, a.Hq / a.Hkv), 2000000000ull);
   prof_end(PG_KERNEL_BWD_DKDV, a.stream);
   return cuda_check(cudaGetLastError(), "bwd sm100 launch");
 }

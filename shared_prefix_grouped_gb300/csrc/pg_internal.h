@@ -49,6 +49,31 @@ inline const Tile* tiles(const pg_layout* L, int which) {
   return reinterpret_cast<const Tile*>(static_cast<const char*>(L->tables) + L->off_tiles[which]);
 }
 
+// CTA order of a grid of n_tiles x H work items (tile, head): heads in chunks of `hc` (the last
+// chunk may be smaller); within a chunk the tiles run heaviest first (the lists are sorted) with the
+// chunk's heads side by side.  A wave then touches the K/V or Q/dO rows of a few heads only, which
+// stay in L2 while every tile of those heads streams them, and the grid still ends on light tiles.
+__host__ __device__ inline void chunked_order(int x, int n_tiles, int H, int hc, int& tile,
+                                              int& head) {
+  const int full = H / hc;                      // complete chunks
+  const int per_chunk = hc * n_tiles;
+  if (x < full * per_chunk) {
+    const int c = x / per_chunk, r = x - c * per_chunk;
+    tile = r / hc;
+    head = c * hc + r % hc;
+  } else {
+    const int hl = H - full * hc, r = x - full * per_chunk;
+    tile = r / hl;
+    head = full * hc + r % hl;
+  }
+}
+
+// Heads per chunk for chunked_order: about eight query heads' worth of rows.
+inline int order_chunk(int heads, int q_heads_per_head) {
+  const int hc = 8 / (q_heads_per_head > 0 ? q_heads_per_head : 1);
+  return hc < 1 ? 1 : (hc > heads ? heads : hc);
+}
+
 // Arguments common to every attention kernel launch.
 struct AttnArgs {
   const pg_layout* layout;
@@ -86,10 +111,19 @@ bool fwd_sm100_supported(const AttnArgs& a);
 pg_status launch_fwd_sm100(const AttnArgs& a, const void* q, const void* k, const void* v, void* o,
                            float* lse);
 bool bwd_sm100_supported(const AttnArgs& a);
+// dq_acc == nullptr: dK and dV only.
 pg_status launch_bwd_sm100(const AttnArgs& a, const void* q, const void* k, const void* v,
                            const void* dO, const float* lse2, const float* Dbuf, float* dq_acc,
                            void* dk, void* dv, const float2* rope_tab);
 pg_status cuda_check(cudaError_t e, const char* what);
+
+// Query-major dQ (pg_attn_dq_sm100.cu): dq (bf16, inverse-rotated with rope_tab when given) from
+// the rotated q/k, v, dO and the preprocess's LSE_2 / Dsum rows.
+bool dq_sm100_supported(const AttnArgs& a);
+pg_status launch_dq_sm100(const AttnArgs& a, const void* q, const void* k, const void* v,
+                          const void* dO, const float* lse2, const float* Dbuf, void* dq,
+                          const float2* rope_tab);
+pg_status read_status_dq_sm100(bool clear, int32_t* code);
 
 // Responses-only forward (pg_attn_score_sm100.cu): its launch shape and partial-result buffers.
 struct ScorePlan {
@@ -126,6 +160,7 @@ pg_status launch_bwd_simt(const AttnArgs& a, const void* q, const void* k, const
 // and, with lse, set lse[h][row] = +inf on them.
 pg_status launch_pad_fill(const AttnArgs& a, void* x0, int heads0, void* x1, int heads1, void* x2,
                           int heads2, float* lse);
+// dq_acc may be nullptr (nothing to zero).
 pg_status launch_bwd_preprocess(const AttnArgs& a, const void* o, const void* dO, const float* lse,
                                 float* Dbuf, float* lse2, float* dq_acc);
 

@@ -313,7 +313,7 @@ __global__ void bwd_pre_kernel(const T* __restrict__ o, const T* __restrict__ dO
   for (int c = lane * 4; c < D; c += 128) {
     float4 a = Vec<T>::load4(o + base + c), b = Vec<T>::load4(dO + base + c);
     acc += dot4(a, b);
-    *reinterpret_cast<float4*>(dq_acc + base + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (dq_acc) *reinterpret_cast<float4*>(dq_acc + base + c) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);

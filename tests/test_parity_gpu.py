@@ -11,7 +11,7 @@ import pytest
 import torch
 
 from oracle import prefix_grouper_oracle as orc
-from shared_prefix_grouped_gb300 import api, workloads
+from shared_prefix_grouped_gb300 import _lib, api, workloads
 from shared_prefix_grouped_gb300.build import build
 
 pytestmark = pytest.mark.gpu
@@ -73,8 +73,11 @@ SMALL = [
 ]
 
 
+PATH_FLAGS = {"default": 0, "simt": _lib.PG_FLAG_SIMT, "det": _lib.PG_FLAG_DETERMINISTIC}
+
+
 @pytest.mark.parametrize("case", SMALL, ids=lambda c: f"w{c[0]}")
-@pytest.mark.parametrize("path", ["default", "simt"])
+@pytest.mark.parametrize("path", ["default", "simt", "det"])
 def test_small_cases(case, path):
     wi, plens, gsz, rs, hq, hkv = case
     w = workloads.WORKLOADS[wi]
@@ -82,8 +85,7 @@ def test_small_cases(case, path):
         w = workloads.small_variant(w, prefix_len=plens[0], suffix_lens=rs, heads_q=hq,
                                     heads_kv=hkv)
     prob = workloads.make_problem(w, prefix_lens=plens, group_sizes=gsz, suffix_lens=rs)
-    flags = 1 if path == "simt" else 0
-    got = run_gpu(prob, flags=flags)
+    got = run_gpu(prob, flags=PATH_FLAGS[path])
     compare(prob, got, TOL[w.dtype])
 
 
@@ -95,13 +97,14 @@ def test_small_cases(case, path):
     ([64], [2], [64, 64]),          # exact tile multiples
     ([3, 0, 70], [1, 2, 0], [0, 2, 1]),  # empty pieces everywhere
 ])
-def test_edge_cases(dtype, lens):
+@pytest.mark.parametrize("det", [False, True])
+def test_edge_cases(dtype, lens, det):
     plens, gsz, rs = lens
     base = workloads.WORKLOADS[0 if dtype == "f32" else 2]
     w = workloads.small_variant(base, prefix_len=plens[0], suffix_lens=rs, heads_q=4, heads_kv=2)
     w = workloads.dataclasses.replace(w, head_dim=128, rope_theta=100.0)
     prob = workloads.make_problem(w, prefix_lens=plens, group_sizes=gsz, suffix_lens=rs)
-    got = run_gpu(prob)
+    got = run_gpu(prob, flags=_lib.PG_FLAG_DETERMINISTIC if det else 0)
     compare(prob, got, TOL[dtype])
 
 
@@ -133,16 +136,31 @@ def test_prefix_gradient_is_deterministic():
     assert torch.equal(a["o"], b["o"]) and torch.equal(a["lse"], b["lse"])
 
 
+def test_deterministic_flag_makes_dq_bitwise_reproducible():
+    # With PG_FLAG_DETERMINISTIC every gradient, dq included, is bitwise identical run to run and
+    # dk / dv are those of the default path (the same key-major kernel computes them).
+    w = workloads.small_variant(workloads.WORKLOADS[2], prefix_len=1000,
+                                suffix_lens=[100, 300, 5, 260, 77], heads_q=8, heads_kv=2)
+    prob = workloads.make_problem(w)
+    det = _lib.PG_FLAG_DETERMINISTIC
+    a, b, c = run_gpu(prob, flags=det), run_gpu(prob, flags=det), run_gpu(prob)
+    for n in ["dq", "dk", "dv"]:
+        assert torch.equal(a[n], b[n]), n
+    assert torch.equal(a["dk"], c["dk"]) and torch.equal(a["dv"], c["dv"])
+    assert orc.normwise_error(a["dq"].double(), c["dq"].double()) < 1e-2
+
+
 # ---------------------------------------------------------------- full-size workloads ----------
 
-@pytest.mark.parametrize("wi,q_heads,groups", [
-    (1, [0, 31], None),             # bf16 MHA, P=4096, G=8, R=512: two of 32 heads
-    (2, [4, 5, 6, 7], [0, 5]),      # bf16 GQA, 8 groups: kv head 1, groups 0 and 5
+@pytest.mark.parametrize("wi,q_heads,groups,flags", [
+    (1, [0, 31], None, 0),          # bf16 MHA, P=4096, G=8, R=512: two of 32 heads
+    (2, [4, 5, 6, 7], [0, 5], 0),   # bf16 GQA, 8 groups: kv head 1, groups 0 and 5
+    (1, [7, 20], None, _lib.PG_FLAG_DETERMINISTIC),   # the deterministic backward at full size
 ])
-def test_full_size_sampled(wi, q_heads, groups):
+def test_full_size_sampled(wi, q_heads, groups, flags):
     w = workloads.WORKLOADS[wi]
     prob = workloads.make_problem(w)
-    got = run_gpu(prob)
+    got = run_gpu(prob, flags=flags)
     errs = compare(prob, got, TOL[w.dtype], q_heads=q_heads, groups=groups)
     print(w.name, errs)
 
