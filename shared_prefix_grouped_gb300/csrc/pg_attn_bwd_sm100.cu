@@ -57,7 +57,8 @@ constexpr int NSQ = 3;          // Q / dO stages
 constexpr int PREFETCH = 2;     // Q / dO blocks fetched into L2 this far ahead of their load
 constexpr uint32_t KHALF = BKV * 64 * 2;   // 16 KiB: [128 rows][64 cols] bf16
 constexpr uint32_t QHALF = BQ * 64 * 2;    // 8 KiB:  [64 rows][64 cols] bf16
-constexpr int nthreads(bool with_dq) { return with_dq ? 448 : 320; }
+// With dQ: warps 10..13 drain dQ.  Without: warp 10 is a second MMA-issuing thread (dV, dK).
+constexpr int nthreads(bool with_dq) { return with_dq ? 448 : 352; }
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ int s_status_bwd = 0;
@@ -74,7 +75,7 @@ struct BwdSmem {
   alignas(128) int4 tokq[NSQ][BQ];   // per-token {g0, pe, own_lo, pos} of the block's queries
   uint64_t kv_full;
   uint64_t qd_full[NSQ], qd_empty[NSQ];
-  uint64_t s_full, s_free, p_full, pds_free, dq_full, dq_free, mma_done;
+  uint64_t s_full, s_free, p_full, pds_free, dq_full, dq_free, mma_done, mma_done2;
   uint32_t tmem;
 };
 
@@ -133,6 +134,7 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     mbar_init(&sm.dq_full, 1);
     mbar_init(&sm.dq_free, 128);
     mbar_init(&sm.mma_done, 1);
+    mbar_init(&sm.mma_done2, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -214,7 +216,9 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       const uint64_t qmn0 = sdesc_sw128(smem_u32(sm.q[0]), QHALF, 1024);
       const uint64_t domn0 = sdesc_sw128(smem_u32(sm.dO[0]), QHALF, 1024);
       bool ok = mbar_wait(&sm.kv_full, 0, wait_ns);
-      for (int it = 0; ok && it <= n_it; ++it) {
+      // Without dQ the gradient products are issued by warp 10, so the score products of the
+      // next block never wait behind them in this thread.
+      for (int it = 0; ok && it <= (kDQ ? n_it : n_it - 1); ++it) {
         if (it < n_it) {
           const int st = it % NSQ;
           if (!mbar_wait(&sm.qd_full[st], (it / NSQ) & 1, wait_ns)) { ok = false; break; }
@@ -235,7 +239,7 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
           }
           mma_commit(&sm.s_full);
         }
-        if (it > 0) {
+        if (kDQ && it > 0) {
           const int jp = it - 1, sp = jp % NSQ;
           if (!mbar_wait(&sm.p_full, jp & 1, wait_ns)) { ok = false; break; }
           tc_fence_after();
@@ -418,7 +422,38 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       ok = false;
     }
     if (!ok) fail(PG_ERR_TIMEOUT);
-  } else if constexpr (kDQ) {
+  } else if (!kDQ) {
+    // ------------------------------------------------------------------ dV / dK MMAs -----
+    // Second issuing thread (no-dQ variant): dV += P^T dO and dK += dS^T Q of each block as soon
+    // as its P^T / dS^T are in TMEM.  Block j's S^T / dP^T products completed before its softmax
+    // could signal p_full, so the qd_empty commit below covers every reader of the stage.
+    if (warp == 10 && elect_one()) {
+      constexpr uint32_t id_g = idesc_bf16(BKV, D, 0, 1);
+      const uint64_t qmn0 = sdesc_sw128(smem_u32(sm.q[0]), QHALF, 1024);
+      const uint64_t domn0 = sdesc_sw128(smem_u32(sm.dO[0]), QHALF, 1024);
+      bool ok = true;
+      for (int jp = 0; jp < n_it; ++jp) {
+        const int sp = jp % NSQ;
+        if (!mbar_wait(&sm.p_full, jp & 1, wait_ns)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t qmn = desc_add(qmn0, sp * 2 * QHALF);
+        const uint64_t domn = desc_add(domn0, sp * 2 * QHALF);
+        const uint32_t acc0 = jp != 0;
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk)
+          mma_ts(t_dv, t_p + kk * 8, desc_add(domn, kk * 2048), id_g, kk == 0 ? acc0 : 1u);
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk)
+          mma_ts(t_dk, t_ds + kk * 8, desc_add(qmn, kk * 2048), id_g, kk == 0 ? acc0 : 1u);
+        mma_commit(&sm.qd_empty[sp]);
+        mma_commit(&sm.pds_free);
+      }
+      if (!ok) fail(PG_ERR_TIMEOUT);
+      mma_commit(&sm.mma_done2);
+      mbar_wait(&sm.mma_done2, 0, wait_ns);
+    }
+    __syncwarp();
+  } else {
     // ------------------------------------------------------------------ dQ drain ---------
     const int quarter = warp & 3;                  // this warp's 32 head dims (= TMEM lanes)
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;

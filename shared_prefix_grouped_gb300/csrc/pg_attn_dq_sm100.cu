@@ -17,11 +17,11 @@
 // call wrote) and writes dQ in bf16.  Every row's dQ is summed by one CTA over the keys in a fixed
 // order: no atomics, bitwise reproducible.
 //
-// Warps (320 threads): 0 TMA producer (Q and dO once, K and V tiles into a 2-stage ring), 1 TMEM
-// allocation and MMA issue (S and dP of tile j, then dQ of tile j - 1), 2..9 softmax and epilogue
-// (warp w reads TMEM lanes 32 (w % 4) .. + 31; warps 2..5 take key columns 0..63, warps 6..9
-// columns 64..127).  Every mbarrier wait is bounded (PG_ERR_TIMEOUT in the status word, then an
-// orderly exit).
+// Warps (352 threads): 0 TMA producer (Q and dO once, K and V tiles into a 2-stage ring), 1 TMEM
+// allocation and the S / dP MMAs, 10 the dQ MMAs (a second issuing thread, so dQ of tile j never
+// waits behind the next tile's loads or score products), 2..9 softmax and epilogue (warp w reads
+// TMEM lanes 32 (w % 4) .. + 31; warps 2..5 take key columns 0..63, warps 6..9 columns 64..127).
+// Every mbarrier wait is bounded (PG_ERR_TIMEOUT in the status word, then an orderly exit).
 #include <math.h>
 
 #include "pg_internal.h"
@@ -40,7 +40,7 @@ constexpr int BN = 128;                   // keys per tile
 constexpr int NS = 2;                     // K/V stages
 constexpr uint32_t QH = BM * 64 * 2;      // [128 rows][64 dims] bf16: 16 KiB
 constexpr uint32_t KH = BN * 64 * 2;      // [128 keys][64 dims] bf16: 16 KiB
-constexpr int NTHREADS = 320;
+constexpr int NTHREADS = 352;
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ int s_status_dq = 0;
@@ -52,7 +52,7 @@ struct DqSmem {
   uint8_t v[NS][2 * KH];
   uint64_t q_full;
   uint64_t kv_full[NS], kv_empty[NS];
-  uint64_t s_full, s_free, p_full, ds_free[2], dq_done, mma_done;
+  uint64_t s_full, s_free, p_full[2], ds_free[2], dq_done, mma_done, mma_done2;
   uint32_t tmem;
 };
 
@@ -118,11 +118,13 @@ attn_dq_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     }
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.s_free, 256);
-    mbar_init(&sm.p_full, 256);
+    mbar_init(&sm.p_full[0], 256);
+    mbar_init(&sm.p_full[1], 256);
     mbar_init(&sm.ds_free[0], 1);
     mbar_init(&sm.ds_free[1], 1);
     mbar_init(&sm.dq_done, 1);
     mbar_init(&sm.mma_done, 1);
+    mbar_init(&sm.mma_done2, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -171,59 +173,70 @@ attn_dq_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issue --------
+    // ------------------------------------------------------------------ S / dP MMAs ------
     if (elect_one()) {
-      constexpr uint32_t id_s = idesc_bf16(BM, BN, 0, 0);   // S, dP
-      constexpr uint32_t id_q = idesc_bf16(BM, D, 0, 1);    // dQ (K as MN-major B)
+      constexpr uint32_t id_s = idesc_bf16(BM, BN, 0, 0);
       const uint64_t qd = sdesc_sw128(smem_u32(sm.q), 16, 1024);
       const uint64_t dod = sdesc_sw128(smem_u32(sm.dO), 16, 1024);
       const uint64_t kd0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
       const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0]), 16, 1024);
-      const uint64_t kmn0 = sdesc_sw128(smem_u32(sm.k[0]), KH, 1024);
       bool ok = mbar_wait(&sm.q_full, 0, wait_ns);
-      for (int j = 0; ok && j <= n; ++j) {
-        if (j < n) {
-          const int s = j % NS;
-          if (!mbar_wait(&sm.kv_full[s], (j / NS) & 1, wait_ns)) { ok = false; break; }
-          // S and dP are single-buffered: the softmax warps must have read tile j - 1's.
-          if (j > 0 && !mbar_wait(&sm.s_free, (j - 1) & 1, wait_ns)) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t kd = desc_add(kd0, s * 2 * KH), vd = desc_add(vd0, s * 2 * KH);
+      for (int j = 0; ok && j < n; ++j) {
+        const int s = j % NS;
+        if (!mbar_wait(&sm.kv_full[s], (j / NS) & 1, wait_ns)) { ok = false; break; }
+        // S and dP are single-buffered: the softmax warps must have read tile j - 1's.
+        if (j > 0 && !mbar_wait(&sm.s_free, (j - 1) & 1, wait_ns)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t kd = desc_add(kd0, s * 2 * KH), vd = desc_add(vd0, s * 2 * KH);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t qo = (kk >> 2) * QH + (kk & 3) * 32;
-            const uint32_t ko = (kk >> 2) * KH + (kk & 3) * 32;
-            mma_ss(t_s, desc_add(qd, qo), desc_add(kd, ko), id_s, kk != 0);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t qo = (kk >> 2) * QH + (kk & 3) * 32;
-            const uint32_t ko = (kk >> 2) * KH + (kk & 3) * 32;
-            mma_ss(t_dp, desc_add(dod, qo), desc_add(vd, ko), id_s, kk != 0);
-          }
-          mma_commit(&sm.s_full);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t qo = (kk >> 2) * QH + (kk & 3) * 32;
+          const uint32_t ko = (kk >> 2) * KH + (kk & 3) * 32;
+          mma_ss(t_s, desc_add(qd, qo), desc_add(kd, ko), id_s, kk != 0);
         }
-        if (j > 0) {
-          const int jp = j - 1, b = jp & 1, sp = jp % NS;
-          if (!mbar_wait(&sm.p_full, jp & 1, wait_ns)) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t kmn = desc_add(kmn0, sp * 2 * KH);
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(t_dq, t_ds + 64 * b + kk * 8, desc_add(kmn, kk * 2048), id_q,
-                   (jp > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&sm.ds_free[b]);
-          mma_commit(&sm.kv_empty[sp]);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t qo = (kk >> 2) * QH + (kk & 3) * 32;
+          const uint32_t ko = (kk >> 2) * KH + (kk & 3) * 32;
+          mma_ss(t_dp, desc_add(dod, qo), desc_add(vd, ko), id_s, kk != 0);
         }
+        mma_commit(&sm.s_full);
       }
       if (!ok) fail(PG_ERR_TIMEOUT);
-      mma_commit(&sm.dq_done);
       mma_commit(&sm.mma_done);
       mbar_wait(&sm.mma_done, 0, wait_ns);
     }
     __syncwarp();
+  } else if (warp == 10) {
+    // ------------------------------------------------------------------ dQ MMAs ----------
+    // dQ += dS K of tile j once its dS is in TMEM.  Tile j's S / dP products completed before its
+    // softmax could signal p_full, so the kv_empty commit covers every reader of the stage.
+    if (elect_one()) {
+      constexpr uint32_t id_q = idesc_bf16(BM, D, 0, 1);    // K as the MN-major B operand
+      const uint64_t kmn0 = sdesc_sw128(smem_u32(sm.k[0]), KH, 1024);
+      bool ok = true;
+      for (int j = 0; j < n; ++j) {
+        const int b = j & 1, s = j % NS;
+        // One p_full per dS buffer: tile j + 2 reuses buffer b only after this product read it.
+        if (!mbar_wait(&sm.p_full[b], (j >> 1) & 1, wait_ns)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t kmn = desc_add(kmn0, s * 2 * KH);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(t_dq, t_ds + 64 * b + kk * 8, desc_add(kmn, kk * 2048), id_q,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&sm.ds_free[b]);
+        mma_commit(&sm.kv_empty[s]);
+      }
+      if (!ok) fail(PG_ERR_TIMEOUT);
+      mma_commit(&sm.dq_done);
+      mma_commit(&sm.mma_done2);
+      mbar_wait(&sm.mma_done2, 0, wait_ns);
+    }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------------ softmax + epilogue -
+    // (warps 2..9)
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;            // key columns [64 half, 64 half + 64)
     const int r = quarter * 32 + lane;
@@ -276,7 +289,7 @@ attn_dq_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
       tmem_st32(t_ds + 64 * b + 32 * half + lane_addr, dw);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&sm.p_full);
+      mbar_arrive(&sm.p_full[b]);
     }
     // Epilogue: dQ * scale, rotated back by the row's RoPE angle, in bf16.  This thread owns the
     // pairs (k, k + 64) for k in [32 half, 32 half + 32).
