@@ -264,10 +264,11 @@ def run_reference(args):
 class Step:
     """Buffers and calls of one fwd+bwd step through the C ABI."""
 
-    def __init__(self, prob, device, flags=0):
+    def __init__(self, prob, device, flags=0, layout=None):
         w = prob.workload
         self.w, self.flags, self.device = w, flags, device
-        self.layout = api.pack(prob.prefix_lens, prob.group_sizes, prob.suffix_lens, device)
+        self.layout = layout if layout is not None else api.pack(
+            prob.prefix_lens, prob.group_sizes, prob.suffix_lens, device)
         self.q, self.k, self.v, self.do = (t.to(device) for t in (prob.q, prob.k, prob.v, prob.do))
         self.o = torch.empty_like(self.q)
         self.lse = torch.empty((w.heads_q, prob.total_tokens), dtype=torch.float32, device=device)
@@ -544,6 +545,87 @@ def run_score_bench(args):
         print(json.dumps(line))
 
 
+def run_tree_bench(args):
+    """Nested prefixes (a shared context, user turns below it, responses below each turn):
+    forward + backward through a pg_pack_tree layout."""
+    world, rank, local = dist_setup()
+    device = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(device)
+    w = workloads.tree_by_name(args.workload)
+    prob = workloads.make_tree_problem(w, seed=w.seed + rank)
+    flags = (_lib.PG_FLAG_SIMT if args.simt else 0) | \
+        (_lib.PG_FLAG_DETERMINISTIC if args.deterministic else 0)
+    step = Step(prob, device, flags, layout=api.pack_tree(w.parent, w.lens, device))
+    pairs = step.layout.pairs
+    step_flops = flops.attn_flops(pairs, w.heads_q, w.head_dim, "fwdbwd")
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(device)
+    L = _lib.lib()
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    ev = [(mk(), mk()) for _ in range(args.steps)]
+    kev = [(mk(), mk()) for _ in range(args.steps)]
+    for a, b in kev:
+        a.record()
+        b.record()
+    prof = _lib.PgProfile(_lib.PG_KERNEL_BWD_DKDV, 0, None, None, 0)
+    sampler = ClockSampler(device.index)
+    sampler.start()
+    barrier(world, device)
+    L.pg_set_profile(prof)
+    for i in range(args.steps):
+        flush.zero_()
+        prof.ev_begin, prof.ev_end = kev[i][0].cuda_event, kev[i][1].cuda_event
+        ev[i][0].record()
+        step()
+        ev[i][1].record()
+    L.pg_set_profile(None)
+    barrier(world, device)
+    clocks = sampler.stop()
+    assert api.device_status() == 0, "a kernel reported an error"
+    sec = sum(a.elapsed_time(b) for a, b in ev) / 1e3 / args.steps
+    sec = max_over_ranks(sec, world, device)
+    ksec = sum(a.elapsed_time(b) for a, b in kev) / 1e3 / args.steps
+    peaks, peak_src = load_peaks()
+    peak = peaks["bf16_tflops"]
+    # repeated-prefix equivalent: every root-to-leaf path as its own sequence
+    tl_paths, parent, lens = [], list(w.parent), list(w.lens)
+    children = [[] for _ in parent]
+    for i, p_ in enumerate(parent):
+        if p_ >= 0:
+            children[p_].append(i)
+    rep_pairs = 0
+    for i in range(len(parent)):
+        if not children[i]:
+            n, a = 0, i
+            while a >= 0:
+                n += lens[a]
+                a = parent[a]
+            rep_pairs += n * (n + 1) // 2
+    line = {"metric": METRIC, "value": step_flops * world / sec / 1e12, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic (seeded N(0,1) Q/K/V/dO; no dataset)",
+            "config": {"workload": w.name, "segments": len(parent), "max_depth":
+                       int(step.layout.struct.max_depth), "total_tokens": prob.total_tokens,
+                       "heads_q": w.heads_q, "heads_kv": w.heads_kv, "head_dim": w.head_dim,
+                       "rope_theta": w.rope_theta, "deterministic_backward": bool(args.deterministic),
+                       "l2": "L2 flushed before every step (outside the events)"},
+            "tokens_per_s": prob.total_tokens * world / sec,
+            "pct_bf16_peak": 100.0 * step_flops / sec / 1e12 / peak, "peak_source": peak_src,
+            "pair_ratio_grouped_over_paths": pairs / rep_pairs,
+            "roofline": {"bound": "tensor", "kernel": "bwd key-major",
+                         "achieved": flops.attn_flops(pairs, w.heads_q, w.head_dim, "bwd") / ksec / 1e12,
+                         "peak": peak, "unit": "TFLOP/s", "traffic": None,
+                         "peak_source": f"bf16 dense burst, {peak_src}"},
+            "clocks": clocks, "gpu_launches": int(prof.launches)}
+    line["roofline"]["frac"] = line["roofline"]["achieved"] / peak
+    if rank == 0:
+        print(json.dumps(line))
+
+
 def run_layer_bench(args):
     """The decoder-layer workload: forward + backward of one layer over the packed groups."""
     from shared_prefix_grouped_gb300 import layer
@@ -604,7 +686,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=[w.name for w in workloads.WORKLOADS] + [workloads.LayerWorkload().name])
+                    choices=[w.name for w in workloads.WORKLOADS] + [workloads.LayerWorkload().name]
+                    + [w.name for w in workloads.TREE_WORKLOADS])
     ap.add_argument("--simt", action="store_true", help="force the fp32 SIMT kernels")
     ap.add_argument("--deterministic", action="store_true",
                     help="bitwise-reproducible backward (query-major dQ kernel)")
@@ -617,6 +700,8 @@ def main():
         run_reference(args)
     elif args.workload == workloads.LayerWorkload().name:
         run_layer_bench(args)
+    elif args.workload in [w.name for w in workloads.TREE_WORKLOADS]:
+        run_tree_bench(args)
     elif workloads.by_name(args.workload).responses_only:
         run_score_bench(args)
     else:

@@ -113,6 +113,10 @@ typedef struct pg_layout {
   int64_t max_response_rows; /* the largest number of response rows (sum of R_bi) in one group */
   int64_t n_pad_rows;      /* padded layouts (pg_pack_padded): number of padding rows, else 0 */
   int64_t off_pad_rows;    /* byte offset of the padding rows' indices (int32) in the tables */
+  int64_t max_depth;       /* segments on the longest root-to-leaf path: 1 (prefixes only) or 2
+                              for pg_pack layouts, up to 8 for pg_pack_tree layouts */
+  int64_t n_intervals;     /* entries (2 x int32 key ranges) of the tiles' interval table */
+  int64_t off_intervals;   /* its byte offset in the tables */
 } pg_layout;
 
 /*
@@ -148,6 +152,29 @@ pg_status pg_pack_host(int32_t num_groups, const int32_t* prefix_lens, const int
 pg_status pg_pack(int32_t num_groups, const int32_t* prefix_lens, const int32_t* group_sizes,
                   const int32_t* suffix_lens, int32_t* position_ids_dev, void* tables_dev,
                   int64_t table_bytes, pg_layout* layout, pg_stream_t stream);
+
+/*
+ * Nested prefixes (Pith review, "Reading between the lines": multi-turn histories shared by many
+ * continuations).  num_nodes segments with seg_lens[i] tokens each; parent[i] is the index of
+ * segment i's parent (-1 for a root), and the segments are listed in depth-first preorder (a parent
+ * before its children, a subtree contiguous), which is also their packed row order.  A token sees
+ * every token of its segment's ancestors and the tokens of its own segment up to itself; its
+ * position id is the total length of its ancestors plus its offset in its segment -- its position
+ * in the root-to-leaf sequence the repeated-prefix baseline would run.  Each root is a group; a root
+ * whose children are all leaves is exactly a pg_pack group.  The attention calls then compute that
+ * attention, and in the backward every segment's gradient sums over all continuations below it.
+ * Buffers and errors as pg_pack_size / pg_pack_host / pg_pack; PG_ERR_INVALID_ARG for a negative
+ * length or an order that is not a depth-first preorder, PG_ERR_UNSUPPORTED for a nesting depth
+ * (segments on a root-to-leaf path) above 8.  PG_FLAG_RESPONSES_ONLY needs depth <= 2.
+ */
+pg_status pg_pack_tree_size(int32_t num_nodes, const int32_t* parent, const int32_t* seg_lens,
+                            int64_t* total_tokens, int64_t* table_bytes);
+pg_status pg_pack_tree_host(int32_t num_nodes, const int32_t* parent, const int32_t* seg_lens,
+                            int32_t* position_ids, void* tables, int64_t table_bytes,
+                            pg_layout* layout);
+pg_status pg_pack_tree(int32_t num_nodes, const int32_t* parent, const int32_t* seg_lens,
+                       int32_t* position_ids_dev, void* tables_dev, int64_t table_bytes,
+                       pg_layout* layout, pg_stream_t stream);
 
 /*
  * Padded layout (skill page "prefix-grouper-grpo", Step 3 "Restructure Input Format"): each of the

@@ -446,6 +446,172 @@ def packed_dense(layout: PackedLayout, q, k, v, do=None, *, theta: float = 0.0,
 
 
 # ------------------------------------------------------------------------------------------------
+# Nested prefixes (trees): one history replayed against many continuations
+# ------------------------------------------------------------------------------------------------
+#
+# The Pith review ("Reading between the lines") names multi-turn, tree-shaped sharing: one history
+# reused by many continuations.  The baseline generalises directly: every root-to-leaf path of
+# segments is one sequence of its own (positions 0 .. its length - 1) run through causal attention.
+# Packed, the segments follow each other in depth-first preorder; a node's tokens come from the
+# first path through it (all paths give the same values by causality), the upstream gradient at a
+# token is routed into that first path, and every gradient is summed over all paths.
+
+@dataclasses.dataclass
+class TreeLayout:
+    parent: List[int]
+    lens: List[int]
+    start: List[int]
+    end: List[int]
+    children: List[List[int]]
+    position_ids: torch.Tensor       # int64 [T]: position in the token's root-to-leaf sequence
+    token_node: torch.Tensor         # int64 [T]
+
+    @property
+    def total_tokens(self) -> int:
+        return int(self.end[-1]) if self.end else 0
+
+
+def tree_layout(parent: Sequence[int], lens: Sequence[int]) -> TreeLayout:
+    """Rows of the nodes in the listed order, which must be a depth-first preorder."""
+    n = len(parent)
+    assert len(lens) == n and all(x >= 0 for x in lens)
+    children = [[] for _ in range(n)]
+    start, end, off, stack, row = [], [], [], [], 0
+    for i in range(n):
+        p = parent[i]
+        assert -1 <= p < i
+        while stack and stack[-1] != p:
+            stack.pop()
+        assert p < 0 or stack, "not a depth-first preorder"
+        if p >= 0:
+            children[p].append(i)
+        off.append(off[p] + lens[p] if p >= 0 else 0)
+        start.append(row)
+        row += lens[i]
+        end.append(row)
+        stack.append(i)
+    pos, node = [], []
+    for i in range(n):
+        pos += [off[i] + j for j in range(lens[i])]
+        node += [i] * lens[i]
+    i64 = lambda xs: torch.tensor(xs, dtype=torch.int64)
+    return TreeLayout(list(parent), list(lens), start, end, children, i64(pos), i64(node))
+
+
+def tree_paths(tl: TreeLayout) -> List[List[int]]:
+    """Root-to-leaf node paths, leaves in listed order."""
+    paths = []
+    for i in range(len(tl.parent)):
+        if not tl.children[i]:
+            path, a = [], i
+            while a >= 0:
+                path.append(a)
+                a = tl.parent[a]
+            paths.append(path[::-1])
+    return paths
+
+
+def tree_visibility(tl: TreeLayout) -> torch.Tensor:
+    """bool [T, T]: row t sees key s iff s's node is an ancestor of t's node, or the same node and
+    s <= t."""
+    T = tl.total_tokens
+    n = len(tl.parent)
+    anc = torch.zeros((n, n), dtype=torch.bool)      # anc[a, b]: a is b or an ancestor of b
+    for b in range(n):
+        a = b
+        while a >= 0:
+            anc[a, b] = True
+            a = tl.parent[a]
+    nt, ns = tl.token_node[:, None], tl.token_node[None, :]
+    t = torch.arange(T)[:, None]
+    s = torch.arange(T)[None, :]
+    same = nt == ns
+    return (anc[ns, nt] & ~same) | (same & (s <= t))
+
+
+def tree_repeated(tl: TreeLayout, q, k, v, do=None, *, theta: float = 0.0,
+                  scale: Optional[float] = None) -> AttnResult:
+    """Grouped attention over nested prefixes computed path by path (the baseline)."""
+    q, k, v = q.to(F64), k.to(F64), v.to(F64)
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    scale = d ** -0.5 if scale is None else scale
+    nan = float("nan")
+    O = torch.full((T, Hq, d), nan, dtype=F64)
+    LSE = torch.full((Hq, T), nan, dtype=F64)
+    bwd = do is not None
+    if bwd:
+        do = do.to(F64)
+        dQ = torch.zeros((T, Hq, d), dtype=F64)
+        dK = torch.zeros((T, Hkv, d), dtype=F64)
+        dV = torch.zeros((T, Hkv, d), dtype=F64)
+    done = torch.zeros(T, dtype=torch.bool)          # rows already taken from an earlier path
+    for path in tree_paths(tl):
+        rows = torch.cat([torch.arange(tl.start[a], tl.end[a]) for a in path])
+        m = rows.numel()
+        if m == 0:
+            continue
+        pos = torch.arange(m)
+        first = ~done[rows]                          # this path is the first one through these rows
+        qi, ki, vi = rope_rotate(q[rows], pos, theta), rope_rotate(k[rows], pos, theta), v[rows]
+        mfn = causal_mask_fn(m)
+        dki = torch.zeros((m, Hkv, d), dtype=F64)
+        dvi = torch.zeros((m, Hkv, d), dtype=F64)
+        for h in range(Hq):
+            kh = _kv_head(h, Hq, Hkv)
+            o, lse = masked_attention_fwd(qi[:, h], ki[:, kh], vi[:, kh], mfn, scale)
+            O[rows[first], h] = o[first]
+            LSE[h, rows[first]] = lse[first]
+            if bwd:
+                doi = do[rows, h] * first[:, None].to(F64)      # dO routed to the first path
+                a_, b_, c_ = masked_attention_bwd(qi[:, h], ki[:, kh], vi[:, kh], o, lse, doi, mfn,
+                                                  scale)
+                dQ[rows, h] += rope_rotate_vjp(a_[:, None, :], pos, theta)[:, 0]
+                dki[:, kh] += b_
+                dvi[:, kh] += c_
+        if bwd:
+            dK[rows] += rope_rotate_vjp(dki, pos, theta)
+            dV[rows] += dvi
+        done[rows] = True
+    if bwd:
+        return AttnResult(O, LSE, dQ, dK, dV)
+    return AttnResult(O, LSE)
+
+
+def tree_packed_dense(tl: TreeLayout, q, k, v, do=None, *, theta: float = 0.0,
+                      scale: Optional[float] = None) -> AttnResult:
+    """Second formulation: one attention over the packed rows with the tree's dense mask."""
+    q, k, v = q.to(F64), k.to(F64), v.to(F64)
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    scale = d ** -0.5 if scale is None else scale
+    mask = tree_visibility(tl)
+    mfn = lambda r0, r1: mask[r0:r1]
+    pos = tl.position_ids
+    qr, kr = rope_rotate(q, pos, theta), rope_rotate(k, pos, theta)
+    O = torch.empty((T, Hq, d), dtype=F64)
+    LSE = torch.empty((Hq, T), dtype=F64)
+    if do is not None:
+        do = do.to(F64)
+        dQr = torch.empty((T, Hq, d), dtype=F64)
+        dKr = torch.zeros((T, Hkv, d), dtype=F64)
+        dV = torch.zeros((T, Hkv, d), dtype=F64)
+    for h in range(Hq):
+        kh = _kv_head(h, Hq, Hkv)
+        o, lse = masked_attention_fwd(qr[:, h], kr[:, kh], v[:, kh], mfn, scale)
+        O[:, h], LSE[h] = o, lse
+        if do is not None:
+            a_, b_, c_ = masked_attention_bwd(qr[:, h], kr[:, kh], v[:, kh], o, lse, do[:, h], mfn,
+                                              scale)
+            dQr[:, h] = a_
+            dKr[:, kh] += b_
+            dV[:, kh] += c_
+    if do is None:
+        return AttnResult(O, LSE)
+    return AttnResult(O, LSE, rope_rotate_vjp(dQr, pos, theta), rope_rotate_vjp(dKr, pos, theta), dV)
+
+
+# ------------------------------------------------------------------------------------------------
 # Comparison helper used by the tests
 # ------------------------------------------------------------------------------------------------
 

@@ -30,6 +30,9 @@ class PgLayout(C.Structure):
         ("max_response_rows", C.c_int64),
         ("n_pad_rows", C.c_int64),
         ("off_pad_rows", C.c_int64),
+        ("max_depth", C.c_int64),
+        ("n_intervals", C.c_int64),
+        ("off_intervals", C.c_int64),
     ]
 
 
@@ -67,6 +70,11 @@ SIGNATURES = {
                                C.POINTER(PgLayout)]),
     "pg_pack": (C.c_int, [C.c_int32, I32P, I32P, I32P, VP, VP, C.c_int64, C.POINTER(PgLayout),
                           VP]),
+    "pg_pack_tree_size": (C.c_int, [C.c_int32, I32P, I32P, I64P, I64P]),
+    "pg_pack_tree_host": (C.c_int, [C.c_int32, I32P, I32P, I32P, VP, C.c_int64,
+                                    C.POINTER(PgLayout)]),
+    "pg_pack_tree": (C.c_int, [C.c_int32, I32P, I32P, VP, VP, C.c_int64, C.POINTER(PgLayout),
+                               VP]),
     "pg_pack_padded_size": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, I32P, I64P,
                                       I64P]),
     "pg_pack_padded_host": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, I32P, I32P, VP,

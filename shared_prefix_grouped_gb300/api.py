@@ -78,6 +78,41 @@ def pack(prefix_lens: Sequence[int], group_sizes: Sequence[int], suffix_lens: Se
     return Layout(prefix_lens, group_sizes, suffix_lens, st, pos, tab)
 
 
+def pack_tree_size(parent: Sequence[int], seg_lens: Sequence[int]):
+    T, nb = C.c_int64(), C.c_int64()
+    check("pg_pack_tree_size", _lib.lib().pg_pack_tree_size(
+        len(parent), int_array(parent), int_array(seg_lens), C.byref(T), C.byref(nb)))
+    return T.value, nb.value
+
+
+def pack_tree_host(parent: Sequence[int], seg_lens: Sequence[int]):
+    """Host-only packing of nested prefixes: (position_ids, tables, struct), as pack_host."""
+    T, nb = pack_tree_size(parent, seg_lens)
+    pos = torch.empty(T, dtype=torch.int32)
+    tab = torch.empty(nb, dtype=torch.uint8)
+    st = PgLayout()
+    check("pg_pack_tree_host", _lib.lib().pg_pack_tree_host(
+        len(parent), int_array(parent), int_array(seg_lens), C.cast(pos.data_ptr(), _lib.I32P),
+        C.c_void_p(tab.data_ptr()), nb, C.byref(st)))
+    return pos, tab, st
+
+
+def pack_tree(parent: Sequence[int], seg_lens: Sequence[int], device="cuda") -> Layout:
+    """Layout of nested prefixes: segments in depth-first preorder, parent[i] = -1 for a root."""
+    device = torch.device(device)
+    T, nb = pack_tree_size(parent, seg_lens)
+    pos = torch.empty(T, dtype=torch.int32, device=device)
+    tab = torch.empty(nb, dtype=torch.uint8, device=device)
+    st = PgLayout()
+    with torch.cuda.device(device):
+        check("pg_pack_tree", _lib.lib().pg_pack_tree(
+            len(parent), int_array(parent), int_array(seg_lens), C.c_void_p(pos.data_ptr()),
+            C.c_void_p(tab.data_ptr()), nb, C.byref(st), _stream_ptr(device)))
+    lay = Layout([], [], [], st, pos, tab)
+    lay.tree = (list(parent), list(seg_lens))
+    return lay
+
+
 def _padded_args(num_groups, prefix_len, group_size, max_response_len, response_lens):
     assert len(response_lens) == num_groups * group_size
     return (int(num_groups), int(prefix_len), int(group_size), int(max_response_len),

@@ -52,6 +52,8 @@ struct Plan {
   int64_t off_tokens = 0, bytes = 0;
   int64_t max_resp = 0;   // largest number of response rows in one group
   int64_t n_pad = 0, off_pad = 0;   // padded layouts: padding-row list
+  int64_t max_depth = 0;            // segments on the longest root-to-leaf path
+  int64_t n_iv = 0, off_iv = 0;     // interval table of the tiles' further causal ranges
 };
 
 static pg_status check_lengths(int32_t B, const int32_t* lp, const int32_t* gs, const int32_t* rs,
@@ -107,6 +109,7 @@ static pg_status check_lengths(int32_t B, const int32_t* lp, const int32_t* gs, 
     n256 += (len + 255) / 256;
     nspan += resp > 0;
     p->max_resp = std::max(p->max_resp, resp);
+    p->max_depth = std::max<int64_t>(p->max_depth, (gs[b] > 0 && lp[b] > 0) ? 2 : 1);
   }
   p->n[FWD64] = p->n[BWD64] = n64;
   p->n[FWD128] = p->n[BWD128] = n128;
@@ -119,6 +122,7 @@ static pg_status check_lengths(int32_t B, const int32_t* lp, const int32_t* gs, 
     p->off[w] = off;
     off = align_up(off + 32 * p->n[w], 256);
   }
+  p->off_iv = off;    // two-level tiles need no further ranges: empty table
   p->bytes = off;
   return PG_OK;
 }
@@ -175,7 +179,6 @@ static void build_tables(int32_t B, const int32_t* lp, const int32_t* gs, const 
         t.q0 = q0;
         t.q1 = q1;
         t.g0 = g0;
-        t.pe = pe;
         t.p_end = std::min(pe, q1);
         if (q1 > pe) {
           t.s_lo = tok[std::max(q0, pe)].z;
@@ -223,7 +226,6 @@ static void build_tables(int32_t B, const int32_t* lp, const int32_t* gs, const 
       t.p_end = pe;
       t.s_lo = pe;
       t.s_hi = gend;
-      t.pe = pe;
       spans.push_back(t);
     }
     g0 = gend;
@@ -299,6 +301,251 @@ static void fill_layout(int32_t B, const Plan& p, const int32_t* pos, const void
   L->max_response_rows = p.max_resp;
   L->n_pad_rows = p.n_pad;
   L->off_pad_rows = p.off_pad;
+  L->max_depth = p.max_depth;
+  L->n_intervals = p.n_iv;
+  L->off_intervals = p.off_iv;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Nested prefixes (trees).  Segments are listed in depth-first preorder, parent before child; the
+// packed rows follow that order, so every node's subtree is one contiguous row range.  A token sees
+// all tokens of its node's ancestors and its own node's tokens up to itself; its position is the
+// total length of its ancestors plus its offset in its node (its position in the root-to-leaf
+// sequence the repeated-prefix baseline would run).
+// ---------------------------------------------------------------------------------------------
+
+struct Tree {
+  std::vector<int32_t> parent, len, start, end, sub_end, off, depth, root_start, root_end;
+  std::vector<char> leaf;
+  // Work units: a single node, or a run of consecutive sibling leaves.
+  struct Unit {
+    int32_t r0, r1;        // rows
+    int32_t node;          // the node (single-node unit) or the leaves' parent
+    bool run;
+  };
+  std::vector<Unit> units;
+};
+
+static pg_status plan_tree(int32_t N, const int32_t* parent, const int32_t* len, Tree* tr,
+                           Plan* p) {
+  if (N < 1 || !parent || !len) {
+    set_error("pg_pack_tree: num_nodes must be >= 1 and arrays non-NULL");
+    return PG_ERR_INVALID_ARG;
+  }
+  tr->parent.assign(parent, parent + N);
+  tr->len.assign(len, len + N);
+  tr->start.resize(N);
+  tr->end.resize(N);
+  tr->sub_end.resize(N);
+  tr->off.resize(N);
+  tr->depth.resize(N);
+  tr->root_start.resize(N);
+  tr->root_end.resize(N);
+  tr->leaf.assign(N, 1);
+  std::vector<int32_t> stack;
+  int64_t row = 0, pairs = 0, maxpos = 0, maxdepth = 0;
+  for (int32_t i = 0; i < N; ++i) {
+    const int32_t par = parent[i];
+    if (len[i] < 0 || par < -1 || par >= i) {
+      set_error("pg_pack_tree: node %d has a negative length or a parent not listed before it", i);
+      return PG_ERR_INVALID_ARG;
+    }
+    // Depth-first preorder: the parent must be on the current root-to-node path.
+    while (!stack.empty() && stack.back() != par) {
+      tr->sub_end[stack.back()] = (int32_t)row;
+      stack.pop_back();
+    }
+    if (par >= 0 && stack.empty()) {
+      set_error("pg_pack_tree: node %d does not follow its parent's subtree in depth-first order",
+                i);
+      return PG_ERR_INVALID_ARG;
+    }
+    tr->start[i] = (int32_t)row;
+    row += len[i];
+    tr->end[i] = (int32_t)row;
+    if (par >= 0) {
+      tr->leaf[par] = 0;
+      tr->off[i] = tr->off[par] + len[par];
+      tr->depth[i] = tr->depth[par] + 1;
+      tr->root_start[i] = tr->root_start[par];
+      tr->root_end[i] = tr->root_end[par];
+    } else {
+      tr->off[i] = 0;
+      tr->depth[i] = 1;
+      tr->root_start[i] = tr->start[i];
+      tr->root_end[i] = tr->end[i];
+    }
+    pairs += (int64_t)len[i] * tr->off[i] + (int64_t)len[i] * (len[i] + 1) / 2;
+    maxpos = std::max<int64_t>(maxpos, (int64_t)tr->off[i] + len[i]);
+    maxdepth = std::max<int64_t>(maxdepth, tr->depth[i]);
+    if (row >= (int64_t(1) << 30)) break;
+    stack.push_back(i);
+  }
+  while (!stack.empty()) {
+    tr->sub_end[stack.back()] = (int32_t)row;
+    stack.pop_back();
+  }
+  if (row <= 0 || row >= (int64_t(1) << 30)) {
+    set_error("pg_pack_tree: total tokens must be in [1, 2^30), got %lld", (long long)row);
+    return PG_ERR_INVALID_ARG;
+  }
+  if (maxdepth > kMaxExtraRanges + 2) {
+    set_error("pg_pack_tree: nesting depth %lld exceeds %d", (long long)maxdepth,
+              kMaxExtraRanges + 2);
+    return PG_ERR_UNSUPPORTED;
+  }
+  // Units: runs of consecutive sibling leaves (non-root), else single nodes; empty nodes skipped.
+  for (int32_t i = 0; i < N; ++i) {
+    if (len[i] == 0) continue;
+    const bool run = tr->leaf[i] && parent[i] >= 0;
+    if (run && !tr->units.empty() && tr->units.back().run && tr->units.back().node == parent[i] &&
+        tr->units.back().r1 == tr->start[i]) {
+      tr->units.back().r1 = tr->end[i];
+      continue;
+    }
+    tr->units.push_back({tr->start[i], tr->end[i], run ? parent[i] : i, run});
+  }
+  int64_t roots = 0;
+  for (int32_t i = 0; i < N; ++i) roots += parent[i] < 0;
+  p->T = row;
+  p->segs = N;
+  p->max_pos = maxpos;
+  p->pairs = pairs;
+  p->max_depth = maxdepth;
+  p->max_resp = 0;
+  // Tile counts per unit; the interval table holds, per forward tile, the causal ranges beyond the
+  // first (at most depth - 1 of them).
+  int64_t n64 = 0, n128 = 0, n256 = 0, n_iv = 0;
+  for (const auto& u : tr->units) {
+    const int64_t L = u.r1 - u.r0;
+    n64 += (L + 63) / 64;
+    n128 += (L + 127) / 128;
+    n256 += (L + 255) / 256;
+    const int64_t extra = std::max<int64_t>(0, tr->depth[u.node] - 1);
+    n_iv += extra * ((L + 63) / 64 + (L + 127) / 128 + (L + 255) / 256);
+  }
+  p->n[FWD64] = p->n[BWD64] = n64;
+  p->n[FWD128] = p->n[BWD128] = n128;
+  p->n[FWD256] = n256;
+  // A tree of depth <= 2 is a two-level group: give it the response spans of the scoring path.
+  int64_t nspan = 0;
+  if (maxdepth <= 2)
+    for (int32_t i = 0; i < N; ++i)
+      if (parent[i] < 0 && tr->sub_end[i] > tr->end[i]) {
+        ++nspan;
+        p->max_resp = std::max<int64_t>(p->max_resp, tr->sub_end[i] - tr->end[i]);
+      }
+  p->n[SPANS] = nspan;
+  p->n_iv = n_iv;
+  int64_t off = 0;
+  p->off_tokens = off;
+  off = align_up(off + 16 * row, 256);
+  for (int w = 0; w < NUM_LISTS; ++w) {
+    p->off[w] = off;
+    off = align_up(off + 32 * p->n[w], 256);
+  }
+  p->off_iv = off;
+  off = align_up(off + 8 * n_iv, 256);
+  p->bytes = off;
+  (void)roots;
+  return PG_OK;
+}
+
+static void build_tree_tables(const Tree& tr, const Plan& p, int32_t* pos, char* tables) {
+  const int32_t N = (int32_t)tr.parent.size();
+  int4* tok = reinterpret_cast<int4*>(tables + p.off_tokens);
+  std::vector<int32_t> node_end(p.T);      // end of each row's own node
+  for (int32_t i = 0; i < N; ++i)
+    for (int32_t t = tr.start[i]; t < tr.end[i]; ++t) {
+      const int32_t ps = tr.off[i] + (t - tr.start[i]);
+      tok[t] = make_int4(tr.root_start[i], tr.root_end[i], tr.start[i], ps);
+      pos[t] = ps;
+      node_end[t] = tr.end[i];
+    }
+  int2* ivs = reinterpret_cast<int2*>(tables + p.off_iv);
+  int64_t n_iv = 0;
+  // The causal ranges a unit's query rows need: its node's ancestors (root first) and, for a
+  // single-node unit, the node itself (clipped to the tile's last row).
+  auto ancestors = [&](int32_t node, bool include_self, std::vector<int2>& out) {
+    out.clear();
+    for (int32_t a = include_self ? node : tr.parent[node]; a >= 0; a = tr.parent[a])
+      if (tr.len[a] > 0) out.push_back(make_int2(tr.start[a], tr.end[a]));
+    std::reverse(out.begin(), out.end());
+  };
+  std::vector<int2> anc;
+  for (int bm = 64, wi = 0; bm <= 256; bm *= 2, ++wi) {
+    std::vector<FwdTile> ft;
+    std::vector<BwdTile> bt;
+    std::vector<int64_t> fc, bc;
+    for (const auto& u : tr.units) {
+      ancestors(u.node, true, anc);   // the node itself, or the leaves' parent, and above
+      int64_t anc_keys = 0;
+      for (const auto& a : anc) anc_keys += a.y - a.x;
+      for (int32_t q0 = u.r0; q0 < u.r1; q0 += bm) {
+        const int32_t q1 = std::min(q0 + bm, u.r1);
+        FwdTile t{};
+        t.q0 = q0;
+        t.q1 = q1;
+        // First causal range: the outermost; the others go to the interval table.
+        std::vector<int2> rng(anc);
+        if (!u.run) rng.back().y = std::min(rng.back().y, q1);
+        t.g0 = rng.empty() ? q0 : rng[0].x;
+        t.p_end = rng.empty() ? q0 : rng[0].y;
+        t.a_off = (int32_t)n_iv;
+        t.a_cnt = (int32_t)(rng.size() > 0 ? rng.size() - 1 : 0);
+        for (size_t k = 1; k < rng.size(); ++k) ivs[n_iv++] = rng[k];
+        if (u.run) {
+          t.s_lo = tok[q0].z;
+          t.s_hi = q1;
+        } else {
+          t.s_lo = t.s_hi = q1;
+        }
+        ft.push_back(t);
+        fc.push_back((int64_t)(q1 - q0) * (anc_keys + (t.s_hi - t.s_lo)));
+        if (wi < 2) {
+          // Key-major: keys [q0, q1) are seen by rows from themselves up to the end of their
+          // node's subtree (a single node) or of their own leaf (a run of leaves).
+          BwdTile b{};
+          b.k0 = q0;
+          b.k1 = q1;
+          b.q_lo = q0;
+          b.g0 = tok[q0].x;
+          if (u.run) {
+            b.q_hi = node_end[q1 - 1];
+            b.pe = q0;             // every key of the tile is seen by its own leaf's rows only
+          } else {
+            b.q_hi = tr.sub_end[u.node];
+            b.pe = q1;             // every key is seen by all later rows of the subtree
+          }
+          bt.push_back(b);
+          bc.push_back((int64_t)(q1 - q0) * (b.q_hi - b.q_lo));
+        }
+      }
+    }
+    sort_by_cost(ft, fc);
+    sort_by_cost(bt, bc);
+    const int fw = wi == 0 ? FWD64 : wi == 1 ? FWD128 : FWD256;
+    memcpy(tables + p.off[fw], ft.data(), ft.size() * sizeof(FwdTile));
+    if (wi < 2) {
+      const int bw = wi == 0 ? BWD64 : BWD128;
+      memcpy(tables + p.off[bw], bt.data(), bt.size() * sizeof(BwdTile));
+    }
+  }
+  if (p.n[SPANS] > 0) {
+    std::vector<FwdTile> spans;
+    for (int32_t i = 0; i < N; ++i)
+      if (tr.parent[i] < 0 && tr.sub_end[i] > tr.end[i]) {
+        FwdTile t{};
+        t.q0 = tr.end[i];
+        t.q1 = tr.sub_end[i];
+        t.g0 = tr.start[i];
+        t.p_end = tr.end[i];
+        t.s_lo = tr.end[i];
+        t.s_hi = tr.sub_end[i];
+        spans.push_back(t);
+      }
+    memcpy(tables + p.off[SPANS], spans.data(), spans.size() * sizeof(FwdTile));
+  }
 }
 
 // Copies a host-built layout to the caller's device buffers and points *layout at them.
@@ -479,6 +726,57 @@ pg_status pg_pack(int32_t num_groups, const int32_t* prefix_lens, const int32_t*
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
+pg_status pg_pack_tree_size(int32_t num_nodes, const int32_t* parent, const int32_t* seg_lens,
+                            int64_t* total_tokens, int64_t* table_bytes) {
+  Plan p;
+  Tree tr;
+  pg_status st = plan_tree(num_nodes, parent, seg_lens, &tr, &p);
+  if (st != PG_OK) return st;
+  if (total_tokens) *total_tokens = p.T;
+  if (table_bytes) *table_bytes = p.bytes;
+  return PG_OK;
+}
+
+pg_status pg_pack_tree_host(int32_t num_nodes, const int32_t* parent, const int32_t* seg_lens,
+                            int32_t* position_ids, void* tables, int64_t table_bytes,
+                            pg_layout* layout) {
+  Plan p;
+  Tree tr;
+  pg_status st = plan_tree(num_nodes, parent, seg_lens, &tr, &p);
+  if (st != PG_OK) return st;
+  if (!position_ids || !tables || !layout || table_bytes < p.bytes) {
+    set_error("pg_pack_tree_host: NULL buffer or table buffer smaller than %lld bytes",
+              (long long)p.bytes);
+    return PG_ERR_INVALID_ARG;
+  }
+  memset(tables, 0, (size_t)p.bytes);
+  build_tree_tables(tr, p, position_ids, static_cast<char*>(tables));
+  int32_t roots = 0;
+  for (int32_t i = 0; i < num_nodes; ++i) roots += parent[i] < 0;
+  fill_layout(roots, p, position_ids, tables, layout);
+  return PG_OK;
+}
+
+pg_status pg_pack_tree(int32_t num_nodes, const int32_t* parent, const int32_t* seg_lens,
+                       int32_t* position_ids_dev, void* tables_dev, int64_t table_bytes,
+                       pg_layout* layout, pg_stream_t stream) {
+  int64_t T = 0, bytes = 0;
+  pg_status st = pg_pack_tree_size(num_nodes, parent, seg_lens, &T, &bytes);
+  if (st != PG_OK) return st;
+  if (!position_ids_dev || !tables_dev || !layout || table_bytes < bytes) {
+    set_error("pg_pack_tree: NULL buffer or table buffer smaller than %lld bytes",
+              (long long)bytes);
+    return PG_ERR_INVALID_ARG;
+  }
+  std::vector<int32_t> pos((size_t)T);
+  std::vector<char> tab((size_t)bytes);
+  pg_layout host;
+  st = pg_pack_tree_host(num_nodes, parent, seg_lens, pos.data(), tab.data(), bytes, &host);
+  if (st != PG_OK) return st;
+  return upload_layout(pos, tab, position_ids_dev, tables_dev, host, layout,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
 pg_status pg_pack_padded_size(int32_t num_groups, int32_t prefix_len, int32_t group_size,
                               int32_t max_response_len, const int32_t* response_lens,
                               int64_t* total_tokens, int64_t* table_bytes) {
@@ -573,6 +871,11 @@ pg_status pg_grouped_attn_fwd(const pg_layout* layout, pg_dtype dtype, int32_t h
   const void* qx = q;
   const void* kx = k;
   const bool responses_only = (a.flags & PG_FLAG_RESPONSES_ONLY) != 0;
+  if (responses_only && layout->max_depth > 2) {
+    set_error("%s: PG_FLAG_RESPONSES_ONLY needs a two-level layout (pg_pack / pg_pack_padded)",
+              who);
+    return PG_ERR_UNSUPPORTED;
+  }
   if (rope && responses_only) {
     // Every key is rotated; of q only the response rows, the only ones read.
     st = launch_rope(a, k, ws + w.k_rot, heads_kv, nullptr, nullptr, 0, false, false, nullptr,

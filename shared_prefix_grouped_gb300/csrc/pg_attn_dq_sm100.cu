@@ -45,6 +45,44 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ int s_status_dq = 0;
 
+// Key tile j of the CTA: the tiles of its causal key ranges first, then of its own range.
+// Built once per CTA in shared memory.
+struct Plan {
+  int n_r, n_a, n;
+  int lo[kMaxKeyRanges], hi[kMaxKeyRanges], cum[kMaxKeyRanges + 1];
+  __device__ void init(const FwdTile& t, const int2* ivs) {
+    KeyRanges kr;
+    kr.init(t, ivs);
+    n_r = kr.n;
+    cum[0] = 0;
+    n_a = 0;
+    for (int r = 0; r < kr.n; ++r) {
+      lo[r] = kr.lo[r];
+      hi[r] = kr.hi[r];
+      cum[r + 1] = cum[r] + (hi[r] - lo[r] + BN - 1) / BN;
+      if (r + 1 == kr.n_causal) n_a = cum[r + 1];
+    }
+    n = cum[kr.n];
+  }
+};
+
+// Walks the key tiles of a Plan in increasing j, keeping the current range in registers (the
+// tables in shared memory are read only when a range ends).
+struct TileCursor {
+  int r, base, next, lo, hi;
+  __device__ explicit TileCursor(const Plan& p) : r(0), base(0), next(p.cum[1]), lo(p.lo[0]), hi(p.hi[0]) {}
+  __device__ int seek(const Plan& p, int j) {   // returns the first key of tile j; hi = its range end
+    while (j >= next && r + 1 < p.n_r) {
+      ++r;
+      base = next;
+      next = p.cum[r + 1];
+      lo = p.lo[r];
+      hi = p.hi[r];
+    }
+    return lo + (j - base) * BN;
+  }
+};
+
 struct DqSmem {
   uint8_t q[2 * QH];
   uint8_t dO[2 * QH];
@@ -54,6 +92,7 @@ struct DqSmem {
   uint64_t kv_full[NS], kv_empty[NS];
   uint64_t s_full, s_free, p_full[2], ds_free[2], dq_done, mma_done, mma_done2;
   uint32_t tmem;
+  Plan plan;
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -64,34 +103,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 __device__ __forceinline__ void fail(int code) { atomicCAS(&s_status_dq, 0, code); }
 
-// Key tile j of the CTA: tiles of the prefix range first, then of the responses' range.
-struct Plan {
-  int g0, p_end, s_lo, s_hi, n_a, n;
-  __device__ explicit Plan(const FwdTile& t) {
-    g0 = t.g0;
-    p_end = t.p_end;
-    s_lo = t.s_lo;
-    s_hi = t.s_hi;
-    n_a = (p_end - g0 + BN - 1) / BN;
-    n = n_a + (s_hi - s_lo + BN - 1) / BN;
-  }
-  __device__ void get(int j, int& kt, int& hi) const {
-    if (j < n_a) {
-      kt = g0 + j * BN;
-      hi = p_end;
-    } else {
-      kt = s_lo + (j - n_a) * BN;
-      hi = s_hi;
-    }
-  }
-};
-
 __global__ void __launch_bounds__(NTHREADS, 1)
 attn_dq_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                      const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                      __nv_bfloat16* __restrict__ dq, const float* __restrict__ lse2,
                      const float* __restrict__ dsum, int64_t ldl, const int4* __restrict__ tok,
-                     const FwdTile* __restrict__ tiles, int Hq, int Hkv, int Ttot,
+                     const FwdTile* __restrict__ tiles, const int2* __restrict__ ivs, int Hq,
+                     int Hkv, int Ttot,
                      float scale_log2, float scale, const float2* __restrict__ rope_tab,
                      int hc, uint64_t wait_ns) {
   extern __shared__ uint8_t smem_raw[];
@@ -103,12 +121,10 @@ attn_dq_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
   const int kh = h / (Hq / Hkv);
   const FwdTile tl = tiles[tile_id];
   if (tl.q0 < 0 || tl.q1 > Ttot || tl.q0 >= tl.q1 || tl.q1 - tl.q0 > BM || tl.g0 < 0 ||
-      tl.s_hi > Ttot) {
+      tl.s_hi > Ttot || tl.a_cnt < 0 || tl.a_cnt > kMaxExtraRanges) {
     if (threadIdx.x == 0) fail(PG_ERR_DEVICE);
     return;
   }
-  const Plan pl(tl);
-  const int n = pl.n;
 
   if (threadIdx.x == 0) {
     mbar_init(&sm.q_full, 1);
@@ -126,6 +142,7 @@ attn_dq_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     mbar_init(&sm.mma_done, 1);
     mbar_init(&sm.mma_done2, 1);
     fence_mbar_init();
+    sm.plan.init(tl, ivs);
   }
   if (warp == 1) {
     tmem_alloc(&sm.tmem, 512);
@@ -136,6 +153,8 @@ attn_dq_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
   tc_fence_after();
   const uint32_t tmem = sm.tmem;
   const uint32_t t_s = tmem, t_dp = tmem + 128, t_dq = tmem + 256, t_ds = tmem + 384;
+  const Plan& pl = sm.plan;
+  const int n = pl.n, n_a = pl.n_a;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer -----
@@ -151,14 +170,14 @@ attn_dq_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
       tma_load_2d(sm.dO, &tdo, &sm.q_full, xq, tl.q0);
       tma_load_2d(sm.dO + QH, &tdo, &sm.q_full, xq + 64, tl.q0);
       int issued = 0;
+      TileCursor cur(pl);
       for (int j = 0; j < n; ++j) {
         const int s = j % NS;
         if (!mbar_wait(&sm.kv_empty[s], ((j / NS) & 1) ^ 1, wait_ns)) {
           fail(PG_ERR_TIMEOUT);
           break;
         }
-        int kt, hi;
-        pl.get(j, kt, hi);
+        const int kt = cur.seek(pl, j);
         mbar_expect_tx(&sm.kv_full[s], 4 * KH);
         tma_load_2d(sm.k[s], &tk, &sm.kv_full[s], xk, kt);
         tma_load_2d(sm.k[s] + KH, &tk, &sm.kv_full[s], xk + 64, kt);
@@ -248,14 +267,15 @@ attn_dq_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     const float dr_ = dsum[(size_t)h * ldl + rowc];
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     bool ok = true;
+    TileCursor cur(pl);
     for (int j = 0; j < n; ++j) {
-      int kt, hi;
-      pl.get(j, kt, hi);
+      const int kt = cur.seek(pl, j);
+      const int hi = cur.hi;
       if (!warp_wait(&sm.s_full, j & 1, wait_ns)) { ok = false; break; }
       tc_fence_after();
       // The row's visible keys in this tile: one contiguous run [lo, lo + len) of columns.
-      const bool full = (j < pl.n_a) && (kt + BN <= hi) && (kt + BN - 1 <= tl.q0);
-      const int lo = (j < pl.n_a) ? 0 : max(ti.z - kt, 0);
+      const bool full = (j < n_a) && (kt + BN <= hi) && (kt + BN - 1 <= tl.q0);
+      const int lo = (j < n_a) ? 0 : max(ti.z - kt, 0);
       const int len = full ? BN : max(min(hi, rowc + 1) - kt - lo, 0);
       uint32_t dw[32];
 #pragma unroll
@@ -370,7 +390,8 @@ pg_status launch_dq_sm100(const AttnArgs& a, const void* q, const void* k, const
   prof_begin(PG_KERNEL_BWD_DQ, a.stream);
   attn_dq_sm100_kernel<<<(unsigned)(L->n_tiles[FWD128] * a.Hq), NTHREADS, smem, a.stream>>>(
       tq, tdo, tk, tv, static_cast<__nv_bfloat16*>(dq), lse2, Dbuf, padded_tokens(L), tokens(L),
-      tiles<FwdTile>(L, FWD128), a.Hq, a.Hkv, (int)T, a.scale * kLog2e, a.scale, rope_tab,
+      tiles<FwdTile>(L, FWD128), intervals(L), a.Hq, a.Hkv, (int)T, a.scale * kLog2e, a.scale,
+      rope_tab,
       order_chunk(a.Hq, 1), 2000000000ull);
   prof_end(PG_KERNEL_BWD_DQ, a.stream);
   return cuda_check(cudaGetLastError(), "dq sm100 launch");

@@ -51,6 +51,51 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 __device__ int s_status_fwd = 0;
 
+// Key tile j of a CTA: the tiles of its causal key ranges (the group's prefix, or a nested
+// prefix's ancestors) first, then of its own range; and which query tiles need it.  Built once per
+// CTA in shared memory.
+struct Plan {
+  int n_r, n_a, n;                  // key ranges, key tiles in causal ranges, all key tiles
+  int lo[kMaxKeyRanges], hi[kMaxKeyRanges], cum[kMaxKeyRanges + 1];
+  int q0, q1;
+  int last[2];      // last query row of each query tile (-1: tile empty)
+  __device__ void init(const FwdTile& t, const int2* ivs) {
+    KeyRanges kr;
+    kr.init(t, ivs);
+    n_r = kr.n;
+    cum[0] = 0;
+    n_a = 0;
+    for (int r = 0; r < kr.n; ++r) {
+      lo[r] = kr.lo[r];
+      hi[r] = kr.hi[r];
+      cum[r + 1] = cum[r] + (hi[r] - lo[r] + BN - 1) / BN;
+      if (r + 1 == kr.n_causal) n_a = cum[r + 1];
+    }
+    n = cum[kr.n];
+    q0 = t.q0;
+    q1 = t.q1;
+    last[0] = min(q0 + BM, q1) - 1;
+    last[1] = (q1 > q0 + BM) ? q1 - 1 : -1;
+  }
+};
+
+// Walks the key tiles of a Plan in increasing j, keeping the current range in registers (the
+// tables in shared memory are read only when a range ends).
+struct TileCursor {
+  int r, base, next, lo, hi;
+  __device__ explicit TileCursor(const Plan& p) : r(0), base(0), next(p.cum[1]), lo(p.lo[0]), hi(p.hi[0]) {}
+  __device__ int seek(const Plan& p, int j) {   // returns the first key of tile j; hi = its range end
+    while (j >= next && r + 1 < p.n_r) {
+      ++r;
+      base = next;
+      next = p.cum[r + 1];
+      lo = p.lo[r];
+      hi = p.hi[r];
+    }
+    return lo + (j - base) * BN;
+  }
+};
+
 struct FwdSmem {
   uint8_t q[2][2 * QHALF];
   uint8_t k[NS][2 * KHALF];
@@ -62,6 +107,7 @@ struct FwdSmem {
   uint64_t pv_done[2][2];   // the P V product reading [query tile][buffer] has completed
   uint64_t mma_done, mma_done2;
   uint32_t tmem;
+  Plan plan;
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -72,45 +118,12 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 __device__ __forceinline__ void fail(int code) { atomicCAS(&s_status_fwd, 0, code); }
 
-// Key tile j of a CTA: tiles of the prefix range first, then of the responses' range; and which
-// query tiles need it.
-struct Plan {
-  int g0, p_end, s_lo, s_hi, n_a, n;
-  int q0, q1;
-  int last[2];      // last query row of each query tile (-1: tile empty)
-  __device__ Plan(const FwdTile& t) {
-    g0 = t.g0;
-    p_end = t.p_end;
-    s_lo = t.s_lo;
-    s_hi = t.s_hi;
-    q0 = t.q0;
-    q1 = t.q1;
-    n_a = (p_end - g0 + BN - 1) / BN;
-    n = n_a + (s_hi - s_lo + BN - 1) / BN;
-    last[0] = min(q0 + BM, q1) - 1;
-    last[1] = (q1 > q0 + BM) ? q1 - 1 : -1;
-  }
-  __device__ void get(int j, int& kt, int& hi) const {
-    if (j < n_a) {
-      kt = g0 + j * BN;
-      hi = p_end;
-    } else {
-      kt = s_lo + (j - n_a) * BN;
-      hi = s_hi;
-    }
-  }
-  __device__ bool rel(int i, int j) const {
-    int kt, hi;
-    get(j, kt, hi);
-    return last[i] >= 0 && kt <= last[i];
-  }
-};
-
 __global__ void __launch_bounds__(NTHREADS, 1)
 attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ o,
                       float* __restrict__ lse, const int4* __restrict__ tok,
-                      const FwdTile* __restrict__ tiles, int Hq, int Hkv, int Ttot,
+                      const FwdTile* __restrict__ tiles, const int2* __restrict__ ivs, int Hq,
+                      int Hkv, int Ttot,
                       float scale_log2, uint64_t wait_ns, uint32_t debug) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -120,13 +133,11 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
   const int kh = h / (Hq / Hkv);
   const FwdTile tl = tiles[tile_id];
   if (tl.q0 < 0 || tl.q1 > Ttot || tl.q0 >= tl.q1 || tl.q1 - tl.q0 > 2 * BM || tl.g0 < 0 ||
-      tl.s_hi > Ttot) {
+      tl.s_hi > Ttot || tl.a_cnt < 0 || tl.a_cnt > kMaxExtraRanges) {
     if (threadIdx.x == 0) fail(PG_ERR_DEVICE);
     return;
   }
-  const Plan pl(tl);
-  const int n = pl.n;
-  const int nq = pl.last[1] >= 0 ? 2 : 1;
+  const int nq = (tl.q1 > tl.q0 + BM) ? 2 : 1;
 
   if (threadIdx.x == 0) {
     mbar_init(&sm.q_full, 1);
@@ -146,6 +157,7 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     mbar_init(&sm.mma_done, 1);
     mbar_init(&sm.mma_done2, 1);
     fence_mbar_init();
+    sm.plan.init(tl, ivs);
   }
   if (warp == 1) {
     tmem_alloc(&sm.tmem, 512);
@@ -155,6 +167,11 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem;
+  const Plan& pl = sm.plan;
+  const int n = pl.n, n_a = pl.n_a;
+  const int last0 = pl.last[0], last1 = pl.last[1];
+  // Query tile i needs key tile j unless the tile starts after the query tile's last row.
+  auto rel = [&](int i, int kt) { const int l = i ? last1 : last0; return l >= 0 && kt <= l; };
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer -----
@@ -169,14 +186,14 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
         tma_load_2d(sm.q[i] + QHALF, &tq, &sm.q_full, xq + 64, tl.q0 + i * BM);
       }
       int issued = 0;
+      TileCursor cur(pl);
       for (int j = 0; j < n; ++j) {
         const int s = j % NS;
         if (!mbar_wait(&sm.kv_empty[s], ((j / NS) & 1) ^ 1, wait_ns)) {
           fail(PG_ERR_TIMEOUT);
           break;
         }
-        int kt, hi;
-        pl.get(j, kt, hi);
+        const int kt = cur.seek(pl, j);
         mbar_expect_tx(&sm.k_full[s], 2 * KHALF);
         tma_load_2d(sm.k[s], &tk, &sm.k_full[s], xk, kt);
         tma_load_2d(sm.k[s] + KHALF, &tk, &sm.k_full[s], xk + 64, kt);
@@ -204,9 +221,11 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       const uint64_t kd0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
       // S_i(j): scores of query tile i against key tile j.  Needs the K tile and the softmax of
       // tile i to have read its previous scores out of TMEM (S_i is single-buffered).
+      TileCursor cur(pl);
       for (int j = 0; ok && j < n; ++j) {
+        const int kt = cur.seek(pl, j);
         for (int i = 0; i < nq; ++i) {
-          if (!pl.rel(i, j)) continue;
+          if (!rel(i, kt)) continue;
           if (!mbar_wait(&sm.k_full[j % NS], (j / NS) & 1, wait_ns)) { ok = false; break; }
           if (n_s[i] > 0 && !mbar_wait(&sm.s_free[i], (n_s[i] - 1) & 1, wait_ns)) {
             ok = false;
@@ -241,10 +260,12 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       int n_pv[2] = {0, 0};       // P V products issued per query tile
       const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0]), KHALF, 1024);
       bool ok = true;
+      TileCursor cur(pl);
       for (int j = 0; ok && j < n; ++j) {
+        const int kt = cur.seek(pl, j);
         if (!mbar_wait(&sm.v_full[j % NS], (j / NS) & 1, wait_ns)) { ok = false; break; }
         for (int i = 0; i < nq && ok; ++i) {
-          if (!pl.rel(i, j)) continue;
+          if (!rel(i, kt)) continue;
           const int b = n_pv[i] & 1;
           if (!mbar_wait(&sm.p_full[i][b], (n_pv[i] >> 1) & 1, wait_ns)) { ok = false; break; }
           tc_fence_after();
@@ -270,7 +291,7 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     const int quarter = warp & 3;                 // TMEM lanes this warp may access
     const int r = quarter * 32 + lane;            // query row within the tile
     const int row = tl.q0 + i * BM + r;
-    const int qlast = pl.last[i];
+    const int qlast = i ? last1 : last0;
     const bool active = qlast >= 0;
     const bool valid = active && row <= qlast;
     const int rowc = valid ? row : (active ? qlast : tl.q0);
@@ -281,10 +302,11 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     int c = 0;
+    TileCursor cur(pl);
     for (int j = 0; active && j < n; ++j) {
-      if (!pl.rel(i, j)) continue;
-      int kt, hi;
-      pl.get(j, kt, hi);
+      const int kt = cur.seek(pl, j);
+      const int hi = cur.hi;
+      if (!rel(i, kt)) continue;
       if (!warp_wait(&sm.s_full[i], c & 1, wait_ns)) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[64];
@@ -294,7 +316,7 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       tc_fence_before();
       mbar_arrive(&sm.s_free[i]);
       // Scores in log2 units; mask where the tile is not entirely visible to every row.
-      const bool full_tile = (j < pl.n_a) && (kt + BN <= hi) && (kt + BN - 1 <= first_row);
+      const bool full_tile = (j < n_a) && (kt + BN <= hi) && (kt + BN - 1 <= first_row);
       float mx = -INFINITY;
       if (full_tile) {
 #pragma unroll
@@ -308,7 +330,7 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
         // prefix range [kt, min(hi, row + 1)); in the responses' range the same run starting no
         // earlier than the row's own response (prefix rows get an empty run there).  One unsigned
         // compare per column, no branches.
-        const int lo = (j < pl.n_a) ? 0 : max(ti.z - kt, 0);
+        const int lo = (j < n_a) ? 0 : max(ti.z - kt, 0);
         const int len = max(min(hi, rowc + 1) - kt - lo, 0);
 #pragma unroll
         for (int cc = 0; cc < BN; ++cc) {
@@ -435,7 +457,7 @@ pg_status launch_fwd_sm100(const AttnArgs& a, const void* q, const void* k, cons
   prof_begin(PG_KERNEL_ATTN_FWD, a.stream);
   attn_fwd_sm100_kernel<<<(unsigned)(L->n_tiles[FWD256] * a.Hq), NTHREADS, smem, a.stream>>>(
       tq, tk, tv, static_cast<__nv_bfloat16*>(o), lse, tokens(L), tiles<FwdTile>(L, FWD256),
-      a.Hq, a.Hkv, (int)T, a.scale * kLog2e, wait_ns, a.debug);
+      intervals(L), a.Hq, a.Hkv, (int)T, a.scale * kLog2e, wait_ns, a.debug);
   prof_end(PG_KERNEL_ATTN_FWD, a.stream);
   return cuda_check(cudaGetLastError(), "fwd sm100 launch");
 }

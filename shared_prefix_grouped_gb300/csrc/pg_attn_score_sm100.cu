@@ -96,10 +96,10 @@ struct Work {
     if (t0 >= sp.q1) return false;
     t_end = min(t0 + TB, sp.q1);
     rows = (t_end - t0) * hp;
-    const int lp = sp.pe - sp.g0;
+    const int lp = sp.p_end - sp.g0;
     const int chunk = ((lp + nsplit - 1) / nsplit + BN - 1) / BN * BN;
-    p_lo = min(sp.g0 + c * chunk, sp.pe);
-    p_hi = min(p_lo + chunk, sp.pe);
+    p_lo = min(sp.g0 + c * chunk, sp.p_end);
+    p_hi = min(p_lo + chunk, sp.p_end);
     if (c == 0) {
       s_lo = tok[t0].z;          // first row of the first token's own response
       s_hi = t_end;

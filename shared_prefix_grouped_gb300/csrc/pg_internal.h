@@ -10,14 +10,46 @@
 
 namespace pg {
 
-// Work item of the forward (and of the SIMT dQ kernel): query rows [q0, q1) of one group.
-// Keys are visited in two ranges: the group's prefix [g0, p_end) and the responses' part
-// [s_lo, s_hi).  A query row t sees key s iff s <= t && s >= g0 && (s < pe || s >= own_lo(t)).
+// Work item of the forward and of the query-major dQ: query rows [q0, q1) of one group (tree).
+// Its keys lie in "causal" ranges -- [g0, p_end) and a_cnt more ranges, entries a_off .. of the
+// layout's interval table (the further ancestors of a nested prefix) -- in which row t sees key s
+// iff s <= t, and in the "own" range [s_lo, s_hi), in which row t sees s iff own_lo(t) <= s <= t.
+// For a two-level group [P; R1; ...; RG]: [g0, p_end) is the prefix (p_end = min(pe, q1)), the own
+// range covers the tile's responses, a_cnt = 0.
 struct FwdTile {
   int32_t q0, q1;      // query rows
-  int32_t g0, p_end;   // prefix keys [g0, p_end), p_end = min(pe, q1)
-  int32_t s_lo, s_hi;  // response keys [s_lo, s_hi) (empty when the tile has no response rows)
-  int32_t pe, pad;     // row after the group's prefix
+  int32_t g0, p_end;   // first causal key range
+  int32_t s_lo, s_hi;  // own key range (empty when the tile has no such rows)
+  int32_t a_off, a_cnt;  // further causal ranges in the interval table
+};
+
+// The key ranges of a FwdTile in visiting order: causal ranges first, then the own range.
+constexpr int kMaxKeyRanges = 8;
+struct KeyRanges {
+  int n, n_causal;
+  int lo[kMaxKeyRanges], hi[kMaxKeyRanges];
+  __host__ __device__ void init(const FwdTile& t, const int2* intervals) {
+    n = 0;
+    if (t.p_end > t.g0) {
+      lo[n] = t.g0;
+      hi[n] = t.p_end;
+      ++n;
+    }
+    for (int i = 0; i < t.a_cnt && n < kMaxKeyRanges - 1; ++i) {
+      const int2 iv = intervals[t.a_off + i];
+      if (iv.y > iv.x) {
+        lo[n] = iv.x;
+        hi[n] = iv.y;
+        ++n;
+      }
+    }
+    n_causal = n;
+    if (t.s_hi > t.s_lo) {
+      lo[n] = t.s_lo;
+      hi[n] = t.s_hi;
+      ++n;
+    }
+  }
 };
 
 // Work item of the key-major backward: key rows [k0, k1) of one group and the query rows
@@ -40,6 +72,13 @@ enum TileList { FWD64 = 0, FWD128 = 1, BWD64 = 2, BWD128 = 3, FWD256 = 4, SPANS 
 // Row stride (elements) of the per-head fp32 rows the backward keeps for LSE and rowsum(dO * O):
 // T rounded up to a multiple of 4, so every row starts 16-byte aligned (a TMA requirement).
 inline int64_t padded_tokens(const pg_layout* L) { return (L->total_tokens + 3) & ~int64_t(3); }
+
+// Maximum number of further causal ranges of a tile (a nested prefix deeper than this is refused).
+constexpr int kMaxExtraRanges = kMaxKeyRanges - 2;
+
+inline const int2* intervals(const pg_layout* L) {
+  return reinterpret_cast<const int2*>(static_cast<const char*>(L->tables) + L->off_intervals);
+}
 
 inline const int4* tokens(const pg_layout* L) {
   return reinterpret_cast<const int4*>(static_cast<const char*>(L->tables) + L->off_tokens);

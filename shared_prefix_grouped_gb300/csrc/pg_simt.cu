@@ -103,10 +103,6 @@ __device__ __forceinline__ float quad_sum(float x) {
   x += __shfl_xor_sync(0xffffffffu, x, 2);
   return x;
 }
-__device__ __forceinline__ bool visible(int t, int s, int4 ti) {
-  // ti = {g0, pe, own_lo, pos} of query row t
-  return s <= t && s >= ti.x && (s < ti.y || s >= ti.z);
-}
 
 // ---------------------------------------------------------------------------------------------
 // RoPE: rotate (or inverse-rotate) the pairs (x[k], x[k + d/2]) of every head of a token by the
@@ -193,26 +189,31 @@ template <typename T, int D>
 __global__ void __launch_bounds__(256)
 fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                 T* __restrict__ o, float* __restrict__ lse, const int4* __restrict__ tok,
-                const FwdTile* __restrict__ tiles, int Hq, int Hkv, int Ttot, float qscale,
-                int responses_only) {
+                const FwdTile* __restrict__ tiles, const int2* __restrict__ ivs, int Hq, int Hkv,
+                int Ttot, float qscale, int responses_only) {
   constexpr int BN = 64, NV = D / 16;
   extern __shared__ float4 smem4[];
   float* Ks = reinterpret_cast<float*>(smem4);
   float* Vs = Ks + BN * D;
   const int tile_id = blockIdx.x / Hq, h = blockIdx.x % Hq;
   const FwdTile tl = tiles[tile_id];
-  if (tl.q0 < 0 || tl.q1 > Ttot || tl.q0 >= tl.q1 || tl.g0 < 0 || tl.s_hi > Ttot) {
+  if (tl.q0 < 0 || tl.q1 > Ttot || tl.q0 >= tl.q1 || tl.g0 < 0 || tl.s_hi > Ttot ||
+      tl.a_cnt < 0 || tl.a_cnt > kMaxExtraRanges) {
     report(PG_ERR_DEVICE);
     return;
   }
-  // Responses only: a tile made of prefix rows has nothing to compute (uniform exit).
-  if (responses_only && tl.q1 <= tl.pe) return;
+  // Responses only (two-level layouts): a row before its group's prefix end (the token table's
+  // pe) is a prefix row and computes nothing; a tile of prefix rows exits at once (uniformly).
+  if (responses_only && tl.q1 <= tok[tl.q1 - 1].y) return;
   const int kh = h / (Hq / Hkv);
   const int tid = threadIdx.x, r = tid >> 2, ql = tid & 3;
   const int row = tl.q0 + r;
-  const bool valid = row < tl.q1 && !(responses_only && row < tl.pe);
+  const int4 tr_ = tok[row < tl.q1 ? row : tl.q1 - 1];
+  const bool valid = row < tl.q1 && !(responses_only && row < tr_.y);
   const int rowc = valid ? row : tl.q1 - 1;
   const int4 ti = tok[rowc];
+  KeyRanges kr;
+  kr.init(tl, ivs);
   float4 qv[NV], acc[NV];
   const T* qrow = q + ((size_t)rowc * Hq + h) * D + 4 * ql;
 #pragma unroll
@@ -222,8 +223,9 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
     acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   float m = -INFINITY, l = 0.f;
-  for (int range = 0; range < 2; ++range) {
-    const int lo = range ? tl.s_lo : tl.g0, hi = range ? tl.s_hi : tl.p_end;
+  for (int range = 0; range < kr.n; ++range) {
+    const int lo = kr.lo[range], hi = kr.hi[range];
+    const bool own = range >= kr.n_causal;   // own range: keys from the row's own segment only
     for (int kt = lo; kt < hi; kt += BN) {
       __syncthreads();
       for (int e = tid; e < BN * D / 4; e += 256) {
@@ -249,7 +251,7 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
           p += dot4(qv[i], *reinterpret_cast<const float4*>(Ks + j * D + 4 * ql + 16 * i));
         p = quad_sum(p);
         int key = kt + j;
-        s[j] = (key < hi && visible(rowc, key, ti)) ? p : -INFINITY;
+        s[j] = (key < hi && key <= rowc && (!own || key >= ti.z)) ? p : -INFINITY;
         mt = fmaxf(mt, s[j]);
       }
       const float mnew = fmaxf(m, mt);
@@ -399,7 +401,9 @@ dkdv_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
         }
         s = quad_sum(s);
         dp = quad_sum(dp);
-        const bool vis = valid && visible(qr, keyc, Ts[j]);
+        // Key-major visibility of a tile: rows [keyc, q_hi) see the key if it is a prefix-like
+        // key of the tile (keyc < pe) or lies in the row's own segment.
+        const bool vis = valid && keyc <= qr && qr < tl.q_hi && (keyc < tl.pe || keyc >= Ts[j].z);
         const float p = vis ? exp2f(s - Ls[j]) : 0.f;
         const float ds = p * (dp - Ds[j]);
 #pragma unroll
@@ -434,18 +438,22 @@ __global__ void __launch_bounds__(256)
 dq_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                const T* __restrict__ dO, const float* __restrict__ lse,
                const float* __restrict__ Dbuf, float* __restrict__ dq_acc,
-               const int4* __restrict__ tok, const FwdTile* __restrict__ tiles, int Hq, int Hkv,
-               int Ttot, int ldd, float scale_log2, float scale) {
+               const int4* __restrict__ tok, const FwdTile* __restrict__ tiles,
+               const int2* __restrict__ ivs, int Hq, int Hkv, int Ttot, int ldd, float scale_log2,
+               float scale) {
   constexpr int BN = 64, NV = D / 16;
   extern __shared__ float4 smem4[];
   float* Ks = reinterpret_cast<float*>(smem4);
   float* Vs = Ks + BN * D;
   const int tile_id = blockIdx.x / Hq, h = blockIdx.x % Hq;
   const FwdTile tl = tiles[tile_id];
-  if (tl.q0 < 0 || tl.q1 > Ttot || tl.q0 >= tl.q1 || tl.g0 < 0 || tl.s_hi > Ttot) {
+  if (tl.q0 < 0 || tl.q1 > Ttot || tl.q0 >= tl.q1 || tl.g0 < 0 || tl.s_hi > Ttot ||
+      tl.a_cnt < 0 || tl.a_cnt > kMaxExtraRanges) {
     report(PG_ERR_DEVICE);
     return;
   }
+  KeyRanges kr;
+  kr.init(tl, ivs);
   const int kh = h / (Hq / Hkv);
   const int tid = threadIdx.x, r = tid >> 2, ql = tid & 3;
   const int row = tl.q0 + r;
@@ -463,8 +471,9 @@ dq_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __rest
   }
   const float L2 = lse[(size_t)h * Ttot + rowc] * kLog2e;
   const float Dr = Dbuf[(size_t)h * ldd + rowc];
-  for (int range = 0; range < 2; ++range) {
-    const int lo = range ? tl.s_lo : tl.g0, hi = range ? tl.s_hi : tl.p_end;
+  for (int range = 0; range < kr.n; ++range) {
+    const int lo = kr.lo[range], hi = kr.hi[range];
+    const bool own = range >= kr.n_causal;
     for (int kt = lo; kt < hi; kt += BN) {
       __syncthreads();
       for (int e = tid; e < BN * D / 4; e += 256) {
@@ -490,7 +499,7 @@ dq_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __rest
         }
         s = quad_sum(s);
         dp = quad_sum(dp);
-        const bool vis = visible(rowc, kt + j, ti);
+        const bool vis = kt + j <= rowc && (!own || kt + j >= ti.z);
         const float p = vis ? exp2f(s - L2) : 0.f;
         const float ds = p * (dp - Dr);
 #pragma unroll
@@ -530,7 +539,7 @@ pg_status fwd_simt_t(const AttnArgs& a, const void* q, const void* k, const void
   prof_begin(PG_KERNEL_ATTN_FWD, a.stream);
   kern<<<(unsigned)(n * a.Hq), 256, smem, a.stream>>>(
       static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
-      static_cast<T*>(o), lse, tokens(L), tiles<FwdTile>(L, FWD64), a.Hq, a.Hkv,
+      static_cast<T*>(o), lse, tokens(L), tiles<FwdTile>(L, FWD64), intervals(L), a.Hq, a.Hkv,
       (int)L->total_tokens, a.scale * kLog2e, (a.flags & PG_FLAG_RESPONSES_ONLY) ? 1 : 0);
   prof_end(PG_KERNEL_ATTN_FWD, a.stream);
   return cuda_check(cudaGetLastError(), "fwd_simt launch");
@@ -565,7 +574,8 @@ pg_status bwd_simt_t(const AttnArgs& a, const void* q, const void* k, const void
     prof_begin(PG_KERNEL_BWD_DQ, a.stream);
     kern<<<(unsigned)(L->n_tiles[FWD64] * a.Hq), 256, smem, a.stream>>>(
         static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
-        static_cast<const T*>(dO), lse, Dbuf, dq_acc, tokens(L), tiles<FwdTile>(L, FWD64), a.Hq,
+        static_cast<const T*>(dO), lse, Dbuf, dq_acc, tokens(L), tiles<FwdTile>(L, FWD64),
+        intervals(L), a.Hq,
         a.Hkv, Ttot, (int)padded_tokens(L), a.scale * kLog2e, a.scale);
     prof_end(PG_KERNEL_BWD_DQ, a.stream);
     return cuda_check(cudaGetLastError(), "dq_simt launch");

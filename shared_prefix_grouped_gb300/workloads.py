@@ -213,3 +213,71 @@ def small_layer(**kw) -> LayerWorkload:
                 group_size=3, prefix_len=150, suffix_len=70, rope_theta=5e5, seed=1104)
     base.update(kw)
     return LayerWorkload(name="llama_layer_small", **base)
+
+
+@dataclasses.dataclass(frozen=True)
+class TreeWorkload:
+    """Nested prefixes: segments in depth-first preorder (parent -1 for a root), e.g. a shared
+    context, several user turns below it and several sampled responses below each turn."""
+
+    name: str
+    dtype: str
+    parent: tuple
+    lens: tuple
+    heads_q: int
+    heads_kv: int
+    head_dim: int
+    rope_theta: float = 0.0
+    seed: int = 1006
+
+
+def multi_turn(context: int, turns: int, turn_len: int, responses: int, response_len: int):
+    """(parent, lens) of one context, `turns` user turns below it, `responses` answers per turn."""
+    parent, lens = [-1], [context]
+    for _ in range(turns):
+        t = len(parent)
+        parent.append(0)
+        lens.append(turn_len)
+        for _ in range(responses):
+            parent.append(t)
+            lens.append(response_len)
+    return tuple(parent), tuple(lens)
+
+
+TREE_WORKLOADS: List[TreeWorkload] = [
+    TreeWorkload("bf16_gqa32x8_d128_tree_p4096_t4x512_r4x256", "bf16",
+                 *multi_turn(4096, 4, 512, 4, 256), 32, 8, 128, rope_theta=5e5, seed=1006),
+]
+
+
+def tree_by_name(name: str) -> TreeWorkload:
+    for w in TREE_WORKLOADS:
+        if w.name == name:
+            return w
+    raise KeyError(name)
+
+
+@dataclasses.dataclass
+class TreeProblem:
+    workload: TreeWorkload
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    do: torch.Tensor
+
+    @property
+    def total_tokens(self) -> int:
+        return sum(self.workload.lens)
+
+
+def make_tree_problem(w: TreeWorkload, seed: Optional[int] = None) -> TreeProblem:
+    """Q, K, V, dO ~ N(0, 1) in fp32, cast to the workload dtype; draw order Q, K, V, dO."""
+    gen = torch.Generator().manual_seed(w.seed if seed is None else seed)
+    T = sum(w.lens)
+    dt = torch_dtype(w.dtype)
+
+    def draw(heads):
+        return torch.randn((T, heads, w.head_dim), generator=gen, dtype=torch.float32).to(dt)
+
+    q, k, v, do = draw(w.heads_q), draw(w.heads_kv), draw(w.heads_kv), draw(w.heads_q)
+    return TreeProblem(w, q, k, v, do)

@@ -102,7 +102,7 @@ def test_pack_host_matches_oracle_bit_exactly(case):
         gend = pe + sum(rs[s:s + g])
         s += g
         if gend > pe:
-            spans.append([pe, gend, g0, pe, pe, gend, pe, 0])
+            spans.append([pe, gend, g0, pe, pe, gend, 0, 0])
         g0 = gend
     assert st.n_tiles[5] == len(spans) and lists[5].tolist() == spans
     assert st.max_response_rows == max([sp[1] - sp[0] for sp in spans], default=0)
@@ -192,3 +192,76 @@ def test_padded_layout_rejects_bad_lengths():
         api.pack_padded_size(1, 4, 2, 3, [4, 1])
     with pytest.raises(_lib.PgError):
         api.pack_padded_size(1, 4, 2, 3, [-1, 1])
+
+
+TREE_CASES = [
+    ([-1, 0, 1, 1, 0, 4, 4, 4], [300, 70, 90, 130, 64, 1, 200, 65]),   # two turns, ragged
+    ([-1, 0, 1, 2, 2, 0, -1, 6, 6], [129, 64, 300, 7, 70, 5, 80, 40, 0]),  # depth 4, two roots
+    ([-1, 0, 0, 2, 2, 2], [0, 33, 100, 64, 1, 250]),                    # empty root
+    ([-1, 0, 0, 0], [257, 31, 1, 200]),                                 # two-level
+    ([-1, 0, 1, 2, 3, 4, 5, 6], [70, 3, 66, 1, 128, 9, 64, 300]),       # depth 8 chain
+]
+
+
+def tree_tables(parent, lens):
+    pos, tab, st = api.pack_tree_host(parent, lens)
+    raw = tab.numpy().tobytes()
+    T = st.total_tokens
+    tok = torch.frombuffer(bytearray(raw[st.off_tokens: st.off_tokens + 16 * T]),
+                           dtype=torch.int32).view(T, 4)
+    ivs = torch.frombuffer(bytearray(raw[st.off_intervals: st.off_intervals + 8 * st.n_intervals]),
+                           dtype=torch.int32).view(-1, 2) if st.n_intervals else torch.zeros((0, 2))
+    lists = []
+    for w in range(5):
+        n, o = st.n_tiles[w], st.off_tiles[w]
+        lists.append(torch.frombuffer(bytearray(raw[o: o + 32 * n]), dtype=torch.int32).view(n, 8)
+                     if n else torch.zeros((0, 8), dtype=torch.int32))
+    return pos, tok, ivs, lists, st
+
+
+@pytest.mark.parametrize("case", TREE_CASES)
+def test_tree_tables_expand_to_the_tree_visibility(case):
+    # The kernels' rules applied to every tile reproduce the oracle's visibility exactly.
+    parent, lens = case
+    pos, tok, ivs, lists, st = tree_tables(parent, lens)
+    tl = orc.tree_layout(parent, lens)
+    mask = orc.tree_visibility(tl)
+    T = tl.total_tokens
+    assert st.total_tokens == T and torch.equal(pos.to(torch.int64), tl.position_ids)
+    assert st.pairs == int(mask.sum()) and st.num_groups == sum(p < 0 for p in parent)
+    t_idx = torch.arange(T)
+    for w, bm in [(0, 64), (1, 128), (4, 256)]:
+        got = torch.zeros((T, T), dtype=torch.bool)
+        covered = torch.zeros(T, dtype=torch.int32)
+        for q0, q1, g0, p_end, s_lo, s_hi, a_off, a_cnt in lists[w].tolist():
+            assert 0 < q1 - q0 <= bm and a_cnt <= 6
+            covered[q0:q1] += 1
+            causal = [(g0, p_end)] + [tuple(ivs[a_off + i].tolist()) for i in range(a_cnt)]
+            for t in range(q0, q1):
+                for lo, hi in causal:
+                    got[t, lo:min(hi, t + 1)] = True
+                own = int(tok[t, 2])
+                got[t, max(s_lo, own):min(s_hi, t + 1)] = True
+        assert torch.equal(covered, torch.ones(T, dtype=torch.int32))
+        assert torch.equal(got, mask), bm
+    for w, bm in [(2, 64), (3, 128)]:
+        got = torch.zeros((T, T), dtype=torch.bool)
+        for k0, k1, q_lo, q_hi, g0, pe, _, _ in lists[w].tolist():
+            assert 0 < k1 - k0 <= bm
+            own = tok[:, 2]
+            for s in range(k0, k1):
+                vis = (t_idx >= s) & (t_idx < q_hi) & ((s < pe) | (own <= s))
+                got[:, s] |= vis
+        assert torch.equal(got, mask), bm
+
+
+def test_tree_layout_rejects_bad_trees():
+    with pytest.raises(_lib.PgError) as e:
+        api.pack_tree_size([-1, 0, -1, 1], [3, 2, 2, 1])     # node 3's parent is not on the path
+    assert e.value.status == _lib.PG_ERR_INVALID_ARG
+    with pytest.raises(_lib.PgError) as e:
+        api.pack_tree_size([-1, 2, 0], [3, 2, 2])            # parent listed after the child
+    assert e.value.status == _lib.PG_ERR_INVALID_ARG
+    with pytest.raises(_lib.PgError) as e:
+        api.pack_tree_size(list(range(-1, 8)), [4] * 9)      # depth 9
+    assert e.value.status == _lib.PG_ERR_UNSUPPORTED

@@ -320,3 +320,96 @@ def test_response_rows_single_response_is_textbook_causal_attention():
     rows = list(range(lp, lp + r))
     o, _ = orc.response_rows(lay, q, k, v, rows, theta=theta, q_heads=[1, 3])
     assert orc.normwise_error(o, o_ref[rows][:, [1, 3]]) < 1e-12
+
+
+# ---------------------------------------------------------------- nested prefixes (trees) ------
+
+TREES = [
+    # (parent, lens): depth-first preorder
+    ([-1, 0, 1, 1, 0, 4, 4, 4], [5, 3, 2, 4, 2, 1, 3, 2]),        # depth 3, two turns
+    ([-1, 0, 1, 2, 2, 0, -1, 6, 6], [4, 2, 3, 1, 2, 3, 3, 2, 0]),  # depth 4, two roots, empty leaf
+    ([-1, 0, 0, 2, 2, 2], [0, 3, 2, 2, 1, 3]),                     # empty root
+]
+
+
+def tree_problem(parent, lens, Hq, Hkv, d, seed):
+    tl = orc.tree_layout(parent, lens)
+    T = tl.total_tokens
+    return (tl, rand((T, Hq, d), seed), rand((T, Hkv, d), seed + 1), rand((T, Hkv, d), seed + 2),
+            rand((T, Hq, d), seed + 3))
+
+
+def test_two_level_tree_is_the_grouped_layout():
+    # A root with leaf children is exactly [P; R1; ...; RG]: same mask, positions and results.
+    lp, rs = 6, [3, 1, 4]
+    tl, q, k, v, do = tree_problem([-1, 0, 0, 0], [lp] + rs, 4, 2, 8, seed=151)
+    lay = orc.pack_layout([lp], [3], rs)
+    assert torch.equal(orc.tree_visibility(tl), orc.visibility_mask(lay))
+    assert torch.equal(tl.position_ids, lay.position_ids)
+    a = orc.tree_repeated(tl, q, k, v, do, theta=7.0)
+    b = orc.repeated_prefix(lay, q, k, v, do, theta=7.0)
+    for x, y in [(a.o, b.o), (a.lse, b.lse), (a.dq, b.dq), (a.dk, b.dk), (a.dv, b.dv)]:
+        assert orc.normwise_error(x, y) < 1e-12
+
+
+def test_chain_tree_is_one_causal_sequence():
+    # Each node the single child of the previous: one sequence, causal SDPA (complex-form RoPE).
+    theta = 20.0
+    tl, q, k, v, do = tree_problem([-1, 0, 1, 2], [3, 2, 4, 1], 2, 1, 8, seed=161)
+    pos = torch.arange(10)
+    assert torch.equal(tl.position_ids, pos)
+    res = orc.tree_repeated(tl, q, k, v, do, theta=theta)
+    qq, kk, vv = (t.clone().requires_grad_(True) for t in (q, k, v))
+    o = F.scaled_dot_product_attention(
+        rope_complex_diff(qq, pos, theta).transpose(0, 1)[None],
+        rope_complex_diff(kk, pos, theta).repeat_interleave(2, dim=1).transpose(0, 1)[None],
+        vv.repeat_interleave(2, dim=1).transpose(0, 1)[None], is_causal=True)[0].transpose(0, 1)
+    (o * do).sum().backward()
+    for a, b in [(res.o, o.detach()), (res.dq, qq.grad), (res.dk, kk.grad), (res.dv, vv.grad)]:
+        assert orc.normwise_error(a, b) < 1e-12
+
+
+@pytest.mark.parametrize("tree", TREES)
+def test_tree_paths_equal_tree_dense_mask(tree):
+    parent, lens = tree
+    tl, q, k, v, do = tree_problem(parent, lens, 4, 2, 8, seed=171)
+    a = orc.tree_repeated(tl, q, k, v, do, theta=11.0)
+    b = orc.tree_packed_dense(tl, q, k, v, do, theta=11.0)
+    for x, y in [(a.o, b.o), (a.lse, b.lse), (a.dq, b.dq), (a.dk, b.dk), (a.dv, b.dv)]:
+        assert orc.normwise_error(x, y) < 1e-12
+
+
+def test_tree_shared_turn_gradient_is_sum_over_paths():
+    # The gradient of a segment shared by several continuations is the sum over the paths, with
+    # the upstream gradient of every row counted once (in the first path through it).
+    parent, lens = TREES[0]
+    tl, q, k, v, do = tree_problem(parent, lens, 2, 2, 4, seed=181)
+    res = orc.tree_repeated(tl, q, k, v, do)
+    T = tl.total_tokens
+    dk_sum = torch.zeros((T, 2, 4), dtype=F64)
+    dv_sum = torch.zeros((T, 2, 4), dtype=F64)
+    seen = torch.zeros(T, dtype=torch.bool)
+    for path in orc.tree_paths(tl):
+        prow = torch.cat([torch.arange(tl.start[a], tl.end[a]) for a in path])
+        do_p = do[prow] * (~seen[prow]).to(F64)[:, None, None]
+        _, _, dk, dv = sdpa_reference(q[prow], k[prow], v[prow], do_p)
+        dk_sum[prow] += dk
+        dv_sum[prow] += dv
+        seen[prow] = True
+    assert orc.normwise_error(res.dk, dk_sum) < 1e-12
+    assert orc.normwise_error(res.dv, dv_sum) < 1e-12
+
+
+def test_tree_no_leakage_between_branches():
+    parent, lens = TREES[0]
+    tl, q, k, v, _ = tree_problem(parent, lens, 2, 1, 4, seed=191)
+    a = orc.tree_repeated(tl, q, k, v, theta=3.0)
+    sl = slice(tl.start[1], tl.end[3])                 # turn 1 and its two continuations
+    q2, k2, v2 = q.clone(), k.clone(), v.clone()
+    q2[sl] += 1.0
+    k2[sl] -= 2.0
+    v2[sl] *= 3.0
+    b = orc.tree_repeated(tl, q2, k2, v2, theta=3.0)
+    keep = [t for t in range(tl.total_tokens) if not (sl.start <= t < sl.stop)]
+    assert torch.equal(a.o[keep], b.o[keep]) and torch.equal(a.lse[:, keep], b.lse[:, keep])
+    assert not torch.equal(a.o[sl], b.o[sl])
