@@ -39,8 +39,8 @@ L2_BYTES = 129 * 2 ** 20
 # in profiles/attn_bwd_sm100_bf16_mha_h32_d128_p4096_g8_r512.md.  Reported only while the kernel
 # source still has the hash it had when the counters were taken, and only for that workload.
 TRAFFIC = {"file": "shared_prefix_grouped_gb300/csrc/pg_attn_bwd_sm100.cu",
-           "sha256": "75186b0ea5aeae2567c5377e8fceb01de2abb29e46ebc42cb41700f938e58d5d",
-           "workload": "bf16_mha_h32_d128_p4096_g8_r512", "bytes": 2653527944}
+           "sha256": "8fd0d0daffe89f032f1d4e5f702c80e2645f13d1d140fa16ade492ca6f4c1ef7",
+           "workload": "bf16_mha_h32_d128_p4096_g8_r512", "bytes": 662743040}
 
 
 def measured_traffic(workload: str):
@@ -273,19 +273,20 @@ class Step:
         self.o = torch.empty_like(self.q)
         self.lse = torch.empty((w.heads_q, prob.total_tokens), dtype=torch.float32, device=device)
         self.dq, self.dk, self.dv = (torch.empty_like(t) for t in (self.q, self.k, self.v))
-        opts = api.make_opts(w.rope_theta, 0.0, flags)
-        self.ws_f = api._workspace(api.workspace_size(self.layout, self.q.dtype, w.heads_q,
-                                                      w.heads_kv, w.head_dim, opts, 0), device)
-        self.ws_b = api._workspace(api.workspace_size(self.layout, self.q.dtype, w.heads_q,
-                                                      w.heads_kv, w.head_dim, opts, 1), device)
+        # One workspace for the step: the forward leaves the rotated q/k and the cos/sin table
+        # in it for the backward (PG_FLAG_KEEP_ROTATED), as a training step saves them.
+        self.flags = flags | _lib.PG_FLAG_KEEP_ROTATED
+        opts = api.make_opts(w.rope_theta, 0.0, self.flags)
+        self.ws = api._workspace(api.workspace_size(self.layout, self.q.dtype, w.heads_q,
+                                                    w.heads_kv, w.head_dim, opts, 1), device)
 
     def __call__(self):
         w = self.w
         api.grouped_attn_fwd(self.layout, self.q, self.k, self.v, rope_theta=w.rope_theta,
-                             flags=self.flags, out=self.o, lse=self.lse, workspace=self.ws_f)
+                             flags=self.flags, out=self.o, lse=self.lse, workspace=self.ws)
         api.grouped_attn_bwd(self.layout, self.q, self.k, self.v, self.o, self.lse, self.do,
                              rope_theta=w.rope_theta, flags=self.flags, dq=self.dq, dk=self.dk,
-                             dv=self.dv, workspace=self.ws_b)
+                             dv=self.dv, workspace=self.ws)
 
 
 def time_steps(step, n, device):

@@ -87,6 +87,16 @@ typedef struct pg_opts {
  */
 #define PG_FLAG_DETERMINISTIC 4u
 
+/*
+ * Rotate q and k once per training step instead of twice: with this flag pg_grouped_attn_fwd writes
+ * the RoPE-rotated q and k and the cos/sin table into its workspace, laid out as the backward's
+ * workspace (so it must be at least pg_workspace_size(..., phase 1) bytes), and
+ * pg_grouped_attn_bwd with the flag reads them from there instead of rotating again.  Pass the
+ * backward the same workspace, unmodified since the forward, with the same layout, q, k, heads and
+ * rope_theta.  Without RoPE the flag changes nothing.
+ */
+#define PG_FLAG_KEEP_ROTATED 8u
+
 /* Test hook for the bounded-wait error path: the tensor-core forward never signals that P is
  * ready, so its MMA thread's wait runs out (after 50 ms instead of 2 s), the kernel records
  * PG_ERR_TIMEOUT in the status word and exits cleanly; the outputs are then undefined. */

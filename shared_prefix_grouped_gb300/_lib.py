@@ -12,6 +12,7 @@ PG_F32, PG_BF16 = 0, 1
 PG_FLAG_SIMT = 1
 PG_FLAG_RESPONSES_ONLY = 2
 PG_FLAG_DETERMINISTIC = 4
+PG_FLAG_KEEP_ROTATED = 8
 
 
 class PgLayout(C.Structure):

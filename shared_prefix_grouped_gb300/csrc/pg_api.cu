@@ -847,7 +847,9 @@ pg_status pg_workspace_size(const pg_layout* layout, pg_dtype dtype, int32_t hea
   if (st != PG_OK) return st;
   bool rope = opts && opts->rope_theta > 0.f;
   const AttnArgs a = make_args(layout, dtype, heads_q, heads_kv, head_dim, opts, nullptr);
-  *bytes = ws_plan(layout, dtype, heads_q, heads_kv, head_dim, rope, phase, a).total;
+  // A forward that keeps its rotated q/k for the backward uses the backward's layout.
+  const int ph = (phase == 0 && rope && (a.flags & PG_FLAG_KEEP_ROTATED)) ? 1 : phase;
+  *bytes = ws_plan(layout, dtype, heads_q, heads_kv, head_dim, rope, ph, a).total;
   return PG_OK;
 }
 
@@ -862,7 +864,13 @@ pg_status pg_grouped_attn_fwd(const pg_layout* layout, pg_dtype dtype, int32_t h
   AttnArgs a = make_args(layout, dtype, heads_q, heads_kv, head_dim, opts,
                          reinterpret_cast<cudaStream_t>(stream));
   bool rope = a.theta > 0.f;
-  WsPlan w = ws_plan(layout, dtype, heads_q, heads_kv, head_dim, rope, 0, a);
+  const bool keep = rope && (a.flags & PG_FLAG_KEEP_ROTATED) != 0;
+  WsPlan w = ws_plan(layout, dtype, heads_q, heads_kv, head_dim, rope, keep ? 1 : 0, a);
+  if (keep && (a.flags & PG_FLAG_RESPONSES_ONLY)) {
+    set_error("%s: PG_FLAG_KEEP_ROTATED is for training steps, not with PG_FLAG_RESPONSES_ONLY",
+              who);
+    return PG_ERR_INVALID_ARG;
+  }
   if (w.total > 0 && (!workspace || workspace_bytes < w.total || !aligned16(workspace))) {
     set_error("%s: workspace must be 16-byte aligned and >= %zu bytes", who, w.total);
     return PG_ERR_INVALID_ARG;
@@ -887,8 +895,10 @@ pg_status pg_grouped_attn_fwd(const pg_layout* layout, pg_dtype dtype, int32_t h
     qx = ws + w.q_rot;
     kx = ws + w.k_rot;
   } else if (rope) {
+    // Keeping the rotation for the backward also stores the cos/sin table it rotates dK/dQ back
+    // with.
     st = launch_rope(a, q, ws + w.q_rot, heads_q, k, ws + w.k_rot, heads_kv, false, false,
-                     nullptr, nullptr);
+                     keep ? reinterpret_cast<float2*>(ws + w.rope_tab) : nullptr, nullptr);
     if (st != PG_OK) return st;
     qx = ws + w.q_rot;
     kx = ws + w.k_rot;
@@ -937,9 +947,12 @@ pg_status pg_grouped_attn_bwd(const pg_layout* layout, pg_dtype dtype, int32_t h
   const void* kx = k;
   float2* rope_tab = rope ? reinterpret_cast<float2*>(ws + w.rope_tab) : nullptr;
   if (rope) {
-    st = launch_rope(a, q, ws + w.q_rot, heads_q, k, ws + w.k_rot, heads_kv, false, false,
-                     rope_tab, nullptr);
-    if (st != PG_OK) return st;
+    // With PG_FLAG_KEEP_ROTATED the forward left the rotated q/k and the table here.
+    if (!(a.flags & PG_FLAG_KEEP_ROTATED)) {
+      st = launch_rope(a, q, ws + w.q_rot, heads_q, k, ws + w.k_rot, heads_kv, false, false,
+                       rope_tab, nullptr);
+      if (st != PG_OK) return st;
+    }
     qx = ws + w.q_rot;
     kx = ws + w.k_rot;
   }

@@ -265,3 +265,18 @@ def test_tree_layout_rejects_bad_trees():
     with pytest.raises(_lib.PgError) as e:
         api.pack_tree_size(list(range(-1, 8)), [4] * 9)      # depth 9
     assert e.value.status == _lib.PG_ERR_UNSUPPORTED
+
+
+def test_keep_rotated_forward_needs_the_backward_workspace():
+    _, tab, st = api.pack_host([300], [2], [40, 60])
+    L = _lib.lib()
+    n0, n1, nk = C.c_size_t(), C.c_size_t(), C.c_size_t()
+    plain = _lib.PgOpts(0.0, 1e4, 0, 0)
+    keep = _lib.PgOpts(0.0, 1e4, _lib.PG_FLAG_KEEP_ROTATED, 0)
+    assert L.pg_workspace_size(C.byref(st), _lib.PG_BF16, 4, 2, 128, C.byref(plain), 0,
+                               C.byref(n0)) == _lib.PG_OK
+    assert L.pg_workspace_size(C.byref(st), _lib.PG_BF16, 4, 2, 128, C.byref(plain), 1,
+                               C.byref(n1)) == _lib.PG_OK
+    assert L.pg_workspace_size(C.byref(st), _lib.PG_BF16, 4, 2, 128, C.byref(keep), 0,
+                               C.byref(nk)) == _lib.PG_OK
+    assert n0.value < n1.value == nk.value

@@ -195,3 +195,32 @@ def test_full_size_long_prefix():
     do_sum = prob.do.double().view(prob.total_tokens, w.heads_kv, rep, w.head_dim).sum(dim=(0, 2))
     dv_sum = got["dv"].double().sum(dim=0)
     assert orc.normwise_error(dv_sum, do_sum) <= tol
+
+
+@pytest.mark.parametrize("det", [False, True])
+def test_keep_rotated_reuses_the_forward_rotation(det):
+    # The forward leaves rotated q/k and the cos/sin table in a backward-sized workspace; the
+    # backward then skips its own rotation.  Same kernels on the same rotated values: results are
+    # bitwise those of the default call pair, and match the oracle.
+    w = workloads.small_variant(workloads.WORKLOADS[2], prefix_len=700,
+                                suffix_lens=[100, 300, 5, 260], heads_q=8, heads_kv=2)
+    prob = workloads.make_problem(w)
+    base = _lib.PG_FLAG_DETERMINISTIC if det else 0
+    ref = run_gpu(prob, flags=base)
+    dev = torch.device("cuda")
+    lay = api.pack(prob.prefix_lens, prob.group_sizes, prob.suffix_lens, dev)
+    q, k, v, do = (t.to(dev) for t in (prob.q, prob.k, prob.v, prob.do))
+    flags = base | _lib.PG_FLAG_KEEP_ROTATED
+    opts = api.make_opts(w.rope_theta, 0.0, flags)
+    ws = api._workspace(api.workspace_size(lay, q.dtype, w.heads_q, w.heads_kv, w.head_dim,
+                                           opts, 1), dev)
+    o, lse = api.grouped_attn_fwd(lay, q, k, v, rope_theta=w.rope_theta, flags=flags,
+                                  workspace=ws)
+    dq, dk, dv = api.grouped_attn_bwd(lay, q, k, v, o, lse, do, rope_theta=w.rope_theta,
+                                      flags=flags, workspace=ws)
+    torch.cuda.synchronize()
+    assert api.device_status() == 0
+    got = {n: t.float().cpu() for n, t in dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv).items()}
+    for n in ["o", "lse", "dk", "dv"] + (["dq"] if det else []):
+        assert torch.equal(got[n], ref[n]), n
+    compare(prob, got, TOL[w.dtype])
