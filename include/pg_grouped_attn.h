@@ -91,9 +91,11 @@ typedef struct pg_opts {
  * Rotate q and k once per training step instead of twice: with this flag pg_grouped_attn_fwd writes
  * the RoPE-rotated q and k and the cos/sin table into its workspace, laid out as the backward's
  * workspace (so it must be at least pg_workspace_size(..., phase 1) bytes), and
- * pg_grouped_attn_bwd with the flag reads them from there instead of rotating again.  Pass the
- * backward the same workspace, unmodified since the forward, with the same layout, q, k, heads and
- * rope_theta.  Without RoPE the flag changes nothing.
+ * pg_grouped_attn_bwd with the flag reads them from there instead of rotating again.  On the bf16
+ * tensor-core path the forward also leaves the backward its log2-domain LSE rows.  Pass the
+ * backward the same
+ * workspace, unmodified since the forward, with the same layout, q, k, heads, rope_theta and flags.
+ * Without RoPE the flag changes nothing.
  */
 #define PG_FLAG_KEEP_ROTATED 8u
 

@@ -912,7 +912,10 @@ pg_status pg_grouped_attn_fwd(const pg_layout* layout, pg_dtype dtype, int32_t h
     else
       st = launch_fwd_simt(a, qx, kx, v, o, lse);
   } else if (!(a.flags & PG_FLAG_SIMT) && fwd_sm100_supported(a)) {
-    st = launch_fwd_sm100(a, qx, kx, v, o, lse);
+    // Keeping the workspace for the backward: also leave it the log2-domain LSE rows.
+    float* lse2_out = keep && bwd_sm100_supported(a) ? reinterpret_cast<float*>(ws + w.lse2)
+                                                     : nullptr;
+    st = launch_fwd_sm100(a, qx, kx, v, o, lse, lse2_out);
   } else {
     st = launch_fwd_simt(a, qx, kx, v, o, lse);
   }
@@ -960,7 +963,10 @@ pg_status pg_grouped_attn_bwd(const pg_layout* layout, pg_dtype dtype, int32_t h
   float* lse2 = reinterpret_cast<float*>(ws + w.lse2);
   float* dq_acc = w.dq_acc == SIZE_MAX ? nullptr : reinterpret_cast<float*>(ws + w.dq_acc);
   float* dk_acc = w.dk_acc == SIZE_MAX ? nullptr : reinterpret_cast<float*>(ws + w.dk_acc);
-  st = launch_bwd_preprocess(a, o, dO, lse, Dbuf, lse2, dq_acc);
+  // With PG_FLAG_KEEP_ROTATED the tensor-core forward already wrote LSE_2.
+  const bool prepared = rope && (a.flags & PG_FLAG_KEEP_ROTATED) && !(a.flags & PG_FLAG_SIMT) &&
+                        bwd_sm100_supported(a) && fwd_sm100_supported(a);
+  st = launch_bwd_preprocess(a, o, dO, lse, Dbuf, lse2, dq_acc, prepared);
   if (st != PG_OK) return st;
   if (!(a.flags & PG_FLAG_SIMT) && bwd_sm100_supported(a)) {
     // dK (inverse-rotated, cast) and dV are written by the key-major kernel itself.  dQ either

@@ -122,8 +122,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ o,
                       float* __restrict__ lse, const int4* __restrict__ tok,
-                      const FwdTile* __restrict__ tiles, const int2* __restrict__ ivs, int Hq,
-                      int Hkv, int Ttot,
+                      const FwdTile* __restrict__ tiles, const int2* __restrict__ ivs,
+                      float* __restrict__ lse2_out, int64_t ldl, int Hq, int Hkv, int Ttot,
                       float scale_log2, uint64_t wait_ns, uint32_t debug) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -419,7 +419,12 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
           }
         }
       }
-      if (valid) lse[(size_t)h * Ttot + row] = (m_used + log2f(l)) * kLn2;
+      if (valid) {
+        const float lse_row = (m_used + log2f(l)) * kLn2;
+        lse[(size_t)h * Ttot + row] = lse_row;
+        // the backward's log2-domain copy, rounded exactly as the preprocess would
+        if (lse2_out) lse2_out[(size_t)h * ldl + row] = lse_row * kLog2e;
+      }
     } else if (active && c > 0) {
       ok = false;
     }
@@ -438,7 +443,7 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
 bool fwd_sm100_supported(const AttnArgs& a) { return a.dtype == PG_BF16 && a.d == 128; }
 
 pg_status launch_fwd_sm100(const AttnArgs& a, const void* q, const void* k, const void* v, void* o,
-                           float* lse) {
+                           float* lse, float* lse2_out) {
   const pg_layout* L = a.layout;
   const int64_t T = L->total_tokens;
   CUtensorMap tq, tk, tv;
@@ -457,7 +462,7 @@ pg_status launch_fwd_sm100(const AttnArgs& a, const void* q, const void* k, cons
   prof_begin(PG_KERNEL_ATTN_FWD, a.stream);
   attn_fwd_sm100_kernel<<<(unsigned)(L->n_tiles[FWD256] * a.Hq), NTHREADS, smem, a.stream>>>(
       tq, tk, tv, static_cast<__nv_bfloat16*>(o), lse, tokens(L), tiles<FwdTile>(L, FWD256),
-      intervals(L), a.Hq, a.Hkv, (int)T, a.scale * kLog2e, wait_ns, a.debug);
+      intervals(L), lse2_out, padded_tokens(L), a.Hq, a.Hkv, (int)T, a.scale * kLog2e, wait_ns, a.debug);
   prof_end(PG_KERNEL_ATTN_FWD, a.stream);
   return cuda_check(cudaGetLastError(), "fwd sm100 launch");
 }

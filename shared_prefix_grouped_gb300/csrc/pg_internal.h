@@ -147,8 +147,10 @@ pg_status read_status_bwd_sm100(bool clear, int32_t* code);
 
 // Tensor-core kernels (pg_attn_*_sm100.cu).
 bool fwd_sm100_supported(const AttnArgs& a);
+// lse2_out ([Hq][padded T], log2 units) is optional: a forward whose workspace the backward
+// reuses writes the backward's copy of the LSE rows.
 pg_status launch_fwd_sm100(const AttnArgs& a, const void* q, const void* k, const void* v, void* o,
-                           float* lse);
+                           float* lse, float* lse2_out = nullptr);
 bool bwd_sm100_supported(const AttnArgs& a);
 // dq_acc == nullptr: dK and dV only.
 pg_status launch_bwd_sm100(const AttnArgs& a, const void* q, const void* k, const void* v,
@@ -199,8 +201,8 @@ pg_status launch_bwd_simt(const AttnArgs& a, const void* q, const void* k, const
 // and, with lse, set lse[h][row] = +inf on them.
 pg_status launch_pad_fill(const AttnArgs& a, void* x0, int heads0, void* x1, int heads1, void* x2,
                           int heads2, float* lse);
-// dq_acc may be nullptr (nothing to zero).
+// dq_acc may be nullptr (nothing to zero); lse2_ready: the forward already wrote lse2's rows.
 pg_status launch_bwd_preprocess(const AttnArgs& a, const void* o, const void* dO, const float* lse,
-                                float* Dbuf, float* lse2, float* dq_acc);
+                                float* Dbuf, float* lse2, float* dq_acc, bool lse2_ready = false);
 
 }  // namespace pg

@@ -295,34 +295,45 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
 // One warp per (t, h).
 // ---------------------------------------------------------------------------------------------
 template <typename T>
-__global__ void bwd_pre_kernel(const T* __restrict__ o, const T* __restrict__ dO,
-                               const float* __restrict__ lse, float* __restrict__ Dbuf,
-                               float* __restrict__ lse2, float* __restrict__ dq_acc, int Hq, int D,
-                               int Ttot, int ldd) {
+__global__ void __launch_bounds__(256)
+bwd_pre_kernel(const T* __restrict__ o, const T* __restrict__ dO, const float* __restrict__ lse,
+               float* __restrict__ Dbuf, float* __restrict__ lse2, float* __restrict__ dq_acc,
+               int Hq, int D, int Ttot, int ldd, int lse2_ready) {
+  // D / 8 lanes per (t, h) row, 8 elements each (16-byte loads of bf16), so a warp covers 2 or 4
+  // rows with every load in flight at once.
+  const int lpr = D >> 3;                        // lanes per row
   const int lane = threadIdx.x & 31;
-  const size_t warp = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (warp >= (size_t)ldd * Hq) return;
-  const int t = (int)(warp / Hq), h = (int)(warp % Hq);
-  if (t >= Ttot) {
-    if (lane == 0) {
-      Dbuf[(size_t)h * ldd + t] = 0.f;
-      lse2[(size_t)h * ldd + t] = 0.f;
-    }
-    return;
-  }
-  const size_t base = ((size_t)t * Hq + h) * D;
+  const size_t gthread = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t row = gthread / lpr;              // over ldd * Hq rows, t-major
+  const int sub = (int)(gthread % lpr);
+  const bool in = row < (size_t)ldd * Hq;
+  const int t = in ? (int)(row / Hq) : 0, h = in ? (int)(row % Hq) : 0;
   float acc = 0.f;
-  for (int c = lane * 4; c < D; c += 128) {
-    float4 a = Vec<T>::load4(o + base + c), b = Vec<T>::load4(dO + base + c);
-    acc += dot4(a, b);
-    if (dq_acc) *reinterpret_cast<float4*>(dq_acc + base + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
+  if (in && t < Ttot) {
+    const size_t base = ((size_t)t * Hq + h) * D + 8 * sub;
+    float a[8], b[8];
+    Vec<T>::load8(o + base, a);
+    Vec<T>::load8(dO + base, b);
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) {
-    Dbuf[(size_t)h * ldd + t] = acc;
-    lse2[(size_t)h * ldd + t] = lse[(size_t)h * Ttot + t] * kLog2e;
+    for (int e = 0; e < 8; ++e) acc = fmaf(a[e], b[e], acc);
+    if (dq_acc) {
+      float4* z = reinterpret_cast<float4*>(dq_acc + base);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
+  for (int off = lpr >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (in && sub == 0) {
+    const size_t idx = (size_t)h * ldd + t;
+    if (t >= Ttot) {                             // padding rows of the fp32 row buffers
+      Dbuf[idx] = 0.f;
+      lse2[idx] = 0.f;
+    } else {
+      Dbuf[idx] = acc;
+      if (!lse2_ready) lse2[idx] = lse[(size_t)h * Ttot + t] * kLog2e;
+    }
+  }
+  (void)lane;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -682,20 +693,20 @@ pg_status launch_fwd_simt(const AttnArgs& a, const void* q, const void* k, const
 }
 
 pg_status launch_bwd_preprocess(const AttnArgs& a, const void* o, const void* dO, const float* lse,
-                                float* Dbuf, float* lse2, float* dq_acc) {
+                                float* Dbuf, float* lse2, float* dq_acc, bool lse2_ready) {
   const int T = (int)a.layout->total_tokens;
   const int ldd = (int)padded_tokens(a.layout);
-  const size_t warps = (size_t)ldd * a.Hq;
-  const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
+  const size_t threads = (size_t)ldd * a.Hq * (a.d / 8);
+  const unsigned blocks = (unsigned)((threads + 255) / 256);
   prof_begin(PG_KERNEL_BWD_PREPROCESS, a.stream);
   if (a.dtype == PG_F32)
     bwd_pre_kernel<float><<<blocks, 256, 0, a.stream>>>(
         static_cast<const float*>(o), static_cast<const float*>(dO), lse, Dbuf, lse2, dq_acc,
-        a.Hq, a.d, T, ldd);
+        a.Hq, a.d, T, ldd, lse2_ready ? 1 : 0);
   else
     bwd_pre_kernel<__nv_bfloat16><<<blocks, 256, 0, a.stream>>>(
         static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, Dbuf,
-        lse2, dq_acc, a.Hq, a.d, T, ldd);
+        lse2, dq_acc, a.Hq, a.d, T, ldd, lse2_ready ? 1 : 0);
   prof_end(PG_KERNEL_BWD_PREPROCESS, a.stream);
   return cuda_check(cudaGetLastError(), "bwd preprocess launch");
 }
