@@ -280,3 +280,14 @@ def test_keep_rotated_forward_needs_the_backward_workspace():
     assert L.pg_workspace_size(C.byref(st), _lib.PG_BF16, 4, 2, 128, C.byref(keep), 0,
                                C.byref(nk)) == _lib.PG_OK
     assert n0.value < n1.value == nk.value
+
+
+def test_responses_only_refuses_nested_layouts():
+    # Scoring needs a two-level layout; a depth-3 tree is refused on the host, before any launch.
+    _, tab, st = api.pack_tree_host([-1, 0, 1], [8, 4, 2])
+    L = _lib.lib()
+    buf = torch.empty(1 << 16, dtype=torch.uint8)
+    p = C.c_void_p(buf.data_ptr())
+    ro = _lib.PgOpts(0.0, 0.0, _lib.PG_FLAG_RESPONSES_ONLY, 0)
+    assert L.pg_grouped_attn_fwd(C.byref(st), _lib.PG_BF16, 2, 1, 128, p, p, p, p, p, C.byref(ro),
+                                 p, 1 << 16, None) == _lib.PG_ERR_UNSUPPORTED
