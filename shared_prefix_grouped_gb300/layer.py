@@ -15,7 +15,7 @@ import dataclasses
 
 import torch
 
-from . import api
+from . import _lib, api
 
 
 @dataclasses.dataclass
@@ -44,15 +44,21 @@ def layer_fwd(layout: api.Layout, x, w_qkv, w_o, w_gu, w_d, g1, g2, *, heads_q, 
     q = api.gemm_bf16(h1, wq, out_dtype=bf)
     k = api.gemm_bf16(h1, wk, out_dtype=bf)
     v = api.gemm_bf16(h1, wv, out_dtype=bf)
+    # One attention workspace for the step: the forward leaves the rotated q/k, the cos/sin table
+    # and its log2-domain LSE there for the backward (PG_FLAG_KEEP_ROTATED).
+    keep = _lib.PG_FLAG_KEEP_ROTATED
+    ws = api._workspace(api.workspace_size(layout, bf, Hq, Hkv, d,
+                                           api.make_opts(rope_theta, 0.0, keep), 1), x.device)
     o, lse = api.grouped_attn_fwd(layout, q.view(T, Hq, d), k.view(T, Hkv, d), v.view(T, Hkv, d),
-                                  rope_theta=rope_theta)
+                                  rope_theta=rope_theta, flags=keep, workspace=ws)
     a = api.gemm_bf16(o.view(T, Hq * d), w_o, out_dtype=bf)
     h2, x2, r2 = api.rmsnorm_fwd(x, g2, eps, residual=a)
     gu = api.gemm_bf16(h2, w_gu, out_dtype=bf)
     act = api.swiglu_fwd(gu)
     y = x2.clone()
     api.gemm_bf16(act, w_d, out=y, accumulate=True)
-    saved = dict(h1=h1, r1=r1, q=q, k=k, v=v, o=o, lse=lse, x2=x2, h2=h2, r2=r2, gu=gu, act=act)
+    saved = dict(h1=h1, r1=r1, q=q, k=k, v=v, o=o, lse=lse, x2=x2, h2=h2, r2=r2, gu=gu, act=act,
+                 attn_ws=ws)
     return y, saved
 
 
@@ -74,7 +80,8 @@ def layer_bwd(layout: api.Layout, x, w_qkv, w_o, w_gu, w_d, g1, g2, saved, dy, *
     dw_o = api.gemm_bf16(dx2, o2, a_mn=True, b_mn=True, out_dtype=f32)
     dq, dk, dv = api.grouped_attn_bwd(layout, s["q"].view(T, Hq, d), s["k"].view(T, Hkv, d),
                                       s["v"].view(T, Hkv, d), s["o"], s["lse"],
-                                      do.view(T, Hq, d), rope_theta=rope_theta)
+                                      do.view(T, Hq, d), rope_theta=rope_theta,
+                                      flags=_lib.PG_FLAG_KEEP_ROTATED, workspace=s["attn_ws"])
     dq, dk, dv = dq.view(T, Hq * d), dk.view(T, Hkv * d), dv.view(T, Hkv * d)
     dh1 = api.gemm_bf16(dq, wq, b_mn=True, out_dtype=f32)
     api.gemm_bf16(dk, wk, b_mn=True, out=dh1, accumulate=True)
