@@ -87,10 +87,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 __device__ __forceinline__ void fail(int code) { atomicCAS(&s_status_bwd, 0, code); }
 
-__device__ __forceinline__ void red_add(float* p, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
-}
-
 template <bool kDQ>
 __global__ void __launch_bounds__(nthreads(kDQ), 1)
 attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,

@@ -461,62 +461,85 @@ attn_score_sm100_kernel(const __grid_constant__ CUtensorMap tq,
   }
 }
 
-// Merge of the splits: one warp per query row of a CTA slot; lane l owns dims [4 l, 4 l + 4).
+// Merge of the splits: four warps per query row of a CTA slot (a block of 256 threads takes two
+// rows); warp w of a row accumulates splits w, w + 4, ..., lane l owns dims [4 l, 4 l + 4), and the
+// four partial sums meet in shared memory.
 // O = sum_c 2^(lse_c - M) O_c / sum_c 2^(lse_c - M), LSE = (M + log2 sum_c 2^(lse_c - M)) ln 2,
-// with M the largest split LSE; splits that saw no key (LSE -inf) drop out.  The split LSEs are
-// read by the lanes in parallel (split c by lane c % 32), the weights reach every lane by shuffle,
-// and the split rows are accumulated four at a time so their loads overlap.
+// with M the largest split LSE; splits that saw no key (LSE -inf) drop out.  Every warp of a row
+// reads all split LSEs (split c by lane c % 32) and forms M and the weights itself.
+constexpr int kMergeWarpsPerRow = 4;
+
 __global__ void __launch_bounds__(256)
 score_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
                      __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
                      const FwdTile* __restrict__ spans, int Hq, int Hkv, int hp, int TB, int nrb,
                      int nsplit, int nblk, int Ttot) {
-  const int lane = threadIdx.x & 31;
-  const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (row >= (int64_t)nblk * ROWS) return;
-  const int blk = (int)(row / ROWS), m = (int)(row % ROWS);
-  const int rb = blk % nrb;
-  const int kh = (blk / nrb) % Hkv;
-  const FwdTile sp = spans[blk / nrb / Hkv];
-  const int t0 = sp.q0 + rb * TB;
-  if (t0 >= sp.q1) return;
-  const int t_end = min(t0 + TB, sp.q1);
-  if (m >= (t_end - t0) * hp) return;
-  const int t = t0 + m / hp, h = kh * hp + m % hp;
-  // nsplit <= 64: lane l holds the LSEs of splits l and l + 32.
+  __shared__ float4 red[2][kMergeWarpsPerRow][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int rl = warp / kMergeWarpsPerRow, wr = warp % kMergeWarpsPerRow;   // row in block, part
+  const int64_t row = (int64_t)blockIdx.x * 2 + rl;
+  bool valid = row < (int64_t)nblk * ROWS;
+  int blk = 0, m = 0, t = 0, h = 0;
+  if (valid) {
+    blk = (int)(row / ROWS);
+    m = (int)(row % ROWS);
+    const int rb = blk % nrb;
+    const int kh = (blk / nrb) % Hkv;
+    const FwdTile sp = spans[blk / nrb / Hkv];
+    const int t0 = sp.q0 + rb * TB;
+    valid = t0 < sp.q1 && m < (min(t0 + TB, sp.q1) - t0) * hp;
+    t = t0 + m / hp;
+    h = kh * hp + m % hp;
+  }
   const size_t stride = (size_t)nblk * ROWS;
-  const float* pl = part_lse + (size_t)blk * ROWS + m;
-  const float la = lane < nsplit ? pl[lane * stride] : -INFINITY;
-  const float lb = lane + 32 < nsplit ? pl[(lane + 32) * stride] : -INFINITY;
-  float M = fmaxf(la, lb);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  const float wa = M == -INFINITY ? 0.f : exp2f(la - M);     // exp2(-inf) = 0 for empty splits
-  const float wb = M == -INFINITY ? 0.f : exp2f(lb - M);
-  float W = wa + wb;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
-  const float* po = part_o + ((size_t)blk * ROWS + m) * D + 4 * lane;
-  const size_t ostride = stride * D;
+  float M = -INFINITY, wa = 0.f, wb = 0.f, W = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c0 = 0; c0 < nsplit; c0 += 4) {
-    float w[4];
-    float4 v[4];
+  if (valid) {    // uniform per warp
+    // nsplit <= 64: lane l holds the LSEs of splits l and l + 32.
+    const float* pl = part_lse + (size_t)blk * ROWS + m;
+    const float la = lane < nsplit ? pl[lane * stride] : -INFINITY;
+    const float lb = lane + 32 < nsplit ? pl[(lane + 32) * stride] : -INFINITY;
+    M = fmaxf(la, lb);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int c = c0 + u;
-      const float wc = __shfl_sync(0xffffffffu, c < 32 ? wa : wb, c & 31);
-      w[u] = c < nsplit ? wc : 0.f;
-      v[u] = (c < nsplit && w[u] > 0.f) ? *reinterpret_cast<const float4*>(po + c * ostride)
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    wa = M == -INFINITY ? 0.f : exp2f(la - M);     // exp2(-inf) = 0 for empty splits
+    wb = M == -INFINITY ? 0.f : exp2f(lb - M);
+    W = wa + wb;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      acc.x = fmaf(w[u], v[u].x, acc.x);
-      acc.y = fmaf(w[u], v[u].y, acc.y);
-      acc.z = fmaf(w[u], v[u].z, acc.z);
-      acc.w = fmaf(w[u], v[u].w, acc.w);
+    for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+    const float* po = part_o + ((size_t)blk * ROWS + m) * D + 4 * lane;
+    const size_t ostride = stride * D;
+    for (int c0 = wr; c0 < nsplit; c0 += 4 * kMergeWarpsPerRow) {
+      float w[4];
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = c0 + u * kMergeWarpsPerRow;
+        const int cc = c < nsplit ? c : 0;
+        const float wc = __shfl_sync(0xffffffffu, cc < 32 ? wa : wb, cc & 31);
+        w[u] = c < nsplit ? wc : 0.f;
+        v[u] = w[u] > 0.f ? *reinterpret_cast<const float4*>(po + (size_t)c * ostride)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        acc.x = fmaf(w[u], v[u].x, acc.x);
+        acc.y = fmaf(w[u], v[u].y, acc.y);
+        acc.z = fmaf(w[u], v[u].z, acc.z);
+        acc.w = fmaf(w[u], v[u].w, acc.w);
+      }
     }
+  }
+  red[rl][wr][lane] = acc;
+  __syncthreads();
+  if (!valid || wr != 0) return;
+#pragma unroll
+  for (int i = 1; i < kMergeWarpsPerRow; ++i) {
+    const float4 x = red[rl][i][lane];
+    acc.x += x.x;
+    acc.y += x.y;
+    acc.z += x.z;
+    acc.w += x.w;
   }
   const float inv = W > 0.f ? 1.f / W : 0.f;
   uint2 packed;
@@ -579,9 +602,9 @@ pg_status launch_score_sm100(const AttnArgs& a, const void* q, const void* k, co
   prof_end(PG_KERNEL_ATTN_FWD, a.stream);
   st = cuda_check(cudaGetLastError(), "score sm100 launch");
   if (st != PG_OK || p.nsplit == 1) return st;
-  const int64_t warps = p.nblk * ROWS;
+  const int64_t rows = p.nblk * ROWS;
   prof_begin(PG_KERNEL_SCORE_COMBINE, a.stream);
-  score_combine_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, a.stream>>>(
+  score_combine_kernel<<<(unsigned)((rows + 1) / 2), 256, 0, a.stream>>>(
       part_o, part_lse, static_cast<__nv_bfloat16*>(o), lse, tiles<FwdTile>(L, SPANS), a.Hq,
       a.Hkv, p.hp, p.TB, p.nrb, p.nsplit, (int)p.nblk, (int)T);
   prof_end(PG_KERNEL_SCORE_COMBINE, a.stream);

@@ -197,15 +197,18 @@ def test_full_size_long_prefix():
     assert orc.normwise_error(dv_sum, do_sum) <= tol
 
 
-@pytest.mark.parametrize("det", [False, True])
-def test_keep_rotated_reuses_the_forward_rotation(det):
+@pytest.mark.parametrize("path", ["default", "det", "simt", "f32"])
+def test_keep_rotated_reuses_the_forward_rotation(path):
     # The forward leaves rotated q/k and the cos/sin table in a backward-sized workspace; the
     # backward then skips its own rotation.  Same kernels on the same rotated values: results are
     # bitwise those of the default call pair, and match the oracle.
-    w = workloads.small_variant(workloads.WORKLOADS[2], prefix_len=700,
+    det = path == "det"
+    w = workloads.small_variant(workloads.WORKLOADS[0 if path == "f32" else 2], prefix_len=700,
                                 suffix_lens=[100, 300, 5, 260], heads_q=8, heads_kv=2)
+    w = workloads.dataclasses.replace(w, rope_theta=1e4)
     prob = workloads.make_problem(w)
-    base = _lib.PG_FLAG_DETERMINISTIC if det else 0
+    base = {"default": 0, "det": _lib.PG_FLAG_DETERMINISTIC, "simt": _lib.PG_FLAG_SIMT,
+            "f32": 0}[path]
     ref = run_gpu(prob, flags=base)
     dev = torch.device("cuda")
     lay = api.pack(prob.prefix_lens, prob.group_sizes, prob.suffix_lens, dev)
@@ -221,6 +224,7 @@ def test_keep_rotated_reuses_the_forward_rotation(det):
     torch.cuda.synchronize()
     assert api.device_status() == 0
     got = {n: t.float().cpu() for n, t in dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv).items()}
-    for n in ["o", "lse", "dk", "dv"] + (["dq"] if det else []):
+    # the SIMT and fp32 paths are deterministic too
+    for n in ["o", "lse", "dk", "dv"] + (["dq"] if path != "default" else []):
         assert torch.equal(got[n], ref[n]), n
     compare(prob, got, TOL[w.dtype])

@@ -92,3 +92,24 @@ def test_tree_workload_sampled():
     prob = workloads.make_tree_problem(w)
     got = run_tree(prob, 0)
     check(prob, got, TOL["bf16"])
+
+
+def test_tree_keep_rotated_deterministic():
+    # A nested layout through the training-step options: one workspace, deterministic backward.
+    parent, lens = workloads.multi_turn(600, 3, 150, 2, 100)
+    w = workloads.TreeWorkload("tree_keep", "bf16", parent, lens, 8, 2, 128, rope_theta=1e4)
+    prob = workloads.make_tree_problem(w)
+    dev = torch.device("cuda")
+    lay = api.pack_tree(w.parent, w.lens, dev)
+    flags = _lib.PG_FLAG_DETERMINISTIC | _lib.PG_FLAG_KEEP_ROTATED
+    q, k, v, do = (t.to(dev) for t in (prob.q, prob.k, prob.v, prob.do))
+    ws = api._workspace(api.workspace_size(lay, q.dtype, 8, 2, 128,
+                                           api.make_opts(w.rope_theta, 0.0, flags), 1), dev)
+    o, lse = api.grouped_attn_fwd(lay, q, k, v, rope_theta=w.rope_theta, flags=flags,
+                                  workspace=ws)
+    dq, dk, dv = api.grouped_attn_bwd(lay, q, k, v, o, lse, do, rope_theta=w.rope_theta,
+                                      flags=flags, workspace=ws)
+    torch.cuda.synchronize()
+    assert api.device_status() == 0
+    got = {n: t.float().cpu() for n, t in dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv).items()}
+    check(prob, got, TOL["bf16"])
