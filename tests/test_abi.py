@@ -291,3 +291,12 @@ def test_responses_only_refuses_nested_layouts():
     ro = _lib.PgOpts(0.0, 0.0, _lib.PG_FLAG_RESPONSES_ONLY, 0)
     assert L.pg_grouped_attn_fwd(C.byref(st), _lib.PG_BF16, 2, 1, 128, p, p, p, p, p, C.byref(ro),
                                  p, 1 << 16, None) == _lib.PG_ERR_UNSUPPORTED
+
+
+def test_tree_packing_matches_hand_fixture():
+    import json
+    fx = json.load(open(os.path.join(ROOT, "tests", "golden", "pack_tree_small.json")))
+    pos, tok, ivs, lists, st = tree_tables(fx["parent"], fx["seg_lens"])
+    assert st.total_tokens == fx["total_tokens"] and st.pairs == fx["grouped_pairs"]
+    assert pos.tolist() == fx["position_ids"]
+    assert st.max_depth == 3

@@ -413,3 +413,18 @@ def test_tree_no_leakage_between_branches():
     keep = [t for t in range(tl.total_tokens) if not (sl.start <= t < sl.stop)]
     assert torch.equal(a.o[keep], b.o[keep]) and torch.equal(a.lse[:, keep], b.lse[:, keep])
     assert not torch.equal(a.o[sl], b.o[sl])
+
+
+def test_tree_layout_matches_hand_fixture():
+    fx = json.load(open(os.path.join(GOLDEN, "pack_tree_small.json")))
+    tl = orc.tree_layout(fx["parent"], fx["seg_lens"])
+    assert tl.total_tokens == fx["total_tokens"]
+    assert tl.position_ids.tolist() == fx["position_ids"]
+    mask = orc.tree_visibility(tl)
+    assert [mask[t].nonzero().flatten().tolist() for t in range(tl.total_tokens)] == \
+        fx["visible_keys"]
+    assert int(mask.sum()) == fx["grouped_pairs"]
+    assert orc.tree_paths(tl) == fx["paths"]
+    lens = fx["seg_lens"]
+    assert sum(n * (n + 1) // 2 for n in (sum(lens[a] for a in p) for p in fx["paths"])) == \
+        fx["repeated_pairs"]
