@@ -886,11 +886,8 @@ pg_status pg_grouped_attn_fwd(const pg_layout* layout, pg_dtype dtype, int32_t h
   }
   if (rope && responses_only) {
     // Every key is rotated; of q only the response rows, the only ones read.
-    st = launch_rope(a, k, ws + w.k_rot, heads_kv, nullptr, nullptr, 0, false, false, nullptr,
-                     nullptr);
-    if (st == PG_OK)
-      st = launch_rope(a, q, ws + w.q_rot, heads_q, nullptr, nullptr, 0, false, false, nullptr,
-                       nullptr, true);
+    st = launch_rope(a, k, ws + w.k_rot, heads_kv, q, ws + w.q_rot, heads_q, false, false,
+                     nullptr, nullptr, RopeRows::kAllThenResponses);
     if (st != PG_OK) return st;
     qx = ws + w.q_rot;
     kx = ws + w.k_rot;

@@ -24,18 +24,21 @@
 //          warp stages its 32 head dims of the block, 32 query rows at a time ([32 x 32] fp32),
 //          in its own shared-memory buffer and adds them into the global dQ accumulator with TMA
 //          bulk reduce-adds.
-// The MMA thread issues S^T / dP^T of block i before the gradient products of block i-1, so the
-// tensor core computes the next scores while the softmax warps work on the current ones.
+// Two threads issue the MMAs: one the score products S^T / dP^T, the other the gradient products
+// dV, dK (and dQ^T) of each block as soon as its P^T / dS^T are ready, so the next block's scores
+// never queue behind the previous block's gradient waits and the tensor core computes them while
+// the softmax warps work on the current ones.
 // The epilogue applies the softmax scale and the inverse RoPE rotation to dK in registers (a
 // thread holds a whole key row, so each (k, k + d/2) pair is local; cos/sin come from the table
 // the RoPE pass of the same call wrote) and writes dK, dV in bf16.
 //
-// Warps: 0 TMA producer, 1 TMEM allocation and MMA issue, 2..9 softmax (key rows; two
-// warpgroups split the 64 query columns), 10..13 dQ drain.  Every mbarrier wait is bounded.
+// Warps: 0 TMA producer, 1 TMEM allocation and the score MMAs, 2..9 softmax (key rows; two
+// warpgroups split the 64 query columns), 10..13 dQ drain, 14 the gradient MMAs.  Every mbarrier
+// wait is bounded.
 //
 // Instantiated twice: with dQ as above, and without it (kDQ = false: no dQ^T product, no dS^T in
-// shared memory, no drain warps) for the deterministic backward, whose dQ comes from the
-// query-major kernel in pg_attn_dq_sm100.cu.
+// shared memory, no drain warps; warp 10 issues the gradient MMAs) for the deterministic
+// backward, whose dQ comes from the query-major kernel in pg_attn_dq_sm100.cu.
 #include <limits.h>
 #include <math.h>
 #include <string.h>
@@ -57,8 +60,10 @@ constexpr int NSQ = 3;          // Q / dO stages
 constexpr int PREFETCH = 2;     // Q / dO blocks fetched into L2 this far ahead of their load
 constexpr uint32_t KHALF = BKV * 64 * 2;   // 16 KiB: [128 rows][64 cols] bf16
 constexpr uint32_t QHALF = BQ * 64 * 2;    // 8 KiB:  [64 rows][64 cols] bf16
-// With dQ: warps 10..13 drain dQ.  Without: warp 10 is a second MMA-issuing thread (dV, dK).
-constexpr int nthreads(bool with_dq) { return with_dq ? 448 : 352; }
+// With dQ: warps 10..13 drain dQ and warp 14 issues the gradient MMAs (dV, dK, dQ^T).  Without:
+// warp 10 issues them (dV, dK).
+constexpr int nthreads(bool with_dq) { return with_dq ? 480 : 352; }
+constexpr int grad_warp(bool with_dq) { return with_dq ? 14 : 10; }
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ int s_status_bwd = 0;
@@ -197,68 +202,34 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer -------
+    // ------------------------------------------------------------------ score MMAs -------
     if (elect_one()) {
       constexpr uint32_t id_s = idesc_bf16(BKV, BQ, 0, 0);     // S^T, dP^T
-      constexpr uint32_t id_g = idesc_bf16(BKV, D, 0, 1);      // dV, dK
-      constexpr uint32_t id_q = idesc_bf16(D, BQ, 1, 1);       // dQ^T
-      // Descriptor bases (K-major use: LBO unused; MN-major use: LBO = the 64-column half).
+      // Descriptor bases (K-major operands: LBO unused).
       const uint64_t kd = sdesc_sw128(smem_u32(sm.k), 16, 1024);
       const uint64_t vd = sdesc_sw128(smem_u32(sm.v), 16, 1024);
-      const uint64_t kmn = sdesc_sw128(smem_u32(sm.k), KHALF, 1024);
-      const uint64_t dsmn = sdesc_sw128(smem_u32(sm.ds), QHALF, 1024);
       const uint64_t qd0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
       const uint64_t dod0 = sdesc_sw128(smem_u32(sm.dO[0]), 16, 1024);
-      const uint64_t qmn0 = sdesc_sw128(smem_u32(sm.q[0]), QHALF, 1024);
-      const uint64_t domn0 = sdesc_sw128(smem_u32(sm.dO[0]), QHALF, 1024);
       bool ok = mbar_wait(&sm.kv_full, 0, wait_ns);
-      // Without dQ the gradient products are issued by warp 10, so the score products of the
-      // next block never wait behind them in this thread.
-      for (int it = 0; ok && it <= (kDQ ? n_it : n_it - 1); ++it) {
-        if (it < n_it) {
-          const int st = it % NSQ;
-          if (!mbar_wait(&sm.qd_full[st], (it / NSQ) & 1, wait_ns)) { ok = false; break; }
-          if (it > 0 && !mbar_wait(&sm.s_free, (it - 1) & 1, wait_ns)) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t qd = desc_add(qd0, st * 2 * QHALF), dod = desc_add(dod0, st * 2 * QHALF);
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int st = it % NSQ;
+        if (!mbar_wait(&sm.qd_full[st], (it / NSQ) & 1, wait_ns)) { ok = false; break; }
+        if (it > 0 && !mbar_wait(&sm.s_free, (it - 1) & 1, wait_ns)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t qd = desc_add(qd0, st * 2 * QHALF), dod = desc_add(dod0, st * 2 * QHALF);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ko = (kk >> 2) * KHALF + (kk & 3) * 32;
-            const uint32_t qo = (kk >> 2) * QHALF + (kk & 3) * 32;
-            mma_ss(t_s, desc_add(kd, ko), desc_add(qd, qo), id_s, kk != 0);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ko = (kk >> 2) * KHALF + (kk & 3) * 32;
-            const uint32_t qo = (kk >> 2) * QHALF + (kk & 3) * 32;
-            mma_ss(t_dp, desc_add(vd, ko), desc_add(dod, qo), id_s, kk != 0);
-          }
-          mma_commit(&sm.s_full);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ko = (kk >> 2) * KHALF + (kk & 3) * 32;
+          const uint32_t qo = (kk >> 2) * QHALF + (kk & 3) * 32;
+          mma_ss(t_s, desc_add(kd, ko), desc_add(qd, qo), id_s, kk != 0);
         }
-        if (kDQ && it > 0) {
-          const int jp = it - 1, sp = jp % NSQ;
-          if (!mbar_wait(&sm.p_full, jp & 1, wait_ns)) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t qmn = desc_add(qmn0, sp * 2 * QHALF);
-          const uint64_t domn = desc_add(domn0, sp * 2 * QHALF);
-          const uint32_t acc0 = jp != 0;
 #pragma unroll
-          for (int kk = 0; kk < BQ / 16; ++kk)
-            mma_ts(t_dv, t_p + kk * 8, desc_add(domn, kk * 2048), id_g, kk == 0 ? acc0 : 1u);
-#pragma unroll
-          for (int kk = 0; kk < BQ / 16; ++kk)
-            mma_ts(t_dk, t_ds + kk * 8, desc_add(qmn, kk * 2048), id_g, kk == 0 ? acc0 : 1u);
-          mma_commit(&sm.qd_empty[sp]);
-          if constexpr (kDQ) {
-            if (jp >= 1 && !mbar_wait(&sm.dq_free, (jp - 1) & 1, wait_ns)) { ok = false; break; }
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < BKV / 16; ++kk)
-              mma_ss(t_dq, desc_add(kmn, kk * 2048), desc_add(dsmn, kk * 2048), id_q, kk != 0);
-            mma_commit(&sm.dq_full);
-          }
-          mma_commit(&sm.pds_free);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ko = (kk >> 2) * KHALF + (kk & 3) * 32;
+          const uint32_t qo = (kk >> 2) * QHALF + (kk & 3) * 32;
+          mma_ss(t_dp, desc_add(vd, ko), desc_add(dod, qo), id_s, kk != 0);
         }
+        mma_commit(&sm.s_full);
       }
       if (!ok) fail(PG_ERR_TIMEOUT);
       mma_commit(&sm.mma_done);
@@ -418,15 +389,20 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       ok = false;
     }
     if (!ok) fail(PG_ERR_TIMEOUT);
-  } else if (!kDQ) {
-    // ------------------------------------------------------------------ dV / dK MMAs -----
-    // Second issuing thread (no-dQ variant): dV += P^T dO and dK += dS^T Q of each block as soon
-    // as its P^T / dS^T are in TMEM.  Block j's S^T / dP^T products completed before its softmax
-    // could signal p_full, so the qd_empty commit below covers every reader of the stage.
-    if (warp == 10 && elect_one()) {
-      constexpr uint32_t id_g = idesc_bf16(BKV, D, 0, 1);
+  } else if (warp == grad_warp(kDQ)) {
+    // ------------------------------------------------------------------ gradient MMAs ----
+    // Second issuing thread: dV += P^T dO and dK += dS^T Q of each block as soon as its P^T /
+    // dS^T are in TMEM, then (with dQ) dQ^T = K^T dS^T once the drain warps have read the
+    // previous block's dQ^T.  Block j's S^T / dP^T products completed before its softmax could
+    // signal p_full, so the qd_empty commit below covers every reader of the stage.
+    if (elect_one()) {
+      constexpr uint32_t id_g = idesc_bf16(BKV, D, 0, 1);      // dV, dK
+      constexpr uint32_t id_q = idesc_bf16(D, BQ, 1, 1);       // dQ^T
+      // MN-major operands: LBO = the 64-column half.
       const uint64_t qmn0 = sdesc_sw128(smem_u32(sm.q[0]), QHALF, 1024);
       const uint64_t domn0 = sdesc_sw128(smem_u32(sm.dO[0]), QHALF, 1024);
+      const uint64_t kmn = sdesc_sw128(smem_u32(sm.k), KHALF, 1024);
+      const uint64_t dsmn = sdesc_sw128(smem_u32(sm.ds), QHALF, 1024);
       bool ok = true;
       for (int jp = 0; jp < n_it; ++jp) {
         const int sp = jp % NSQ;
@@ -442,6 +418,18 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
         for (int kk = 0; kk < BQ / 16; ++kk)
           mma_ts(t_dk, t_ds + kk * 8, desc_add(qmn, kk * 2048), id_g, kk == 0 ? acc0 : 1u);
         mma_commit(&sm.qd_empty[sp]);
+        if constexpr (kDQ) {
+          if (jp >= 1 && !mbar_wait(&sm.dq_free, (jp - 1) & 1, wait_ns)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BKV / 16; ++kk)
+            mma_ss(t_dq, desc_add(kmn, kk * 2048), desc_add(dsmn, kk * 2048), id_q, kk != 0);
+          mma_commit(&sm.dq_full);
+        } else {
+          (void)kmn;
+          (void)dsmn;
+          (void)id_q;
+        }
         mma_commit(&sm.pds_free);
       }
       if (!ok) fail(PG_ERR_TIMEOUT);
@@ -449,7 +437,7 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       mbar_wait(&sm.mma_done2, 0, wait_ns);
     }
     __syncwarp();
-  } else {
+  } else if (kDQ) {
     // ------------------------------------------------------------------ dQ drain ---------
     const int quarter = warp & 3;                  // this warp's 32 head dims (= TMEM lanes)
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;

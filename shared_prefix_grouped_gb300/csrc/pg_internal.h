@@ -182,16 +182,22 @@ pg_status launch_score_sm100(const AttnArgs& a, const void* q, const void* k, co
 pg_status read_status_score_sm100(bool clear, int32_t* code);
 
 // RoPE inverse frequencies theta^(-2k/d), k < d/2, computed on the host in fp64.
+// RoPE frequencies as fractions of a turn: turn[k] = frac(inv_freq_k / 2 pi) in 0.64 fixed point,
+// so that position x turn[k] taken modulo 2^64 is the angle already reduced to one turn (integer
+// arithmetic in the kernel: double precision is slow on this part).
 struct RopeFreq {
-  double inv[64];
-  double inv_two_pi;
+  uint64_t turn[64];
 };
 
+// Which token rows a RoPE pass rotates: every row of both tensors; the response rows (the
+// layout's response spans) of both; or every row of the first tensor and the response rows of
+// the second, in separate blocks of one launch.
+enum class RopeRows { kAll, kResponses, kAllThenResponses };
+
 // SIMT kernels (pg_simt.cu).
-// responses_only: rotate the response tokens only (the layout's response spans).
 pg_status launch_rope(const AttnArgs& a, const void* x0, void* y0, int heads0, const void* x1,
                       void* y1, int heads1, bool inverse, bool in_fp32, float2* table_out,
-                      const float2* table_in, bool responses_only = false);
+                      const float2* table_in, RopeRows rows = RopeRows::kAll);
 pg_status launch_fwd_simt(const AttnArgs& a, const void* q, const void* k, const void* v, void* o,
                           float* lse);
 pg_status launch_bwd_simt(const AttnArgs& a, const void* q, const void* k, const void* v,

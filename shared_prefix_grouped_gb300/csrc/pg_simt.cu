@@ -118,18 +118,35 @@ __device__ __forceinline__ float quad_sum(float x) {
 constexpr int kRopeThreads = 256;
 constexpr int kRopeMaxTokens = 8;
 
+// 2 pi / 2^32: one unit of a turn's upper 32 fraction bits, in radians.
+constexpr float kRadPerTurnUnit = 1.4629180792671596e-09f;
+
 template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(kRopeThreads)
 rope_kernel(const Tin* __restrict__ x0, Tout* __restrict__ y0, int h0,
             const Tin* __restrict__ x1, Tout* __restrict__ y1, int h1, int d, int Ttot, int tpb,
-            const FwdTile* __restrict__ spans, int span_blocks,
+            const FwdTile* __restrict__ spans, int span_blocks, int split, int tpb1,
             const int32_t* __restrict__ pos_ids, RopeFreq f, int rope, float sgn,
             float2* __restrict__ table_out, const float2* __restrict__ table_in) {
   __shared__ float cs[kRopeMaxTokens][64], sn[kRopeMaxTokens][64];
-  int t_first = blockIdx.x * tpb, t_limit = Ttot;
+  int blk = blockIdx.x;
+  if (split > 0) {
+    // Two parts: blocks [0, split) rotate every row of x0, the others the response rows of x1.
+    if (blk >= split) {
+      blk -= split;
+      x0 = x1;
+      y0 = y1;
+      h0 = h1;
+      tpb = tpb1;
+    } else {
+      spans = nullptr;
+    }
+    h1 = 0;
+  }
+  int t_first = blk * tpb, t_limit = Ttot;
   if (spans != nullptr) {
-    const FwdTile sp = spans[blockIdx.x / span_blocks];
-    t_first = sp.q0 + (blockIdx.x % span_blocks) * tpb;
+    const FwdTile sp = spans[blk / span_blocks];
+    t_first = sp.q0 + (blk % span_blocks) * tpb;
     t_limit = min(sp.q1, Ttot);
     if (t_first >= t_limit) return;
   }
@@ -143,10 +160,11 @@ rope_kernel(const Tin* __restrict__ x0, Tout* __restrict__ y0, int h0,
         c = v.x;
         s = v.y;
       } else {
-        const double two_pi = 6.283185307179586476925;
-        const double a = (double)pos_ids[t] * f.inv[k];
-        const double r = fma(-two_pi, rint(a * f.inv_two_pi), a);
-        sincosf((float)r, &s, &c);
+        // position x (inv_freq / 2 pi) modulo one turn, exact in 0.64 fixed point (positions
+        // are non-negative); its upper 32 bits read as signed give the angle in [-pi, pi).
+        const uint64_t turns = (uint64_t)(uint32_t)pos_ids[t] * f.turn[k];
+        const float r = (float)(int32_t)(uint32_t)(turns >> 32) * kRadPerTurnUnit;
+        sincosf(r, &s, &c);
         if (table_out) table_out[(size_t)t * half + k] = make_float2(c, s);
       }
     }
@@ -597,28 +615,43 @@ pg_status bwd_simt_t(const AttnArgs& a, const void* q, const void* k, const void
 
 RopeFreq rope_freq(const AttnArgs& a) {
   RopeFreq f{};
-  for (int k = 0; k < a.d / 2 && k < 64; ++k)
-    f.inv[k] = a.theta > 0.f ? pow((double)a.theta, -2.0 * k / a.d) : 0.0;
-  f.inv_two_pi = 1.0 / 6.283185307179586476925;
+  if (a.theta > 0.f)
+    for (int k = 0; k < a.d / 2 && k < 64; ++k) {
+      double c = pow((double)a.theta, -2.0 * k / a.d) / 6.283185307179586476925;
+      c -= floor(c);                                  // whole turns drop out of position x c
+      f.turn[k] = (uint64_t)ldexp(c, 64);             // c < 1, so this is below 2^64
+    }
   return f;
 }
 
 pg_status launch_rope(const AttnArgs& a, const void* x0, void* y0, int heads0, const void* x1,
                       void* y1, int heads1, bool inverse, bool in_fp32, float2* table_out,
-                      const float2* table_in, bool responses_only) {
+                      const float2* table_in, RopeRows rows) {
   const int T = (int)a.layout->total_tokens;
   const int rope = a.theta > 0.f ? 1 : 0;
   const RopeFreq f = rope_freq(a);
   const float sgn = inverse ? -1.f : 1.f;
   const int32_t* pos = a.layout->position_ids;
   // Tokens per block: enough 16-byte work items (heads x d/16 per token) for the block's threads.
-  const int items = (heads0 + (x1 ? heads1 : 0)) * (a.d / 16);
-  const int tpb = std::max(1, std::min(kRopeMaxTokens, kRopeThreads / std::max(items, 1)));
-  const FwdTile* spans = responses_only ? tiles<FwdTile>(a.layout, SPANS) : nullptr;
+  auto per_block = [&](int heads) {
+    const int items = heads * (a.d / 16);
+    return std::max(1, std::min(kRopeMaxTokens, kRopeThreads / std::max(items, 1)));
+  };
+  const bool split = rows == RopeRows::kAllThenResponses;
+  if (split && (x1 == nullptr || table_out != nullptr || table_in != nullptr)) {
+    set_error("rope: the two-part pass takes two tensors and no cos/sin table");
+    return PG_ERR_INVALID_ARG;
+  }
+  const int tpb = per_block(heads0 + (x1 && !split ? heads1 : 0));
+  const int tpb1 = split ? per_block(heads1) : tpb;
+  const bool use_spans = rows != RopeRows::kAll;
+  const FwdTile* spans = use_spans ? tiles<FwdTile>(a.layout, SPANS) : nullptr;
   const int span_blocks =
-      responses_only ? (int)std::max<int64_t>(1, (a.layout->max_response_rows + tpb - 1) / tpb) : 1;
-  const int64_t nblocks =
-      responses_only ? a.layout->n_tiles[SPANS] * span_blocks : (T + tpb - 1) / tpb;
+      use_spans ? (int)std::max<int64_t>(1, (a.layout->max_response_rows + tpb1 - 1) / tpb1) : 1;
+  const int64_t all_blocks = (T + tpb - 1) / tpb;
+  const int64_t resp_blocks = a.layout->n_tiles[SPANS] * span_blocks;
+  const int64_t nblocks = split ? all_blocks + resp_blocks : use_spans ? resp_blocks : all_blocks;
+  const int split_at = split ? (int)all_blocks : 0;
   if (nblocks == 0) return PG_OK;
   dim3 grid((unsigned)nblocks), block(kRopeThreads);
   const pg_kernel kid = inverse ? PG_KERNEL_ROPE_BWD : PG_KERNEL_ROPE;
@@ -626,18 +659,18 @@ pg_status launch_rope(const AttnArgs& a, const void* x0, void* y0, int heads0, c
   if (a.dtype == PG_F32) {
     rope_kernel<float, float><<<grid, block, 0, a.stream>>>(
         static_cast<const float*>(x0), static_cast<float*>(y0), heads0,
-        static_cast<const float*>(x1), static_cast<float*>(y1), heads1, a.d, T, tpb, spans, span_blocks, pos, f,
-        rope, sgn, table_out, table_in);
+        static_cast<const float*>(x1), static_cast<float*>(y1), heads1, a.d, T, tpb, spans, span_blocks, split_at, tpb1, pos,
+        f, rope, sgn, table_out, table_in);
   } else if (in_fp32) {
     rope_kernel<float, __nv_bfloat16><<<grid, block, 0, a.stream>>>(
         static_cast<const float*>(x0), static_cast<__nv_bfloat16*>(y0), heads0,
         static_cast<const float*>(x1), static_cast<__nv_bfloat16*>(y1), heads1, a.d, T, tpb, spans, span_blocks,
-        pos, f, rope, sgn, table_out, table_in);
+        split_at, tpb1, pos, f, rope, sgn, table_out, table_in);
   } else {
     rope_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, block, 0, a.stream>>>(
         static_cast<const __nv_bfloat16*>(x0), static_cast<__nv_bfloat16*>(y0), heads0,
         static_cast<const __nv_bfloat16*>(x1), static_cast<__nv_bfloat16*>(y1), heads1, a.d, T, tpb,
-        spans, span_blocks, pos, f, rope, sgn, table_out, table_in);
+        spans, span_blocks, split_at, tpb1, pos, f, rope, sgn, table_out, table_in);
   }
   prof_end(kid, a.stream);
   return cuda_check(cudaGetLastError(), "rope launch");
