@@ -121,8 +121,10 @@ constexpr int kRopeMaxTokens = 8;
 // 2 pi / 2^32: one unit of a turn's upper 32 fraction bits, in radians.
 constexpr float kRadPerTurnUnit = 1.4629180792671596e-09f;
 
+// With bf16 input a thread needs at most 32 registers, so eight blocks fit on an SM: the pass is
+// bound by the bytes each SM keeps in flight.
 template <typename Tin, typename Tout>
-__global__ void __launch_bounds__(kRopeThreads)
+__global__ void __launch_bounds__(kRopeThreads, sizeof(Tin) == 2 ? 8 : 6)
 rope_kernel(const Tin* __restrict__ x0, Tout* __restrict__ y0, int h0,
             const Tin* __restrict__ x1, Tout* __restrict__ y1, int h1, int d, int Ttot, int tpb,
             const FwdTile* __restrict__ spans, int span_blocks, int split, int tpb1,
