@@ -99,6 +99,19 @@ typedef struct pg_opts {
  */
 #define PG_FLAG_KEEP_ROTATED 8u
 
+/*
+ * q and k arrive already RoPE-rotated at the layout's position ids with opts->rope_theta (for
+ * example by pg_gemm_bf16_rope in the projection that produced them, from the table pg_rope_table
+ * wrote): the calls do not rotate them again.  The backward still returns dq and dk with respect
+ * to the un-rotated q and k (rotating them back with the cos/sin table), exactly as without the
+ * flag, so the table must be in the workspace: call pg_rope_table on the backward's workspace
+ * (same layout, heads, rope_theta and flags) before the forward, and keep it unchanged until the
+ * backward.  Needs rope_theta > 0 (PG_ERR_INVALID_ARG otherwise).  Combines with
+ * PG_FLAG_KEEP_ROTATED (the forward then leaves only its LSE rows for the backward),
+ * PG_FLAG_DETERMINISTIC, PG_FLAG_SIMT and PG_FLAG_RESPONSES_ONLY.
+ */
+#define PG_FLAG_PRE_ROTATED 16u
+
 /* Test hook for the bounded-wait error path: the tensor-core forward never signals that P is
  * ready, so its MMA thread's wait runs out (after 50 ms instead of 2 s), the kernel records
  * PG_ERR_TIMEOUT in the status word and exits cleanly; the outputs are then undefined. */
@@ -252,6 +265,20 @@ pg_status pg_grouped_attn_bwd(const pg_layout* layout, pg_dtype dtype, int32_t h
                               const void* v, const void* o, const float* lse, const void* dO,
                               void* dq, void* dk, void* dv, const pg_opts* opts, void* workspace,
                               size_t workspace_bytes, pg_stream_t stream);
+
+/*
+ * RoPE cos/sin table for PG_FLAG_PRE_ROTATED: writes (cos a, sin a), a = position_ids[t] *
+ * rope_theta^(-2k/d), as float2 [T][d/2] (row t, column k; fp32) into `workspace` -- the
+ * workspace later passed to pg_grouped_attn_bwd (and, with PG_FLAG_KEEP_ROTATED, to
+ * pg_grouped_attn_fwd) with the same layout, dtype, heads and opts, where the table occupies the
+ * first T * d/2 * 8 bytes -- and returns its device address in *table (for pg_gemm_bf16_rope).
+ * opts must carry rope_theta > 0 and PG_FLAG_PRE_ROTATED; workspace >= pg_workspace_size(..., 1),
+ * 16-byte aligned.  Asynchronous on `stream`.
+ * Errors: PG_ERR_INVALID_ARG (host check, nothing launched); PG_ERR_CUDA on a launch failure.
+ */
+pg_status pg_rope_table(const pg_layout* layout, pg_dtype dtype, int32_t heads_q, int32_t heads_kv,
+                        int32_t head_dim, const pg_opts* opts, void* workspace,
+                        size_t workspace_bytes, const void** table, pg_stream_t stream);
 
 /* Kernels of the library, for pg_set_profile. */
 typedef enum pg_kernel {

@@ -31,6 +31,22 @@ pg_status pg_gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, int32_t a
                        int64_t ldc, int32_t accumulate, pg_stream_t stream);
 
 /*
+ * The q or k projection with RoPE in its epilogue: C[m, n] = rotate(sum_k A[m * lda + k] *
+ * B[n * ldb + k]) in bf16, where every head_dim-wide column block of a row m is rotated as the
+ * attention calls rotate q and k (rotate-half pairs (j, j + head_dim/2), j < head_dim/2, by the
+ * angle whose (cos, sin) is table[m * head_dim/2 + j]): the fp32 accumulator is rotated before
+ * the one rounding to bf16.  table: the float2 [table_rows][head_dim/2] table of pg_rope_table
+ * (table_rows = the layout's total tokens, at least M; row m of A is token m).  A and B
+ * row-major (K-major), bf16, 16-byte aligned, lda and ldb multiples of 8; C bf16, 16-byte
+ * aligned, ldc a multiple of 8 and >= N; head_dim 64 or 128 dividing N.  The result feeds the
+ * attention calls with PG_FLAG_PRE_ROTATED.
+ * Errors: PG_ERR_INVALID_ARG (host check, nothing launched); PG_ERR_CUDA on a launch failure.
+ */
+pg_status pg_gemm_bf16_rope(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                            const void* B, int64_t ldb, void* C, int64_t ldc, int32_t head_dim,
+                            const void* table, int64_t table_rows, pg_stream_t stream);
+
+/*
  * RMSNorm forward over T rows of `hidden` bf16 values (Llama style: no mean subtraction):
  *   y = x + residual (stored to sum_out in bf16, when residual is not NULL), else y = x;
  *   out = y / sqrt(mean(y^2) + eps) * gamma  (bf16);  rstd[t] = 1 / sqrt(mean(y_t^2) + eps) (fp32).

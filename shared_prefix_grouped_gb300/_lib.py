@@ -13,6 +13,7 @@ PG_FLAG_SIMT = 1
 PG_FLAG_RESPONSES_ONLY = 2
 PG_FLAG_DETERMINISTIC = 4
 PG_FLAG_KEEP_ROTATED = 8
+PG_FLAG_PRE_ROTATED = 16
 
 
 class PgLayout(C.Structure):
@@ -94,9 +95,13 @@ SIGNATURES = {
     "pg_grouped_attn_fwd_noalloc": (C.c_int, [C.POINTER(PgLayout), C.c_int, C.c_int32,
                                               C.c_int32, C.c_int32, VP, VP, VP, VP, VP,
                                               C.POINTER(PgOpts), VP]),
+    "pg_rope_table": (C.c_int, [C.POINTER(PgLayout), C.c_int, C.c_int32, C.c_int32, C.c_int32,
+                                C.POINTER(PgOpts), VP, C.c_size_t, C.POINTER(VP), VP]),
     "pg_set_profile": (C.c_int, [C.POINTER(PgProfile)]),
     "pg_gemm_bf16": (C.c_int, [C.c_int64, C.c_int64, C.c_int64, VP, C.c_int32, C.c_int64, VP,
                                C.c_int32, C.c_int64, VP, C.c_int, C.c_int64, C.c_int32, VP]),
+    "pg_gemm_bf16_rope": (C.c_int, [C.c_int64, C.c_int64, C.c_int64, VP, C.c_int64, VP, C.c_int64,
+                                    VP, C.c_int64, C.c_int32, VP, C.c_int64, VP]),
     "pg_rmsnorm_fwd": (C.c_int, [C.c_int64, C.c_int32, VP, VP, VP, C.c_float, VP, VP, VP, VP]),
     "pg_rmsnorm_bwd_workspace": (C.c_size_t, [C.c_int64, C.c_int32]),
     "pg_rmsnorm_bwd": (C.c_int, [C.c_int64, C.c_int32, VP, VP, VP, VP, C.c_int, VP, VP, C.c_int,

@@ -236,6 +236,41 @@ def grouped_attn_bwd(layout: Layout, q, k, v, o, lse, do, *, rope_theta: float =
     return dq, dk, dv
 
 
+def rope_table(layout: Layout, dtype: torch.dtype, Hq: int, Hkv: int, d: int,
+               workspace: torch.Tensor, *, rope_theta: float, flags: int) -> int:
+    """Writes the cos/sin table of PG_FLAG_PRE_ROTATED into `workspace` (pg_rope_table) and
+    returns its device address; flags must include PG_FLAG_PRE_ROTATED."""
+    opts = make_opts(rope_theta, 0.0, flags)
+    table = C.c_void_p()
+    with torch.cuda.device(workspace.device):
+        check("pg_rope_table", _lib.lib().pg_rope_table(
+            C.byref(layout.struct), _DT[dtype], Hq, Hkv, d, C.byref(opts), _ptr(workspace),
+            workspace.numel(), C.byref(table), _stream_ptr(workspace.device)))
+    return int(table.value)
+
+
+def gemm_bf16_rope(a: torch.Tensor, b: torch.Tensor, table: int, table_rows: int, head_dim: int,
+                   out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """bf16 [M, N] = a [M, K] @ b [N, K]^T with every head_dim-wide column block RoPE-rotated in
+    the epilogue by the rows' (cos, sin) from `table` (pg_gemm_bf16_rope)."""
+    if a.dtype != torch.bfloat16 or b.dtype != torch.bfloat16:
+        raise ValueError("gemm_bf16_rope takes bf16 operands")
+    _contig(a, b)
+    M, K = a.shape
+    N, Kb = b.shape
+    if K != Kb:
+        raise ValueError("inner dimensions differ")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    if out.dtype != torch.bfloat16 or out.dim() != 2 or out.stride(1) != 1 or out.shape != (M, N):
+        raise ValueError("out must be a bf16 [M, N] matrix with unit column stride")
+    with torch.cuda.device(a.device):
+        check("pg_gemm_bf16_rope", _lib.lib().pg_gemm_bf16_rope(
+            M, N, K, _ptr(a), a.shape[1], _ptr(b), b.shape[1], _ptr(out), out.stride(0), head_dim,
+            C.c_void_p(table), table_rows, _stream_ptr(a.device)))
+    return out
+
+
 def device_status(clear: bool = True) -> int:
     """The kernels' status word (0 = ok); synchronous."""
     return int(_lib.lib().pg_device_status(1 if clear else 0))

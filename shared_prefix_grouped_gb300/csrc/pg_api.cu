@@ -593,7 +593,10 @@ static WsPlan ws_plan(const pg_layout* L, pg_dtype dt, int Hq, int Hkv, int d, b
   // Offset 0 is a valid slot; record "absent" as SIZE_MAX.
   w.q_rot = w.k_rot = w.rope_tab = w.Dbuf = w.lse2 = w.dq_acc = w.dk_acc = SIZE_MAX;
   w.part_o = w.part_lse = SIZE_MAX;
-  if (rope) {
+  if (rope && (a.flags & PG_FLAG_PRE_ROTATED)) {
+    // q and k come rotated; only the backward's cos/sin table, at offset 0 (pg_rope_table).
+    if (phase == 1) w.rope_tab = take(T * (d / 2) * sizeof(float2));
+  } else if (rope) {
     w.q_rot = take(T * Hq * d * esize(dt));
     w.k_rot = take(T * Hkv * d * esize(dt));
     if (phase == 1) w.rope_tab = take(T * (d / 2) * sizeof(float2));
@@ -643,6 +646,10 @@ static pg_status check_attn(const pg_layout* L, pg_dtype dt, int Hq, int Hkv, in
   }
   if (opts && (opts->softmax_scale < 0.f || opts->rope_theta < 0.f)) {
     set_error("%s: softmax_scale and rope_theta must be >= 0", who);
+    return PG_ERR_INVALID_ARG;
+  }
+  if (opts && (opts->flags & PG_FLAG_PRE_ROTATED) && !(opts->rope_theta > 0.f)) {
+    set_error("%s: PG_FLAG_PRE_ROTATED needs rope_theta > 0", who);
     return PG_ERR_INVALID_ARG;
   }
   int i = 0;
@@ -884,14 +891,16 @@ pg_status pg_grouped_attn_fwd(const pg_layout* layout, pg_dtype dtype, int32_t h
               who);
     return PG_ERR_UNSUPPORTED;
   }
-  if (rope && responses_only) {
+  // Already-rotated q and k (PG_FLAG_PRE_ROTATED) go to the kernels as they are.
+  const bool rotate = rope && !(a.flags & PG_FLAG_PRE_ROTATED);
+  if (rotate && responses_only) {
     // Every key is rotated; of q only the response rows, the only ones read.
     st = launch_rope(a, k, ws + w.k_rot, heads_kv, q, ws + w.q_rot, heads_q, false, false,
                      nullptr, nullptr, RopeRows::kAllThenResponses);
     if (st != PG_OK) return st;
     qx = ws + w.q_rot;
     kx = ws + w.k_rot;
-  } else if (rope) {
+  } else if (rotate) {
     // Keeping the rotation for the backward also stores the cos/sin table it rotates dK/dQ back
     // with.
     st = launch_rope(a, q, ws + w.q_rot, heads_q, k, ws + w.k_rot, heads_kv, false, false,
@@ -946,7 +955,8 @@ pg_status pg_grouped_attn_bwd(const pg_layout* layout, pg_dtype dtype, int32_t h
   const void* qx = q;
   const void* kx = k;
   float2* rope_tab = rope ? reinterpret_cast<float2*>(ws + w.rope_tab) : nullptr;
-  if (rope) {
+  // PG_FLAG_PRE_ROTATED: q and k come rotated and pg_rope_table wrote the table.
+  if (rope && !(a.flags & PG_FLAG_PRE_ROTATED)) {
     // With PG_FLAG_KEEP_ROTATED the forward left the rotated q/k and the table here.
     if (!(a.flags & PG_FLAG_KEEP_ROTATED)) {
       st = launch_rope(a, q, ws + w.q_rot, heads_q, k, ws + w.k_rot, heads_kv, false, false,
@@ -986,6 +996,32 @@ pg_status pg_grouped_attn_bwd(const pg_layout* layout, pg_dtype dtype, int32_t h
   // Padded layout: the padding rows' gradients are zero (their queries had no weight; no real
   // query sees their keys); write them as exact zeros.
   return launch_pad_fill(a, dq, heads_q, dk, heads_kv, dv, heads_kv, nullptr);
+}
+
+pg_status pg_rope_table(const pg_layout* layout, pg_dtype dtype, int32_t heads_q, int32_t heads_kv,
+                        int32_t head_dim, const pg_opts* opts, void* workspace,
+                        size_t workspace_bytes, const void** table, pg_stream_t stream) {
+  const char* who = "pg_rope_table";
+  pg_status st = check_attn(layout, dtype, heads_q, heads_kv, head_dim, opts, {workspace}, who);
+  if (st != PG_OK) return st;
+  if (!table || !opts || !(opts->flags & PG_FLAG_PRE_ROTATED)) {
+    set_error("%s: needs opts with PG_FLAG_PRE_ROTATED and rope_theta > 0, and a table pointer",
+              who);
+    return PG_ERR_INVALID_ARG;
+  }
+  const AttnArgs a = make_args(layout, dtype, heads_q, heads_kv, head_dim, opts,
+                               reinterpret_cast<cudaStream_t>(stream));
+  const WsPlan w = ws_plan(layout, dtype, heads_q, heads_kv, head_dim, true, 1, a);
+  if (workspace_bytes < w.total) {
+    set_error("%s: workspace must be >= %zu bytes (the backward's)", who, w.total);
+    return PG_ERR_INVALID_ARG;
+  }
+  float2* tab = reinterpret_cast<float2*>(static_cast<char*>(workspace) + w.rope_tab);
+  // The RoPE pass with no tensors to rotate writes only the table.
+  st = launch_rope(a, nullptr, nullptr, 0, nullptr, nullptr, 0, false, false, tab, nullptr);
+  if (st != PG_OK) return st;
+  *table = tab;
+  return PG_OK;
 }
 
 pg_status pg_set_profile(pg_profile* profile) {

@@ -9,6 +9,12 @@
 // warp 1 issues the MMAs (128 x 256 x 16 each, 4 per 64-wide K block, descriptors built once and
 // advanced by constant offsets), then all four warps drain TMEM (warp w owns accumulator lanes /
 // C rows 32w .. 32w + 31) with 16-byte stores where the tile is in bounds and aligned.
+//
+// The RoPE variant (the q / k projections feeding the attention calls with PG_FLAG_PRE_ROTATED)
+// rotates every head_dim-wide column block of the accumulator in its epilogue: a thread holds a
+// whole row, so each rotate-half pair (j, j + head_dim/2) is read from TMEM by the same thread,
+// rotated in fp32 by its row's (cos, sin) from the table and rounded to bf16 once.  A 256-wide
+// tile starts on a head boundary (head_dim 64 or 128 divides 256), so no pair straddles tiles.
 #include "pg_internal.h"
 #include "pg_sm100.cuh"
 #include "pg_tmap.h"
@@ -36,11 +42,11 @@ struct GemmSmem {
   uint32_t tmem;
 };
 
-template <int A_MN, int B_MN, typename OutT>
+template <int A_MN, int B_MN, typename OutT, bool ROPE>
 __global__ void __launch_bounds__(128, 1)
 gemm_bf16_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
                  OutT* __restrict__ C, int M, int N, int K, long long ldc, int accumulate,
-                 int vec_ok) {
+                 int vec_ok, const float2* __restrict__ rope_tab, int head_dim) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   GemmSmem& sm = *reinterpret_cast<GemmSmem*>(base);
@@ -132,9 +138,54 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__
 
   // Epilogue: every warp drains its 32 accumulator lanes.
   if (!mbar_wait(&sm.done, 0, WAIT_NS)) ok = false;
+  ok = __all_sync(0xffffffffu, ok);     // the TMEM loads below are warp-collective
   tc_fence_after();
   const int row = m0 + warp * 32 + lane;
-  if (ok) {
+  if constexpr (ROPE) {
+    // bf16 output, 16-byte stores (checked on the host), whole heads (head_dim divides N).
+    const int half = head_dim >> 1;
+    const float4* tab =
+        reinterpret_cast<const float4*>(rope_tab + (size_t)(row < M ? row : M - 1) * half);
+#pragma unroll 1
+    for (int hc = 0; ok && hc < BN; hc += head_dim) {
+#pragma unroll 1
+      for (int j0 = 0; j0 < half; j0 += 32) {
+        uint32_t x1[32], x2[32];
+        const uint32_t t = tmem + ((uint32_t)(warp * 32) << 16) + hc + j0;
+        tmem_ld32(t, x1);
+        tmem_ld32(t + half, x2);
+        tmem_ld_wait();
+        if (row < M && n0 + hc < N) {
+          float lo[32], hi[32];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float4 e = tab[(j0 + j) >> 1];      // (cos, sin) of pairs j0 + j, j0 + j + 1
+            const float a0 = __uint_as_float(x1[j]), b0 = __uint_as_float(x2[j]);
+            const float a1 = __uint_as_float(x1[j + 1]), b1 = __uint_as_float(x2[j + 1]);
+            lo[j] = a0 * e.x - b0 * e.y;
+            hi[j] = b0 * e.x + a0 * e.y;
+            lo[j + 1] = a1 * e.z - b1 * e.w;
+            hi[j + 1] = b1 * e.z + a1 * e.w;
+          }
+          OutT* dst = C + (long long)row * ldc + n0 + hc + j0;
+#pragma unroll
+          for (int j = 0; j < 32; j += 8) {
+            uint4 w;
+            w.x = pack_bf16x2(lo[j], lo[j + 1]);
+            w.y = pack_bf16x2(lo[j + 2], lo[j + 3]);
+            w.z = pack_bf16x2(lo[j + 4], lo[j + 5]);
+            w.w = pack_bf16x2(lo[j + 6], lo[j + 7]);
+            *reinterpret_cast<uint4*>(dst + j) = w;
+            w.x = pack_bf16x2(hi[j], hi[j + 1]);
+            w.y = pack_bf16x2(hi[j + 2], hi[j + 3]);
+            w.z = pack_bf16x2(hi[j + 4], hi[j + 5]);
+            w.w = pack_bf16x2(hi[j + 6], hi[j + 7]);
+            *reinterpret_cast<uint4*>(dst + half + j) = w;
+          }
+        }
+      }
+    }
+  } else if (ok) {
     // 16-byte stores need the row start aligned: ldc * sizeof(OutT) a multiple of 16 and an
     // aligned C (checked on the host: vec_ok).
 #pragma unroll 1
@@ -199,10 +250,11 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__
   }
 }
 
-template <int A_MN, int B_MN, typename OutT>
+template <int A_MN, int B_MN, typename OutT, bool ROPE = false>
 pg_status launch(const CUtensorMap& ta, const CUtensorMap& tb, void* C, int M, int N, int K,
-                 long long ldc, int acc, cudaStream_t s) {
-  auto kern = gemm_bf16_kernel<A_MN, B_MN, OutT>;
+                 long long ldc, int acc, cudaStream_t s, const float2* rope_tab = nullptr,
+                 int head_dim = 0) {
+  auto kern = gemm_bf16_kernel<A_MN, B_MN, OutT, ROPE>;
   const size_t smem = sizeof(GemmSmem) + 1024;
   pg_status st = cuda_check(
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
@@ -212,7 +264,8 @@ pg_status launch(const CUtensorMap& ta, const CUtensorMap& tb, void* C, int M, i
   prof_begin(PG_KERNEL_GEMM, s);
   const int vec_ok = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0) &&
                      ((ldc * (long long)sizeof(OutT)) % 16 == 0);
-  kern<<<grid, 128, smem, s>>>(ta, tb, static_cast<OutT*>(C), M, N, K, ldc, acc, vec_ok);
+  kern<<<grid, 128, smem, s>>>(ta, tb, static_cast<OutT*>(C), M, N, K, ldc, acc, vec_ok,
+                               rope_tab, head_dim);
   prof_end(PG_KERNEL_GEMM, s);
   return cuda_check(cudaGetLastError(), "gemm launch");
 }
@@ -269,4 +322,33 @@ extern "C" pg_status pg_gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A
   if (!a_mn && b_mn) return launch<0, 1, __nv_bfloat16>(ta, tb, C, m, n, k, ldc, accumulate, s);
   if (a_mn && !b_mn) return launch<1, 0, __nv_bfloat16>(ta, tb, C, m, n, k, ldc, accumulate, s);
   return launch<1, 1, __nv_bfloat16>(ta, tb, C, m, n, k, ldc, accumulate, s);
+}
+
+extern "C" pg_status pg_gemm_bf16_rope(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                                       const void* B, int64_t ldb, void* C, int64_t ldc,
+                                       int32_t head_dim, const void* table,
+                                       int64_t table_rows, pg_stream_t stream) {
+  if (M < 1 || N < 1 || K < 1 || M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 31) ||
+      !A || !B || !C || !table || table_rows < M) {
+    set_error("pg_gemm_bf16_rope: bad sizes, NULL pointer or a table with fewer than M rows");
+    return PG_ERR_INVALID_ARG;
+  }
+  if ((head_dim != 64 && head_dim != 128) || N % head_dim != 0) {
+    set_error("pg_gemm_bf16_rope: head_dim must be 64 or 128 and divide N");
+    return PG_ERR_INVALID_ARG;
+  }
+  if (lda % 8 || ldb % 8 || ldc % 8 || lda < K || ldb < K || ldc < N ||
+      (reinterpret_cast<uintptr_t>(C) & 15u) || (reinterpret_cast<uintptr_t>(table) & 15u)) {
+    set_error("pg_gemm_bf16_rope: leading dimensions must be multiples of 8 covering the rows, "
+              "C and the table 16-byte aligned");
+    return PG_ERR_INVALID_ARG;
+  }
+  CUtensorMap ta, tb;
+  pg_status st = make_tmap_2d_bf16(&ta, A, K, M, lda * 2, 64, 128);
+  if (st != PG_OK) return st;
+  st = make_tmap_2d_bf16(&tb, B, K, N, ldb * 2, 64, BN);
+  if (st != PG_OK) return st;
+  return launch<0, 0, __nv_bfloat16, true>(ta, tb, C, (int)M, (int)N, (int)K, ldc, 0,
+                                           reinterpret_cast<cudaStream_t>(stream),
+                                           static_cast<const float2*>(table), head_dim);
 }

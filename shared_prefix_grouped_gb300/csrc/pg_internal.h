@@ -181,18 +181,18 @@ pg_status launch_score_sm100(const AttnArgs& a, const void* q, const void* k, co
                              void* o, float* lse, float* part_o, float* part_lse);
 pg_status read_status_score_sm100(bool clear, int32_t* code);
 
-// RoPE inverse frequencies theta^(-2k/d), k < d/2, computed on the host in fp64.
-// RoPE frequencies as fractions of a turn: turn[k] = frac(inv_freq_k / 2 pi) in 0.64 fixed point,
-// so that position x turn[k] taken modulo 2^64 is the angle already reduced to one turn (integer
-// arithmetic in the kernel: double precision is slow on this part).
+// RoPE frequencies inv_freq_k = theta^(-2k/d), k < d/2 (computed on the host in fp64), as
+// fractions of a turn: turn[k] = frac(inv_freq_k / 2 pi) in 0.64 fixed point, so that position x
+// turn[k] taken modulo 2^64 is the angle already reduced to one turn (integer arithmetic in the
+// kernel: double precision is slow on this part).
 struct RopeFreq {
   uint64_t turn[64];
 };
 
-// Which token rows a RoPE pass rotates: every row of both tensors; the response rows (the
-// layout's response spans) of both; or every row of the first tensor and the response rows of
-// the second, in separate blocks of one launch.
-enum class RopeRows { kAll, kResponses, kAllThenResponses };
+// Which token rows a RoPE pass rotates: every row of both tensors, or every row of the first
+// tensor and only the response rows (the layout's response spans) of the second, in separate
+// blocks of one launch.
+enum class RopeRows { kAll, kAllThenResponses };
 
 // SIMT kernels (pg_simt.cu).
 pg_status launch_rope(const AttnArgs& a, const void* x0, void* y0, int heads0, const void* x1,

@@ -646,13 +646,11 @@ pg_status launch_rope(const AttnArgs& a, const void* x0, void* y0, int heads0, c
   }
   const int tpb = per_block(heads0 + (x1 && !split ? heads1 : 0));
   const int tpb1 = split ? per_block(heads1) : tpb;
-  const bool use_spans = rows != RopeRows::kAll;
-  const FwdTile* spans = use_spans ? tiles<FwdTile>(a.layout, SPANS) : nullptr;
+  const FwdTile* spans = split ? tiles<FwdTile>(a.layout, SPANS) : nullptr;
   const int span_blocks =
-      use_spans ? (int)std::max<int64_t>(1, (a.layout->max_response_rows + tpb1 - 1) / tpb1) : 1;
+      split ? (int)std::max<int64_t>(1, (a.layout->max_response_rows + tpb1 - 1) / tpb1) : 1;
   const int64_t all_blocks = (T + tpb - 1) / tpb;
-  const int64_t resp_blocks = a.layout->n_tiles[SPANS] * span_blocks;
-  const int64_t nblocks = split ? all_blocks + resp_blocks : use_spans ? resp_blocks : all_blocks;
+  const int64_t nblocks = all_blocks + (split ? a.layout->n_tiles[SPANS] * span_blocks : 0);
   const int split_at = split ? (int)all_blocks : 0;
   if (nblocks == 0) return PG_OK;
   dim3 grid((unsigned)nblocks), block(kRopeThreads);

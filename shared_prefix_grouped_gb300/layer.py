@@ -5,7 +5,8 @@ Every linear projection and MLP runs over the packed tokens, so a group's shared
 through them once instead of once per response (abstract page of Prefix Grouper: the shared
 prefix is encoded only once; Pith review, "Core claim": the cost tends to 1/G of the baseline).
 
-Forward:  h1 = rmsnorm(x) g1;  q, k, v = h1 W_q^T, h1 W_k^T, h1 W_v^T;  o = attn(q, k, v);
+Forward:  h1 = rmsnorm(x) g1;  q, k, v = h1 W_q^T, h1 W_k^T, h1 W_v^T (RoPE of q and k applied in
+          their GEMMs' epilogue, or with fused_rope=False by the attention call);  o = attn(q, k, v);
           x2 = x + o W_o^T;  h2 = rmsnorm(x2) g2;  [g | u] = h2 W_gu^T;  y = x2 + (silu(g) u) W_d^T
 Backward: the chain rule through the same steps, weight gradients in fp32.
 """
@@ -35,22 +36,31 @@ def _views(w_qkv, Hq, Hkv, d):
 
 
 def layer_fwd(layout: api.Layout, x, w_qkv, w_o, w_gu, w_d, g1, g2, *, heads_q, heads_kv,
-              head_dim, rope_theta, eps):
+              head_dim, rope_theta, eps, fused_rope: bool = True):
     T, H = x.shape
     Hq, Hkv, d = heads_q, heads_kv, head_dim
     wq, wk, wv = _views(w_qkv, Hq, Hkv, d)
     bf = torch.bfloat16
     h1, _, r1 = api.rmsnorm_fwd(x, g1, eps)
-    q = api.gemm_bf16(h1, wq, out_dtype=bf)
-    k = api.gemm_bf16(h1, wk, out_dtype=bf)
-    v = api.gemm_bf16(h1, wv, out_dtype=bf)
-    # One attention workspace for the step: the forward leaves the rotated q/k, the cos/sin table
-    # and its log2-domain LSE there for the backward (PG_FLAG_KEEP_ROTATED).
-    keep = _lib.PG_FLAG_KEEP_ROTATED
+    # One attention workspace for the step: the forward leaves its log2-domain LSE (and, unless
+    # the projections rotate q and k themselves, the rotated q/k and the cos/sin table) there for
+    # the backward (PG_FLAG_KEEP_ROTATED).
+    fused = fused_rope and rope_theta > 0
+    flags = _lib.PG_FLAG_KEEP_ROTATED | (_lib.PG_FLAG_PRE_ROTATED if fused else 0)
     ws = api._workspace(api.workspace_size(layout, bf, Hq, Hkv, d,
-                                           api.make_opts(rope_theta, 0.0, keep), 1), x.device)
+                                           api.make_opts(rope_theta, 0.0, flags), 1), x.device)
+    if fused:
+        # RoPE in the q and k projections' epilogue, from the workspace's cos/sin table (which the
+        # backward also rotates dq and dk back with).
+        tab = api.rope_table(layout, bf, Hq, Hkv, d, ws, rope_theta=rope_theta, flags=flags)
+        q = api.gemm_bf16_rope(h1, wq, tab, T, d)
+        k = api.gemm_bf16_rope(h1, wk, tab, T, d)
+    else:
+        q = api.gemm_bf16(h1, wq, out_dtype=bf)
+        k = api.gemm_bf16(h1, wk, out_dtype=bf)
+    v = api.gemm_bf16(h1, wv, out_dtype=bf)
     o, lse = api.grouped_attn_fwd(layout, q.view(T, Hq, d), k.view(T, Hkv, d), v.view(T, Hkv, d),
-                                  rope_theta=rope_theta, flags=keep, workspace=ws)
+                                  rope_theta=rope_theta, flags=flags, workspace=ws)
     a = api.gemm_bf16(o.view(T, Hq * d), w_o, out_dtype=bf)
     h2, x2, r2 = api.rmsnorm_fwd(x, g2, eps, residual=a)
     gu = api.gemm_bf16(h2, w_gu, out_dtype=bf)
@@ -58,7 +68,7 @@ def layer_fwd(layout: api.Layout, x, w_qkv, w_o, w_gu, w_d, g1, g2, *, heads_q, 
     y = x2.clone()
     api.gemm_bf16(act, w_d, out=y, accumulate=True)
     saved = dict(h1=h1, r1=r1, q=q, k=k, v=v, o=o, lse=lse, x2=x2, h2=h2, r2=r2, gu=gu, act=act,
-                 attn_ws=ws)
+                 attn_ws=ws, attn_flags=flags)
     return y, saved
 
 
@@ -81,7 +91,7 @@ def layer_bwd(layout: api.Layout, x, w_qkv, w_o, w_gu, w_d, g1, g2, saved, dy, *
     dq, dk, dv = api.grouped_attn_bwd(layout, s["q"].view(T, Hq, d), s["k"].view(T, Hkv, d),
                                       s["v"].view(T, Hkv, d), s["o"], s["lse"],
                                       do.view(T, Hq, d), rope_theta=rope_theta,
-                                      flags=_lib.PG_FLAG_KEEP_ROTATED, workspace=s["attn_ws"])
+                                      flags=s["attn_flags"], workspace=s["attn_ws"])
     dq, dk, dv = dq.view(T, Hq * d), dk.view(T, Hkv * d), dv.view(T, Hkv * d)
     dh1 = api.gemm_bf16(dq, wq, b_mn=True, out_dtype=f32)
     api.gemm_bf16(dk, wk, b_mn=True, out=dh1, accumulate=True)

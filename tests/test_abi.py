@@ -300,3 +300,54 @@ def test_tree_packing_matches_hand_fixture():
     assert st.total_tokens == fx["total_tokens"] and st.pairs == fx["grouped_pairs"]
     assert pos.tolist() == fx["position_ids"]
     assert st.max_depth == 3
+
+
+def test_pre_rotated_workspace_and_argument_checks():
+    # With q and k arriving rotated the backward's workspace holds no rotated copies of them, only
+    # the cos/sin table; the flag needs RoPE; the table call and the RoPE GEMM check their
+    # arguments on the host (nothing here reaches a launch).
+    _, tab, st = api.pack_host([300], [2], [40, 60])
+    T, Hq, Hkv, d = st.total_tokens, 4, 2, 128
+    L = _lib.lib()
+    pre, keep = _lib.PG_FLAG_PRE_ROTATED, _lib.PG_FLAG_KEEP_ROTATED
+
+    def size(flags, theta, phase):
+        n = C.c_size_t()
+        rc = L.pg_workspace_size(C.byref(st), _lib.PG_BF16, Hq, Hkv, d,
+                                 C.byref(_lib.PgOpts(0.0, theta, flags, 0)), phase, C.byref(n))
+        return rc, n.value
+
+    def al(b):
+        return (b + 255) // 256 * 256
+
+    rc0, plain1 = size(0, 1e4, 1)
+    rc1, pre1 = size(pre, 1e4, 1)
+    assert rc0 == rc1 == _lib.PG_OK
+    assert plain1 - pre1 == al(T * Hq * d * 2) + al(T * Hkv * d * 2)
+    assert size(pre, 1e4, 0) == (_lib.PG_OK, 0)
+    assert size(pre | keep, 1e4, 0) == (_lib.PG_OK, pre1)
+    assert size(pre, 0.0, 1)[0] == _lib.PG_ERR_INVALID_ARG
+
+    buf = torch.empty(1 << 16, dtype=torch.uint8)
+    p = C.c_void_p(buf.data_ptr())
+    out = C.c_void_p()
+
+    def table(flags, theta, nbytes):
+        return L.pg_rope_table(C.byref(st), _lib.PG_BF16, Hq, Hkv, d,
+                               C.byref(_lib.PgOpts(0.0, theta, flags, 0)), p, nbytes,
+                               C.byref(out), None)
+
+    assert table(0, 1e4, pre1) == _lib.PG_ERR_INVALID_ARG          # flag missing
+    assert table(pre, 0.0, pre1) == _lib.PG_ERR_INVALID_ARG        # no RoPE
+    assert table(pre, 1e4, pre1 - 1) == _lib.PG_ERR_INVALID_ARG    # workspace too small
+
+    def gemm(M, N, K, ldc, hd, tab_ptr, rows):
+        return L.pg_gemm_bf16_rope(M, N, K, p, K, p, K, p, ldc, hd, tab_ptr, rows, None)
+
+    assert gemm(256, 384, 64, 384, 96, p, 256) == _lib.PG_ERR_INVALID_ARG     # head_dim
+    assert gemm(256, 320, 64, 320, 128, p, 256) == _lib.PG_ERR_INVALID_ARG    # N % head_dim
+    assert gemm(256, 384, 64, 384, 128, p, 255) == _lib.PG_ERR_INVALID_ARG    # table too short
+    assert gemm(256, 384, 64, 384, 128, None, 256) == _lib.PG_ERR_INVALID_ARG  # no table
+    assert gemm(256, 384, 64, 388, 128, p, 256) == _lib.PG_ERR_INVALID_ARG    # ldc % 8
+    assert gemm(256, 384, 64, 384, 96, p, 256) == _lib.PG_ERR_INVALID_ARG
+    assert b"head_dim" in L.pg_last_error_message()

@@ -1,7 +1,8 @@
 """GPU parity of the decoder layer (GEMMs, RMSNorm, SwiGLU, grouped attention through the C ABI).
 
 * a small layer (head_dim 128, hidden 256) against the fp64 CPU layer oracle (repeated-prefix
-  baseline), outputs, input gradient and every parameter gradient, normwise <= 2e-2;
+  baseline), outputs, input gradient and every parameter gradient, normwise <= 2e-2, with RoPE
+  applied in the q / k projections' GEMM epilogue (the default) and by the attention call;
 * the full decoder-layer workload (hidden 4096, 32/8 heads, MLP 14336, B=2, P=8192, G=8, R=1024)
   against the same GPU kernels run on the materialised repeated-prefix layout (every [P; Ri] as
   its own sequence), which the pages say must give identical outputs and parameter gradients.
@@ -25,7 +26,7 @@ def built():
     build()
 
 
-def run_layer(prob, prefix_lens, group_sizes, suffix_lens, x, dy):
+def run_layer(prob, prefix_lens, group_sizes, suffix_lens, x, dy, fused_rope=True):
     w = prob.workload
     dev = torch.device("cuda")
     lay = api.pack(prefix_lens, group_sizes, suffix_lens, dev)
@@ -33,17 +34,19 @@ def run_layer(prob, prefix_lens, group_sizes, suffix_lens, x, dy):
     kw = dict(heads_q=w.heads_q, heads_kv=w.heads_kv, head_dim=w.head_dim, rope_theta=w.rope_theta,
               eps=w.rms_eps)
     x, dy = x.to(dev), dy.to(dev)
-    y, saved = layer.layer_fwd(lay, x, *W, **kw)
+    y, saved = layer.layer_fwd(lay, x, *W, fused_rope=fused_rope, **kw)
     g = layer.layer_bwd(lay, x, *W, saved, dy, **kw)
     torch.cuda.synchronize()
     assert api.device_status() == 0
     return y, g
 
 
-def test_small_layer_matches_oracle():
+@pytest.mark.parametrize("fused_rope", [True, False], ids=["rope_in_gemm", "rope_in_attn"])
+def test_small_layer_matches_oracle(fused_rope):
     w = workloads.small_layer()
     prob = workloads.make_layer_problem(w, suffix_lens=[70, 1, 129, 64, 30, 200])
-    y, g = run_layer(prob, prob.prefix_lens, prob.group_sizes, prob.suffix_lens, prob.x, prob.dy)
+    y, g = run_layer(prob, prob.prefix_lens, prob.group_sizes, prob.suffix_lens, prob.x, prob.dy,
+                     fused_rope)
     W = (prob.w_qkv, prob.w_o, prob.w_gu, prob.w_d, prob.g1, prob.g2)
     ref = lo.layer_repeated(prob.prefix_lens, prob.group_sizes, prob.suffix_lens, prob.x, prob.dy,
                             W, heads_q=w.heads_q, heads_kv=w.heads_kv, head_dim=w.head_dim,
