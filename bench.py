@@ -492,6 +492,8 @@ def repeated_leg(prob, device, flags, grouped_sec, args):
     del rstep
     torch.cuda.empty_cache()
     return {"ms_per_step": sec * 1e3, "tokens": rep.total_tokens,
+            # the repeated layout's tokens the grouped step covers per second
+            "baseline_equivalent_tokens_per_s": rep.total_tokens / grouped_sec,
             "counted_tflops": flops.attn_flops(rep_pairs, w.heads_q, w.head_dim) / sec / 1e12,
             "speedup_grouped_vs_repeated": sec / grouped_sec,
             "pair_ratio_grouped_over_repeated":
