@@ -32,15 +32,16 @@ sys.path.insert(0, ROOT)
 from shared_prefix_grouped_gb300 import _lib, api, flops, workloads  # noqa: E402
 
 METRIC = "grouped-attn fwd+bwd TFLOP/s, tokens/s & % BF16 peak vs repeated-prefix (1 GB300)"
-DEFAULT_WORKLOAD = workloads.WORKLOADS[1].name
+# The long-prefix GRPO shape: one group, P=16384, G=16 responses of U[256,1024] tokens, GQA 32/8.
+DEFAULT_WORKLOAD = workloads.WORKLOADS[3].name
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 L2_BYTES = 129 * 2 ** 20
-# DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu capture summarised
-# in profiles/attn_bwd_sm100_bf16_mha_h32_d128_p4096_g8_r512.md.  Reported only while the kernel
-# source still has the hash it had when the counters were taken, and only for that workload.
+# DRAM bytes (read + write) of one launch of the dominant kernel, from the committed ncu capture of
+# this kernel on this workload.  Reported only while the kernel source still has the hash it had
+# when the counters were taken, and only for that workload.
 TRAFFIC = {"file": "shared_prefix_grouped_gb300/csrc/pg_attn_bwd_sm100.cu",
            "sha256": "995768ee7d7a309aa39a392afdb56533133341bf7ea70ff884b12baac4da27d0",
-           "workload": "bf16_mha_h32_d128_p4096_g8_r512", "bytes": 663095552}
+           "workload": "bf16_gqa32x8_d128_p16384_g16_r256-1024", "bytes": 3222228000}
 
 
 def key_major_flops(pairs: int, w, deterministic: bool) -> float:
@@ -215,11 +216,15 @@ def oracle_sample(prob, head: int, n_resp: int):
 
 
 def cpu_baseline_leg(prob, budget_s=12.0, max_s=30.0):
+    """The oracle on a bounded sample: group 0's prefix and its first n responses, one query head
+    at a time, n sized from a one-response probe so the whole leg stays within ~10-30 s."""
     w = prob.workload
     G = prob.group_sizes[0]
+    dt1, _ = oracle_sample(prob, 0, 1)
+    n_resp = G if dt1 * G <= max_s else max(1, int(budget_s / dt1))
     total_t, total_f, heads = 0.0, 0.0, 0
     for h in range(w.heads_q):
-        dt, fl = oracle_sample(prob, h, G)
+        dt, fl = oracle_sample(prob, h, n_resp)
         total_t += dt
         total_f += fl
         heads += 1
@@ -227,8 +232,8 @@ def cpu_baseline_leg(prob, budget_s=12.0, max_s=30.0):
             break
     return {"value": total_f / total_t / 1e12, "unit": "TFLOP/s", "cores": torch.get_num_threads(),
             "kind": "oracle",
-            "sample": f"group 0, all {G} responses, {heads} of {w.heads_q} query heads, "
-                      f"fp64 repeated-prefix forward+backward, {total_t:.1f} s"}
+            "sample": f"group 0, prefix + {n_resp} of {G} responses, {heads} of {w.heads_q} query "
+                      f"heads, fp64 repeated-prefix forward+backward, {total_t:.1f} s"}
 
 
 def run_reference(args):
@@ -386,7 +391,7 @@ def run_ours(args):
             "clocks": clocks, "gpu_launches": int(prof.launches)}
     if rank == 0 and not args.skip_extras:
         line["e2e"] = e2e_leg(step, prob, device, args, step_flops, world)
-        line["repeated_prefix"] = repeated_leg(prob, device, flags, sec, args)
+        line["repeated_prefix"] = repeated_leg(prob, device, flags, sec, args, grouped=step)
         if world == 1:
             line["cpu_baseline"] = cpu_baseline_leg(prob)
     if rank == 0:
@@ -459,27 +464,38 @@ def e2e_leg(step, prob, device, args, step_flops, world):
             "pipelining": "H2D of step i+1 and D2H of step i-1 overlap step i (two buffer sets)"}
 
 
-def repeated_leg(prob, device, flags, grouped_sec, args):
+def repeated_leg(prob, device, flags, grouped_sec, args, grouped=None):
     """The same attention as the repeated-prefix baseline on this GPU: every [P; Ri] materialised
-    as its own sequence and run through the same kernels."""
+    as its own sequence and run through the same kernels, timed, and (given the grouped step)
+    compared with the grouped outputs.
+
+    Upstream gradients at prefix rows go into each group's first copy only (zero in the others),
+    so the repeated layout's gradients, summed over copies for prefix rows, are the gradients of
+    the packed function.  Mapped back: O / LSE rows from the copy that holds each packed row's
+    upstream gradient (prefix rows from copy 0, response rows from their own copy), dQ / dK / dV
+    summed over copies.  Errors are normwise (max|grouped - repeated| / max|repeated| per
+    tensor)."""
     w = prob.workload
-    lps, gss, rss, idx = [], [], [], []
+    lps, gss, rss, idx, keep = [], [], [], [], []
     s = 0
     g0 = 0
     for b, (lp, G) in enumerate(zip(prob.prefix_lens, prob.group_sizes)):
         seg0 = g0 + lp
-        for i in range(G):
-            r = prob.suffix_lens[s + i]
+        for i in range(max(G, 1)):
+            r = prob.suffix_lens[s + i] if G else 0
             lps.append(lp)
             gss.append(1)
             rss.append(r)
             idx.append(torch.arange(g0, g0 + lp))
             idx.append(torch.arange(seg0, seg0 + r))
+            keep.append(torch.full((lp,), i == 0, dtype=torch.bool))
+            keep.append(torch.ones(r, dtype=torch.bool))
             seg0 += r
         g0 = seg0
         s += G
-    idx = torch.cat(idx)
-    rep = workloads.Problem(w, lps, gss, rss, prob.q[idx], prob.k[idx], prob.v[idx], prob.do[idx])
+    idx, keep = torch.cat(idx), torch.cat(keep)
+    do_rep = prob.do[idx] * keep[:, None, None].to(prob.do.dtype)
+    rep = workloads.Problem(w, lps, gss, rss, prob.q[idx], prob.k[idx], prob.v[idx], do_rep)
     try:
         rstep = Step(rep, device, flags)
     except torch.cuda.OutOfMemoryError:
@@ -489,15 +505,45 @@ def repeated_leg(prob, device, flags, grouped_sec, args):
     n = max(3, min(args.steps, 10))
     sec = time_steps(rstep, n, device)
     rep_pairs = rstep.layout.pairs
+    out = {"ms_per_step": sec * 1e3, "tokens": rep.total_tokens,
+           # the repeated layout's tokens the grouped step covers per second
+           "baseline_equivalent_tokens_per_s": rep.total_tokens / grouped_sec,
+           "counted_tflops": flops.attn_flops(rep_pairs, w.heads_q, w.head_dim) / sec / 1e12,
+           "speedup_grouped_vs_repeated": sec / grouped_sec,
+           "pair_ratio_grouped_over_repeated":
+               flops.total_pairs(prob.prefix_lens, prob.group_sizes, prob.suffix_lens) / rep_pairs}
+    if grouped is not None:
+        grouped()
+        rstep()
+        torch.cuda.synchronize(device)
+        errs = equivalence_errors(grouped, rstep, idx.to(device), keep.to(device))
+        out["normwise_err"] = errs
+        out["max_normwise_err"] = max(errs.values())
+        out["equivalence"] = ("grouped vs repeated-prefix on this GPU: O, LSE from the copy holding "
+                              "each row's upstream gradient, dQ/dK/dV summed over copies")
     del rstep
     torch.cuda.empty_cache()
-    return {"ms_per_step": sec * 1e3, "tokens": rep.total_tokens,
-            # the repeated layout's tokens the grouped step covers per second
-            "baseline_equivalent_tokens_per_s": rep.total_tokens / grouped_sec,
-            "counted_tflops": flops.attn_flops(rep_pairs, w.heads_q, w.head_dim) / sec / 1e12,
-            "speedup_grouped_vs_repeated": sec / grouped_sec,
-            "pair_ratio_grouped_over_repeated":
-                flops.total_pairs(prob.prefix_lens, prob.group_sizes, prob.suffix_lens) / rep_pairs}
+    return out
+
+
+def equivalence_errors(g, r, idx, keep):
+    """Normwise errors of the grouped step's outputs against the repeated step's, mapped back."""
+    T = g.q.shape[0]
+    sel = idx[keep]
+    errs = {}
+    for name in ("o", "lse", "dq", "dk", "dv"):
+        x, y = getattr(g, name).float(), getattr(r, name).float()
+        if name == "lse":
+            ref = torch.empty_like(x)
+            ref[:, sel] = y[:, keep]
+        elif name == "o":
+            ref = torch.empty_like(x)
+            ref[sel] = y[keep]
+        else:
+            ref = torch.zeros((T,) + tuple(x.shape[1:]), dtype=torch.float32, device=x.device)
+            ref.index_add_(0, idx, y)
+        errs[name] = float((x - ref).abs().max() / ref.abs().max())
+    return errs
 
 
 SCORE_METRIC = ("grouped-attn responses-only forward (scoring) TFLOP/s & HBM GB/s "

@@ -45,7 +45,9 @@ Readings of points the pages leave open (all stated here so a reader can check t
 Parity unpinned: none.  Every function here is pinned by tests that do not call it alone: the
 packing by hand-computed fixtures, RoPE by its complex-number form and group properties, attention by
 torch's own scaled_dot_product_attention and autograd (G = 1 and Lp = 0 reduce to that routine),
-finite differences, closed forms (Q = 0, constant V) and the packed dense-mask formulation.
+finite differences, closed forms (Q = 0, constant V) and the packed dense-mask formulation; the
+comparison helper normwise_error by hand-worked values (denominator, sign, the skipped non-finite
+reference entries, a NaN in the compared tensor, the near-zero branch).
 """
 from __future__ import annotations
 

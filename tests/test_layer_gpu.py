@@ -3,6 +3,9 @@
 * a small layer (head_dim 128, hidden 256) against the fp64 CPU layer oracle (repeated-prefix
   baseline), outputs, input gradient and every parameter gradient, normwise <= 2e-2, with RoPE
   applied in the q / k projections' GEMM epilogue (the default) and by the attention call;
+* the layer at the full workload's dimensions (hidden 4096, 32/8 heads, head_dim 128, MLP 14336,
+  RoPE 5e5) on a short ragged batch (two groups, T = 862) against the same oracle, so every GEMM
+  runs at its full K and N;
 * the full decoder-layer workload (hidden 4096, 32/8 heads, MLP 14336, B=2, P=8192, G=8, R=1024)
   against the same GPU kernels run on the materialised repeated-prefix layout (every [P; Ri] as
   its own sequence), which the pages say must give identical outputs and parameter gradients.
@@ -53,6 +56,21 @@ def test_small_layer_matches_oracle(fused_rope):
                             theta=w.rope_theta, eps=w.rms_eps)
     got = dict(y=y, dx=g.dx, w_qkv=g.w_qkv, w_o=g.w_o, w_gu=g.w_gu, w_d=g.w_d, g1=g.g1, g2=g.g2)
     errs = {n: orc.normwise_error(t.float().cpu(), getattr(ref, n)) for n, t in got.items()}
+    assert all(e <= TOL for e in errs.values()), errs
+
+
+def test_full_dims_layer_matches_oracle():
+    w = workloads.dataclasses.replace(workloads.LayerWorkload(), name="llama_layer_full_dims_short",
+                                      prefix_len=200, group_size=3, num_groups=2)
+    prob = workloads.make_layer_problem(w, suffix_lens=[40, 1, 130, 64, 77, 150])
+    y, g = run_layer(prob, prob.prefix_lens, prob.group_sizes, prob.suffix_lens, prob.x, prob.dy)
+    W = (prob.w_qkv, prob.w_o, prob.w_gu, prob.w_d, prob.g1, prob.g2)
+    ref = lo.layer_repeated(prob.prefix_lens, prob.group_sizes, prob.suffix_lens, prob.x, prob.dy,
+                            W, heads_q=w.heads_q, heads_kv=w.heads_kv, head_dim=w.head_dim,
+                            theta=w.rope_theta, eps=w.rms_eps)
+    got = dict(y=y, dx=g.dx, w_qkv=g.w_qkv, w_o=g.w_o, w_gu=g.w_gu, w_d=g.w_d, g1=g.g1, g2=g.g2)
+    errs = {n: orc.normwise_error(t.float().cpu(), getattr(ref, n)) for n, t in got.items()}
+    print(errs)
     assert all(e <= TOL for e in errs.values()), errs
 
 

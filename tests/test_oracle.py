@@ -428,3 +428,58 @@ def test_tree_layout_matches_hand_fixture():
     lens = fx["seg_lens"]
     assert sum(n * (n + 1) // 2 for n in (sum(lens[a] for a in p) for p in fx["paths"])) == \
         fx["repeated_pairs"]
+
+
+# ------------------------------------------------------------------ the comparison helper ------
+
+def test_normwise_error_hand_computed_values():
+    """normwise_error = max|x - ref| / max|ref| over the finite entries of ref, values worked by
+    hand: a wrong denominator (max|x|, a mean, an elementwise ratio), a dropped abs() or a NaN
+    swallowed by the max would each change one of these."""
+    nan, inf = float("nan"), float("inf")
+    ref = torch.tensor([[1.0, -4.0], [2.0, 0.5]], dtype=F64)
+    assert orc.normwise_error(ref.clone(), ref) == 0.0
+    x = ref.clone()
+    x[0, 1] = -3.0                        # |diff| 1, max|ref| 4
+    assert orc.normwise_error(x, ref) == 0.25
+    x = ref.clone()
+    x[1, 1] = 0.25                        # |diff| 0.25 on the smallest entry: 0.25 / 4
+    assert orc.normwise_error(x, ref) == 0.0625
+    x = ref.clone()
+    x[0, 0] = 9.0                         # |diff| 8; max|x| = 9 must not be the denominator
+    assert orc.normwise_error(x, ref) == 2.0
+    x = ref.clone()
+    x[1, 0] = -2.0                        # sign error: |diff| 4
+    assert orc.normwise_error(x, ref) == 1.0
+    # x in a narrower dtype is upcast, not compared in its own precision
+    assert orc.normwise_error(ref.float(), ref) == 0.0
+    assert orc.normwise_error(torch.tensor([1.5], dtype=torch.bfloat16),
+                              torch.tensor([2.0], dtype=F64)) == 0.25
+
+
+def test_normwise_error_non_finite_entries():
+    nan, inf = float("nan"), float("inf")
+    ref = torch.tensor([1.0, -4.0, 2.0], dtype=F64)
+    # a NaN or inf in x where ref is finite must fail any tolerance
+    for bad in (nan, inf, -inf):
+        x = ref.clone()
+        x[2] = bad
+        e = orc.normwise_error(x, ref)
+        assert not e <= 1e30, (bad, e)
+    # entries where ref is not finite (heads or groups the oracle did not compute) are skipped,
+    # also for the denominator
+    ref2 = torch.tensor([1.0, nan, -2.0, inf], dtype=F64)
+    x = torch.tensor([1.5, 123.0, -2.0, -7.0], dtype=F64)
+    assert orc.normwise_error(x, ref2) == 0.25
+    assert orc.normwise_error(x, torch.full((4,), nan, dtype=F64)) == 0.0
+
+
+def test_normwise_error_zero_reference_is_absolute():
+    # A reference that is zero up to rounding (max|ref| < 1e-12) is compared absolutely.
+    ref = torch.tensor([0.0, 5e-13, -1e-13], dtype=F64)
+    x = torch.tensor([3e-13, -2e-3, 0.0], dtype=F64)
+    assert math.isclose(orc.normwise_error(x, ref), 2e-3 + 5e-13, rel_tol=1e-12)
+    # at and above the threshold the error is relative again
+    ref = torch.tensor([1e-12, 0.0], dtype=F64)
+    x = torch.tensor([2e-12, 0.0], dtype=F64)
+    assert math.isclose(orc.normwise_error(x, ref), 1.0, rel_tol=1e-12)
