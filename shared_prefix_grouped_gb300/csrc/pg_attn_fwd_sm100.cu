@@ -5,23 +5,30 @@
 // prefix [g0, p_end) -- every response row sees all of it, prefix rows causally -- then the
 // responses' part [s_lo, s_hi) (Pith review of Prefix Grouper, "What carries the argument": prefix
 // self-attention plus suffix attention over the prefix and the row's own response).  Both query
-// tiles share each K/V tile loaded into shared memory, and all CTAs of a group read the same
-// prefix K/V tiles, which stay resident in L2 across the group's query tiles and heads.
+// tiles share each K/V tile loaded into shared memory, and the CTAs run in chunks of query heads
+// that share a few key/value heads (the query heads of one KV head side by side on the same query
+// tile), so a group's prefix K/V tiles are read from DRAM about once per chunk and served from L2
+// to every query tile of the group -- the prefix is encoded once, not once per response.
 //
-// Warp roles (352 threads):
-//   warp 0      TMA producer: Q tiles once, then 64-key K and V tiles into a 4-stage ring
-//   warp 1      TMEM allocation and the score MMAs, warp 10 the P V MMAs (one elected thread
-//               each, so both kinds are queued on the tensor core at once), per key tile j and
-//               query tile i:
-//                 S_i = Q_i K_j^T   (M 128 x N 64 keys x K 128; fp32 TMEM columns [64 i, 64 i + 64))
-//                 O_i += P_i V_j    (M 128 x N 128 dims x K 64; fp32 TMEM columns [128 + 128 i, ...)),
-//                                   with P_i read from TMEM (bf16, columns [384 + 64 i + 32 b, ...)
-//                                   for buffer b) and V from shared memory
+// Key tiles are 128 keys wide, so the score product runs at the full MMA rate (N = 128):
+//   S_i = Q_i K_j^T   M 128 rows x N 128 keys x K 128 dims, fp32 in TMEM columns [128 i, 128 i + 128)
+//   O_i += P_i V_j    M 128 rows x N 128 dims x K 128 keys, fp32 in TMEM columns [256 + 128 i, ...)
+// P_i (bf16) is written over the first 64 columns of S_i, from which the P V product reads it as
+// its A operand.  One thread issues every MMA, in the order
+//   ... P V of tile 0 (key tile j), S of tile 0 (key tile j + 1), P V of tile 1 (j), S of tile 1 (j + 1) ...
+// so the tensor core, which executes a CTA's MMAs in issue order, finishes reading P_i(j) before
+// S_i(j + 1) overwrites those columns, and while the softmax of one query tile runs the tensor
+// core works on the other tile's products.
+//
+// Warp roles (320 threads):
+//   warp 0      TMA producer: Q tiles once, then 128-key K tiles into a 3-stage ring and V tiles
+//               into a 2-stage ring, K one tile ahead of V (K is needed first)
+//   warp 1      TMEM allocation and the MMA issuer (one elected thread)
 //   warps 2..5  softmax of query tile 0, warps 6..9 of query tile 1: one thread per query row
 //               (TMEM lane = row); S from TMEM to registers, masking, online max / sum in fp32
-//               (exp2 with the scale folded in), P rounded to bf16 and stored into TMEM (the A
-//               operand of P V, double-buffered), O rescaled in TMEM only when the running max
-//               grows by more than 2^8, and the final O / l, LSE epilogue.
+//               (exp2 with the scale folded in), P rounded to bf16 and stored into TMEM, O
+//               rescaled in TMEM only when the running max grows by more than 2^8, and the final
+//               O / l, LSE epilogue.
 // A key tile that lies entirely after the last row of query tile 0 is skipped for that tile.
 //
 // Every mbarrier wait is bounded (PG_ERR_TIMEOUT in the status word, then an orderly exit: copies
@@ -40,11 +47,12 @@ namespace {
 
 constexpr int D = 128;          // head_dim
 constexpr int BM = 128;         // query rows per query tile (two per CTA)
-constexpr int BN = 64;          // keys per tile
-constexpr int NS = 4;           // K/V pipeline stages
+constexpr int BN = 128;         // keys per tile
+constexpr int NSK = 3;          // K pipeline stages
+constexpr int NSV = 2;          // V pipeline stages
 constexpr uint32_t QHALF = BM * 64 * 2;    // [128 rows][64 dims] bf16: 16 KiB
-constexpr uint32_t KHALF = BN * 64 * 2;    // [64 keys][64 dims] bf16: 8 KiB
-constexpr int NTHREADS = 352;
+constexpr uint32_t KHALF = BN * 64 * 2;    // [128 keys][64 dims] bf16: 16 KiB
+constexpr int NTHREADS = 320;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -98,14 +106,14 @@ struct TileCursor {
 
 struct FwdSmem {
   uint8_t q[2][2 * QHALF];
-  uint8_t k[NS][2 * KHALF];
-  uint8_t v[NS][2 * KHALF];
+  uint8_t k[NSK][2 * KHALF];
+  uint8_t v[NSV][2 * KHALF];
   uint64_t q_full;
-  uint64_t k_full[NS], v_full[NS], kv_empty[NS];
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full[2][2];    // P of [query tile][buffer] written
-  uint64_t pv_done[2][2];   // the P V product reading [query tile][buffer] has completed
-  uint64_t mma_done, mma_done2;
+  uint64_t k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV];
+  uint64_t s_full[2];       // S of [query tile] complete
+  uint64_t p_full[2];       // P of [query tile] written (128 softmax threads)
+  uint64_t pv_done[2];      // the P V product of [query tile] has completed
+  uint64_t mma_done;
   uint32_t tmem;
   Plan plan;
 };
@@ -118,18 +126,67 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 __device__ __forceinline__ void fail(int code) { atomicCAS(&s_status_fwd, 0, code); }
 
+// 64 consecutive fp32 columns of this thread's TMEM lane into registers.
+__device__ __forceinline__ void load64(uint32_t taddr, uint32_t (&r)[64]) {
+  tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+  tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+  tmem_ld_wait();
+}
+
+// Max of 64 raw scores (columns c0 .. c0 + 63 of the tile); with kMasked, columns outside the
+// visible run [lo, lo + len) count as -inf.
+template <bool kMasked>
+__device__ __forceinline__ float max64(const uint32_t (&r)[64], int c0, int lo, int len) {
+  float mx = -INFINITY;
+#pragma unroll
+  for (int cc = 0; cc < 64; ++cc) {
+    const float x = __uint_as_float(r[cc]);
+    mx = fmaxf(mx, (!kMasked || (unsigned)(c0 + cc - lo) < (unsigned)len) ? x : -INFINITY);
+  }
+  return mx;
+}
+
+// P = exp2(s * scale_log2 - mref) of 64 columns (c0 ..), rounded to bf16 and stored to TMEM
+// columns [p_addr, p_addr + 32); returns the sum of the fp32 values.
+template <bool kMasked>
+__device__ __forceinline__ float exp64(const uint32_t (&r)[64], int c0, int lo, int len,
+                                       float scale_log2, float mref, uint32_t p_addr) {
+  float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t pw[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int cc = 32 * h + 2 * e;
+      float x0 = __uint_as_float(r[cc]), x1 = __uint_as_float(r[cc + 1]);
+      if (kMasked) {
+        x0 = (unsigned)(c0 + cc - lo) < (unsigned)len ? x0 : -INFINITY;
+        x1 = (unsigned)(c0 + cc + 1 - lo) < (unsigned)len ? x1 : -INFINITY;
+      }
+      const float p0 = fast_exp2(fmaf(x0, scale_log2, -mref));
+      const float p1 = fast_exp2(fmaf(x1, scale_log2, -mref));
+      sum0 += p0;
+      sum1 += p1;
+      pw[e] = pack_bf16x2(p0, p1);
+    }
+    tmem_st16(p_addr + 16 * h, pw);
+  }
+  return sum0 + sum1;
+}
+
 __global__ void __launch_bounds__(NTHREADS, 1)
 attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ o,
                       float* __restrict__ lse, const int4* __restrict__ tok,
                       const FwdTile* __restrict__ tiles, const int2* __restrict__ ivs,
                       float* __restrict__ lse2_out, int64_t ldl, int Hq, int Hkv, int Ttot,
-                      float scale_log2, uint64_t wait_ns, uint32_t debug) {
+                      float scale_log2, int hc, uint64_t wait_ns, uint32_t debug) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   FwdSmem& sm = *reinterpret_cast<FwdSmem*>(base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile_id = blockIdx.x / Hq, h = blockIdx.x % Hq;
+  int tile_id, h;
+  chunked_order(blockIdx.x, gridDim.x / Hq, Hq, hc, tile_id, h);
   const int kh = h / (Hq / Hkv);
   const FwdTile tl = tiles[tile_id];
   if (tl.q0 < 0 || tl.q1 > Ttot || tl.q0 >= tl.q1 || tl.q1 - tl.q0 > 2 * BM || tl.g0 < 0 ||
@@ -141,21 +198,20 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
 
   if (threadIdx.x == 0) {
     mbar_init(&sm.q_full, 1);
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < NSK; ++s) {
       mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.k_empty[s], 1);
+    }
+    for (int s = 0; s < NSV; ++s) {
       mbar_init(&sm.v_full[s], 1);
-      mbar_init(&sm.kv_empty[s], 1);
+      mbar_init(&sm.v_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.s_full[i], 1);
-      mbar_init(&sm.s_free[i], 128);
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(&sm.p_full[i][b], 128);
-        mbar_init(&sm.pv_done[i][b], 1);
-      }
+      mbar_init(&sm.p_full[i], 128);
+      mbar_init(&sm.pv_done[i], 1);
     }
     mbar_init(&sm.mma_done, 1);
-    mbar_init(&sm.mma_done2, 1);
     fence_mbar_init();
     sm.plan.init(tl, ivs);
   }
@@ -185,104 +241,119 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
         tma_load_2d(sm.q[i], &tq, &sm.q_full, xq, tl.q0 + i * BM);
         tma_load_2d(sm.q[i] + QHALF, &tq, &sm.q_full, xq + 64, tl.q0 + i * BM);
       }
-      int issued = 0;
+      // K(j + 1) is issued before V(j): the score product of key tile j + 1 follows the P V
+      // product of key tile j closely, and the deeper K ring gives its load the longer lead.
+      int k_issued = 0, v_issued = 0;
+      bool ok = true;
       TileCursor cur(pl);
-      for (int j = 0; j < n; ++j) {
-        const int s = j % NS;
-        if (!mbar_wait(&sm.kv_empty[s], ((j / NS) & 1) ^ 1, wait_ns)) {
-          fail(PG_ERR_TIMEOUT);
-          break;
-        }
+      auto load_k = [&](int j) -> bool {
+        const int s = j % NSK;
+        if (!mbar_wait(&sm.k_empty[s], ((j / NSK) & 1) ^ 1, wait_ns)) return false;
         const int kt = cur.seek(pl, j);
         mbar_expect_tx(&sm.k_full[s], 2 * KHALF);
         tma_load_2d(sm.k[s], &tk, &sm.k_full[s], xk, kt);
         tma_load_2d(sm.k[s] + KHALF, &tk, &sm.k_full[s], xk + 64, kt);
+        ++k_issued;
+        return true;
+      };
+      TileCursor vcur(pl);
+      auto load_v = [&](int j) -> bool {
+        const int s = j % NSV;
+        if (!mbar_wait(&sm.v_empty[s], ((j / NSV) & 1) ^ 1, wait_ns)) return false;
+        const int kt = vcur.seek(pl, j);
         mbar_expect_tx(&sm.v_full[s], 2 * KHALF);
         tma_load_2d(sm.v[s], &tv, &sm.v_full[s], xk, kt);
         tma_load_2d(sm.v[s] + KHALF, &tv, &sm.v_full[s], xk + 64, kt);
-        ++issued;
+        ++v_issued;
+        return true;
+      };
+      if (n > 0) ok = load_k(0);
+      for (int j = 0; ok && j < n; ++j) {
+        if (j + 1 < n && !load_k(j + 1)) { ok = false; break; }
+        if (!load_v(j)) { ok = false; break; }
       }
+      if (!ok) fail(PG_ERR_TIMEOUT);
       // Leave no copy in flight: the last stages' loads must have landed before exit.
       mbar_wait(&sm.q_full, 0, wait_ns);
-      for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j) {
-        mbar_wait(&sm.k_full[j % NS], (j / NS) & 1, wait_ns);
-        mbar_wait(&sm.v_full[j % NS], (j / NS) & 1, wait_ns);
-      }
+      for (int j = (k_issued > NSK ? k_issued - NSK : 0); j < k_issued; ++j)
+        mbar_wait(&sm.k_full[j % NSK], (j / NSK) & 1, wait_ns);
+      for (int j = (v_issued > NSV ? v_issued - NSV : 0); j < v_issued; ++j)
+        mbar_wait(&sm.v_full[j % NSV], (j / NSV) & 1, wait_ns);
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ score MMAs -------
+    // ------------------------------------------------------------------ MMA issuer -------
     if (elect_one()) {
       constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
-      int n_s[2] = {0, 0};        // S products issued per query tile
-      bool ok = mbar_wait(&sm.q_full, 0, wait_ns);
+      constexpr uint32_t idesc_pv = idesc_bf16(BM, D, 0, 1);
       // Descriptor bases: buffers of a kind are contiguous, so buffer n is base + n * stride.
       const uint64_t qd0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
       const uint64_t kd0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
-      // S_i(j): scores of query tile i against key tile j.  Needs the K tile and the softmax of
-      // tile i to have read its previous scores out of TMEM (S_i is single-buffered).
-      TileCursor cur(pl);
-      for (int j = 0; ok && j < n; ++j) {
-        const int kt = cur.seek(pl, j);
-        for (int i = 0; i < nq; ++i) {
-          if (!rel(i, kt)) continue;
-          if (!mbar_wait(&sm.k_full[j % NS], (j / NS) & 1, wait_ns)) { ok = false; break; }
-          if (n_s[i] > 0 && !mbar_wait(&sm.s_free[i], (n_s[i] - 1) & 1, wait_ns)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t qd = desc_add(qd0, i * 2 * QHALF);
-          const uint64_t kd = desc_add(kd0, (j % NS) * 2 * KHALF);
-          const uint32_t ts = tmem + 64 * i;
+      // V as the MN-major B operand of P V: the two 64-dim halves are LBO apart.
+      const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0]), KHALF, 1024);
+      int n_pv[2] = {0, 0};       // P V products issued per query tile
+      bool ok = mbar_wait(&sm.q_full, 0, wait_ns);
+      // Every K and V load phase is waited for, in order, whether or not a query tile uses the
+      // key tile, so a stage is never refilled while its previous load could still be landing.
+      auto wait_k = [&](int j) { return mbar_wait(&sm.k_full[j % NSK], (j / NSK) & 1, wait_ns); };
+      auto wait_v = [&](int j) { return mbar_wait(&sm.v_full[j % NSV], (j / NSV) & 1, wait_ns); };
+      // S_i(j): scores of query tile i against key tile j into TMEM columns [128 i, 128 i + 128).
+      auto issue_s = [&](int i, int j) {
+        tc_fence_after();
+        const uint64_t qd = desc_add(qd0, i * 2 * QHALF);
+        const uint64_t kd = desc_add(kd0, (j % NSK) * 2 * KHALF);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            mma_ss(ts, desc_add(qd, (kk >> 2) * QHALF + (kk & 3) * 32),
-                   desc_add(kd, (kk >> 2) * KHALF + (kk & 3) * 32), idesc_s, kk != 0);
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + 128 * i, desc_add(qd, (kk >> 2) * QHALF + (kk & 3) * 32),
+                 desc_add(kd, (kk >> 2) * KHALF + (kk & 3) * 32), idesc_s, kk != 0);
+        mma_commit(&sm.s_full[i]);
+      };
+      // O_i += P_i(j) V_j, P_i read from the first 64 columns of S_i.
+      auto issue_pv = [&](int i, int j) -> bool {
+        if (!mbar_wait(&sm.p_full[i], n_pv[i] & 1, wait_ns)) return false;
+        tc_fence_after();
+        const uint64_t vd = desc_add(vd0, (j % NSV) * 2 * KHALF);
+        const uint32_t acc0 = n_pv[i] != 0;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(tmem + 256 + 128 * i, tmem + 128 * i + kk * 8, desc_add(vd, kk * 2048), idesc_pv,
+                 kk == 0 ? acc0 : 1u);
+        mma_commit(&sm.pv_done[i]);
+        ++n_pv[i];
+        return true;
+      };
+      TileCursor cur(pl);
+      int kt_next = n > 0 ? cur.seek(pl, 0) : 0;
+      if (ok && n > 0) {
+        ok = wait_k(0);
+        for (int i = 0; ok && i < nq; ++i)
+          if (rel(i, kt_next)) issue_s(i, 0);
+        mma_commit(&sm.k_empty[0]);
+      }
+      for (int j = 0; ok && j < n; ++j) {
+        const int kt = kt_next;
+        const bool more = j + 1 < n;
+        kt_next = more ? cur.seek(pl, j + 1) : 0;
+        if (!wait_v(j)) { ok = false; break; }
+        bool k_ready = !more;
+        for (int i = 0; ok && i < nq; ++i) {
+          if (rel(i, kt) && !issue_pv(i, j)) { ok = false; break; }
+          if (more && rel(i, kt_next)) {
+            if (!k_ready && !(k_ready = wait_k(j + 1))) { ok = false; break; }
+            issue_s(i, j + 1);
           }
-          mma_commit(&sm.s_full[i]);
-          ++n_s[i];
         }
+        if (!ok) break;
+        if (!k_ready && !wait_k(j + 1)) { ok = false; break; }
+        // A stage is free once every product issued so far has completed: V_j after both P V
+        // products of key tile j, K_{j+1} after both score products of key tile j + 1.
+        mma_commit(&sm.v_empty[j % NSV]);
+        if (more) mma_commit(&sm.k_empty[(j + 1) % NSK]);
       }
       if (!ok) fail(PG_ERR_TIMEOUT);
       // Every MMA issued above completes before TMEM is released.
       mma_commit(&sm.mma_done);
       mbar_wait(&sm.mma_done, 0, wait_ns);
-    }
-    __syncwarp();
-  } else if (warp == 10) {
-    // ------------------------------------------------------------------ P V MMAs ---------
-    // A second issuing thread: the products of P with V are queued while the next scores are
-    // still being issued.  Ordering with the score MMAs goes through the barriers (a key tile's
-    // scores completed before its P was written).
-    if (elect_one()) {
-      constexpr uint32_t idesc_pv = idesc_bf16(BM, D, 0, 1);
-      int n_pv[2] = {0, 0};       // P V products issued per query tile
-      const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0]), KHALF, 1024);
-      bool ok = true;
-      TileCursor cur(pl);
-      for (int j = 0; ok && j < n; ++j) {
-        const int kt = cur.seek(pl, j);
-        if (!mbar_wait(&sm.v_full[j % NS], (j / NS) & 1, wait_ns)) { ok = false; break; }
-        for (int i = 0; i < nq && ok; ++i) {
-          if (!rel(i, kt)) continue;
-          const int b = n_pv[i] & 1;
-          if (!mbar_wait(&sm.p_full[i][b], (n_pv[i] >> 1) & 1, wait_ns)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t pt = tmem + 384 + 64 * i + 32 * b, to = tmem + 128 + 128 * i;
-          const uint64_t vd = desc_add(vd0, (j % NS) * 2 * KHALF);
-          const uint32_t acc0 = n_pv[i] != 0;
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(to, pt + kk * 8, desc_add(vd, kk * 2048), idesc_pv, kk == 0 ? acc0 : 1u);
-          mma_commit(&sm.pv_done[i][b]);
-          ++n_pv[i];
-        }
-        mma_commit(&sm.kv_empty[j % NS]);
-      }
-      if (!ok) fail(PG_ERR_TIMEOUT);
-      mma_commit(&sm.mma_done2);
-      mbar_wait(&sm.mma_done2, 0, wait_ns);
     }
     __syncwarp();
   } else {
@@ -297,7 +368,7 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     const int rowc = valid ? row : (active ? qlast : tl.q0);
     const int4 ti = tok[rowc];                    // {g0, pe, own_lo, pos}
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-    const uint32_t t_s = tmem + 64 * i, t_o = tmem + 128 + 128 * i;
+    const uint32_t t_s = tmem + 128 * i + lane_addr, t_o = tmem + 256 + 128 * i + lane_addr;
     const int first_row = tl.q0 + i * BM;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
@@ -309,38 +380,22 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       if (!rel(i, kt)) continue;
       if (!warp_wait(&sm.s_full[i], c & 1, wait_ns)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sr[64];
-      tmem_ld32(t_s + lane_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(t_s + lane_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&sm.s_free[i]);
-      // Scores in log2 units; mask where the tile is not entirely visible to every row.
+      // The row is handled 64 columns at a time (64 score registers): the max of columns
+      // 64..127 first (values dropped), then columns 0..63 (max, exp2, P), then 64..127 again
+      // (exp2, P).  P of columns [32 h, 32 h + 32) goes to TMEM columns [16 h, 16 h + 16), over
+      // scores this thread has already read.  Masked columns become -inf, so their P is exactly
+      // zero; within one key tile a row's visible keys are one contiguous run of columns: in the
+      // prefix range [kt, min(hi, row + 1)); in the responses' range the same run starting no
+      // earlier than the row's own response (prefix rows get an empty run there).
       const bool full_tile = (j < n_a) && (kt + BN <= hi) && (kt + BN - 1 <= first_row);
-      float mx = -INFINITY;
-      if (full_tile) {
-#pragma unroll
-        for (int cc = 0; cc < BN; ++cc) {
-          const float x = __uint_as_float(sr[cc]) * scale_log2;
-          sr[cc] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
-        }
-      } else {
-        // Within one key tile a row's visible keys are one contiguous run of columns: in the
-        // prefix range [kt, min(hi, row + 1)); in the responses' range the same run starting no
-        // earlier than the row's own response (prefix rows get an empty run there).  One unsigned
-        // compare per column, no branches.
-        const int lo = (j < n_a) ? 0 : max(ti.z - kt, 0);
-        const int len = max(min(hi, rowc + 1) - kt - lo, 0);
-#pragma unroll
-        for (int cc = 0; cc < BN; ++cc) {
-          const bool vis = (unsigned)(cc - lo) < (unsigned)len;
-          const float x = vis ? __uint_as_float(sr[cc]) * scale_log2 : -INFINITY;
-          sr[cc] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
-        }
-      }
-      const float m_new = fmaxf(m_used, mx);
+      const int lo = (j < n_a) ? 0 : max(ti.z - kt, 0);
+      const int len = max(min(hi, rowc + 1) - kt - lo, 0);
+      uint32_t sr[64];
+      load64(t_s + 64, sr);
+      float mx = full_tile ? max64<false>(sr, 64, lo, len) : max64<true>(sr, 64, lo, len);
+      load64(t_s, sr);
+      mx = fmaxf(mx, full_tile ? max64<false>(sr, 0, lo, len) : max64<true>(sr, 0, lo, len));
+      const float m_new = fmaxf(m_used, mx * scale_log2);
       const bool rescale = m_new > m_used + kRescaleThreshold;   // false when m_new is -inf
       float corr = 1.f;
       if (rescale) {
@@ -349,63 +404,42 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
         l *= corr;
       }
       const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-      // P = exp2(s - m), rounded to bf16.
-      uint32_t pw[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const float p0 = fast_exp2(__uint_as_float(sr[2 * e]) - mref);
-        const float p1 = fast_exp2(__uint_as_float(sr[2 * e + 1]) - mref);
-        l += p0 + p1;
-        pw[e] = pack_bf16x2(p0, p1);
-      }
-      // P is double-buffered in TMEM: the product that read this buffer two key tiles ago must
-      // be done.
-      // Rescaling O needs the previous key tile's product done too.
-      const int b = c & 1;
+      // Rescaling O needs the previous key tile's P V product done (it is: its S completed after
+      // it, and a commit covers every earlier product; the wait returns at once).
       const bool any_rescale = __any_sync(0xffffffffu, rescale) && c > 0;
       if (any_rescale) {
-        if (!warp_wait(&sm.pv_done[i][(c - 1) & 1], ((c - 1) >> 1) & 1, wait_ns)) {
-          ok = false;
-          break;
-        }
-      }
-      if (c >= 2 && !warp_wait(&sm.pv_done[i][b], ((c >> 1) - 1) & 1, wait_ns)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (any_rescale) {
+        if (!warp_wait(&sm.pv_done[i], (c - 1) & 1, wait_ns)) { ok = false; break; }
         tc_fence_after();
-        {
 #pragma unroll 1
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t orr[32];
-            tmem_ld32(t_o + lane_addr + q4 * 32, orr);
-            tmem_ld_wait();
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t orr[32];
+          tmem_ld32(t_o + q4 * 32, orr);
+          tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * corr);
-            tmem_st32(t_o + lane_addr + q4 * 32, orr);
-          }
-          tmem_st_wait();
+          for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * corr);
+          tmem_st32(t_o + q4 * 32, orr);
         }
       }
-      tmem_st32(tmem + 384 + 64 * i + 32 * b + lane_addr, pw);
+      l += full_tile ? exp64<false>(sr, 0, lo, len, scale_log2, mref, t_s)
+                     : exp64<true>(sr, 0, lo, len, scale_log2, mref, t_s);
+      load64(t_s + 64, sr);
+      l += full_tile ? exp64<false>(sr, 64, lo, len, scale_log2, mref, t_s + 32)
+                     : exp64<true>(sr, 64, lo, len, scale_log2, mref, t_s + 32);
       tmem_st_wait();
       ++c;
       if (debug & PG_DEBUG_WITHHOLD_P) continue;   // test hook: never signal P (bounded waits)
       tc_fence_before();
-      mbar_arrive(&sm.p_full[i][b]);
+      mbar_arrive(&sm.p_full[i]);
     }
     // Epilogue: O / l and the natural-log LSE.
-    if (active && ok && c > 0 &&
-        warp_wait(&sm.pv_done[i][(c - 1) & 1], ((c - 1) >> 1) & 1, wait_ns)) {
+    if (active && ok && c > 0 && warp_wait(&sm.pv_done[i], (c - 1) & 1, wait_ns)) {
       tc_fence_after();
       const float inv = 1.f / l;
       __nv_bfloat16* orow = o + ((size_t)rowc * Hq + h) * D;
 #pragma unroll 1
       for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t orr[32];
-        tmem_ld32(t_o + lane_addr + q4 * 32, orr);
+        tmem_ld32(t_o + q4 * 32, orr);
         tmem_ld_wait();
         if (valid) {
 #pragma unroll
@@ -459,10 +493,14 @@ pg_status launch_fwd_sm100(const AttnArgs& a, const void* q, const void* k, cons
                   "fwd smem attribute");
   if (st != PG_OK) return st;
   const uint64_t wait_ns = (a.debug & PG_DEBUG_WITHHOLD_P) ? 50000000ull : 2000000000ull;
+  // CTAs in chunks of query heads covering a few whole KV heads (about eight query heads).
+  const int rep = a.Hq / a.Hkv;
+  const int hc = order_chunk(a.Hkv, rep) * rep;
   prof_begin(PG_KERNEL_ATTN_FWD, a.stream);
   attn_fwd_sm100_kernel<<<(unsigned)(L->n_tiles[FWD256] * a.Hq), NTHREADS, smem, a.stream>>>(
       tq, tk, tv, static_cast<__nv_bfloat16*>(o), lse, tokens(L), tiles<FwdTile>(L, FWD256),
-      intervals(L), lse2_out, padded_tokens(L), a.Hq, a.Hkv, (int)T, a.scale * kLog2e, wait_ns, a.debug);
+      intervals(L), lse2_out, padded_tokens(L), a.Hq, a.Hkv, (int)T, a.scale * kLog2e, hc,
+      wait_ns, a.debug);
   prof_end(PG_KERNEL_ATTN_FWD, a.stream);
   return cuda_check(cudaGetLastError(), "fwd sm100 launch");
 }
