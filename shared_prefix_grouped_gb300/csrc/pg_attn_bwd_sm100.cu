@@ -1,8 +1,8 @@
 // Grouped-attention backward on the 5th-generation tensor cores (bf16, head_dim 128).
 //
 // Key-major: one CTA owns 128 keys of one group and one key/value head (a BwdTile) and sweeps, in
-// a fixed order, every query head of that KV head and every block of 64 query rows that can see
-// its keys.  For a prefix key block that is the rest of the prefix and then all responses of the
+// a fixed order, every block of 64 query rows that can see its keys and, for each block, every
+// query head of that KV head (the heads innermost, so consecutive steps read neighbouring rows).  For a prefix key block that is the rest of the prefix and then all responses of the
 // group, so the prefix dK / dV -- the sum over the G baseline copies of the shared prefix (Pith
 // review of Prefix Grouper, Appendix A.1 objection: the shared prefix's gradient equals the sum of
 // the copies' gradients) -- is accumulated in TMEM by one CTA in a fixed order: bitwise
@@ -10,8 +10,7 @@
 // buffer (its summation order is not fixed).
 //
 // Per query block (64 rows), with K, V resident in shared memory and Q, dO, the blocks' LSE (log2
-// units), rowsum(dO * O) and visibility entries arriving by TMA in a 3-stage ring (and fetched
-// into L2 two blocks before that):
+// units), rowsum(dO * O) and visibility entries arriving by TMA in a 3-stage ring:
 //   S^T  = K Q^T          M 128 keys x N 64 queries x K 128   (TMEM cols [0, 64))
 //   dP^T = V dO^T         M 128 x N 64 x K 128                 (TMEM cols [64, 128))
 //   P^T  = exp2(S^T * scale * log2 e - LSE_2[q]),  dS^T = P^T * (dP^T - Dsum[q])   (registers,
@@ -20,10 +19,11 @@
 //   dV  += P^T dO         M 128 x N 128 dims x K 64, A = P^T from TMEM  (TMEM cols [256, 384))
 //   dK  += dS^T Q         M 128 x N 128 x K 64, A = dS^T from TMEM      (TMEM cols [384, 512))
 //   dQ^T = K^T dS^T       M 128 dims x N 64 queries x K 128    (TMEM cols [128, 192)),
-//          drained by four warps (one thread per head-dim lane): each
-//          warp stages its 32 head dims of the block, 32 query rows at a time ([32 x 32] fp32),
-//          in its own shared-memory buffer and adds them into the global dQ accumulator with TMA
-//          bulk reduce-adds.
+//          drained by four warps (one thread per head-dim lane): the warps stage the block, 32
+//          query rows at a time, into a shared [32 x 128] fp32 box (each warp its 32 head dims;
+//          two boxes alternate) and one thread adds each box into the global dQ accumulator with
+//          a TMA bulk reduce-add -- one 16 KB operation per half block, which the memory system
+//          takes faster than four 4 KB ones.
 // Two threads issue the MMAs: one the score products S^T / dP^T, the other the gradient products
 // dV, dK (and dQ^T) of each block as soon as its P^T / dS^T are ready, so the next block's scores
 // never queue behind the previous block's gradient waits and the tensor core computes them while
@@ -57,7 +57,6 @@ constexpr int D = 128;
 constexpr int BKV = 128;        // keys per CTA
 constexpr int BQ = 64;          // query rows per block
 constexpr int NSQ = 3;          // Q / dO stages
-constexpr int PREFETCH = 2;     // Q / dO blocks fetched into L2 this far ahead of their load
 constexpr uint32_t KHALF = BKV * 64 * 2;   // 16 KiB: [128 rows][64 cols] bf16
 constexpr uint32_t QHALF = BQ * 64 * 2;    // 8 KiB:  [64 rows][64 cols] bf16
 // With dQ: warps 10..13 drain dQ and warp 14 issues the gradient MMAs (dV, dK, dQ^T).  Without:
@@ -74,7 +73,7 @@ struct BwdSmem {
   uint8_t q[NSQ][2 * QHALF];
   uint8_t dO[NSQ][2 * QHALF];
   uint8_t ds[KHALF];        // dS^T [128 keys][64 queries] bf16, SW128
-  alignas(1024) float dqs[4][BQ / 2][32];   // per drain warp: half its slice of a dQ block
+  alignas(1024) float dqs[2][BQ / 2][D];    // dQ staging: two [32 queries][128 dims] fp32 boxes
   alignas(128) float lse2[NSQ][BQ];
   alignas(128) float dsum[NSQ][BQ];
   alignas(128) int4 tokq[NSQ][BQ];   // per-token {g0, pe, own_lo, pos} of the block's queries
@@ -170,18 +169,10 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int st = it % NSQ;
-      const int h = kh * rep + it / nqt;
-      const int qt = qt0 + (it % nqt) * BQ;
+      const int h = kh * rep + it % rep;
+      const int qt = qt0 + (it / rep) * BQ;
       if (!warp_wait(&sm.qd_empty[st], ((it / NSQ) & 1) ^ 1, wait_ns)) { ok = false; break; }
       if (leader) {
-        const int ip = it + PREFETCH + NSQ;
-        if (ip < n_it) {
-          const int hp = kh * rep + ip / nqt, qp = qt0 + (ip % nqt) * BQ;
-          tma_prefetch_l2_2d(&tq, hp * D, qp);
-          tma_prefetch_l2_2d(&tq, hp * D + 64, qp);
-          tma_prefetch_l2_2d(&tdo, hp * D, qp);
-          tma_prefetch_l2_2d(&tdo, hp * D + 64, qp);
-        }
         mbar_expect_tx(&sm.qd_full[st], 4 * QHALF + 2 * BQ * 4 + BQ * 16);
         tma_load_2d(sm.q[st], &tq, &sm.qd_full[st], h * D, qt);
         tma_load_2d(sm.q[st] + QHALF, &tq, &sm.qd_full[st], h * D + 64, qt);
@@ -251,7 +242,7 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int st = it % NSQ;
-      const int qt = qt0 + (it % nqt) * BQ;
+      const int qt = qt0 + (it / rep) * BQ;
       if (!warp_wait(&sm.s_full, it & 1, wait_ns)) { ok = false; break; }
       if (!warp_wait(&sm.qd_full[st], (it / NSQ) & 1, wait_ns)) { ok = false; break; }
       tc_fence_after();
@@ -441,12 +432,15 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     // ------------------------------------------------------------------ dQ drain ---------
     const int quarter = warp & 3;                  // this warp's 32 head dims (= TMEM lanes)
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-    float (*stage)[32] = sm.dqs[quarter];
+    // One thread issues the reduce-adds of all four warps: a whole [32 x 128] box per half
+    // block (fewer, larger bulk operations than one per warp).
+    const bool issuer = warp == 10 && lane == 0;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
-      const int h = kh * rep + it / nqt;
-      const int qt = qt0 + (it % nqt) * BQ;
-      if (!warp_wait(&sm.dq_full, it & 1, wait_ns)) { ok = false; break; }
+      const int h = kh * rep + it % rep;
+      const int qt = qt0 + (it / rep) * BQ;
+      // The four drain warps leave the loop together, so none waits at a barrier below alone.
+      if (!named_bar_and(1, 128, warp_wait(&sm.dq_full, it & 1, wait_ns))) { ok = false; break; }
       tc_fence_after();
       uint32_t g[64];
       tmem_ld32(t_dq + lane_addr, *reinterpret_cast<uint32_t(*)[32]>(&g[0]));
@@ -456,22 +450,24 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       mbar_arrive(&sm.dq_free);
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        // This warp's previous reduce must have finished reading its staging buffer.
-        if (lane == 0) bulk_wait_group_read0();
-        __syncwarp();
+        float (*box)[D] = sm.dqs[hf];
+        // The reduce that last read this box (the previous block's) must be done with it; the
+        // other box's may still be reading.
+        if (issuer) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        named_bar_sync(1, 128);
 #pragma unroll
         for (int c = 0; c < BQ / 2; ++c)
-          stage[c][lane] = __uint_as_float(g[hf * (BQ / 2) + c]) * scale;
+          box[c][quarter * 32 + lane] = __uint_as_float(g[hf * (BQ / 2) + c]) * scale;
         fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
+        named_bar_sync(1, 128);
+        if (issuer) {
           // Rows past the group receive +0; rows past the tensor are clipped by the TMA unit.
-          tma_reduce_add_2d(&tdq, &stage[0][0], h * D + quarter * 32, qt + hf * (BQ / 2));
+          tma_reduce_add_2d(&tdq, &box[0][0], h * D, qt + hf * (BQ / 2));
           bulk_commit_group();
         }
       }
     }
-    if (lane == 0) bulk_wait_group0();
+    if (issuer) bulk_wait_group0();
     __syncwarp();
     if (!ok) fail(PG_ERR_TIMEOUT);
   }
@@ -509,7 +505,7 @@ pg_status launch_bwd_sm100(const AttnArgs& a, const void* q, const void* k, cons
   const bool with_dq = dq_acc != nullptr;
   memset(&tdq, 0, sizeof(tdq));
   if (st == PG_OK && with_dq)
-    st = make_tmap_2d_b32(&tdq, dq_acc, true, (uint64_t)a.Hq * D, T, (uint64_t)a.Hq * D * 4, 32,
+    st = make_tmap_2d_b32(&tdq, dq_acc, true, (uint64_t)a.Hq * D, T, (uint64_t)a.Hq * D * 4, D,
                           BQ / 2);
   if (st != PG_OK) return st;
   const size_t smem = sizeof(BwdSmem) + 1024;

@@ -133,9 +133,9 @@ attn_dq_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
       mbar_init(&sm.kv_empty[s], 1);
     }
     mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.s_free, 256);
-    mbar_init(&sm.p_full[0], 256);
-    mbar_init(&sm.p_full[1], 256);
+    mbar_init(&sm.s_free, 8);      // softmax warps
+    mbar_init(&sm.p_full[0], 8);
+    mbar_init(&sm.p_full[1], 8);
     mbar_init(&sm.ds_free[0], 1);
     mbar_init(&sm.ds_free[1], 1);
     mbar_init(&sm.dq_done, 1);
@@ -287,7 +287,7 @@ attn_dq_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
         tmem_ld_wait();
         if (c2 == 1) {
           tc_fence_before();
-          mbar_arrive(&sm.s_free);
+          warp_arrive(&sm.s_free);
         }
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
@@ -309,7 +309,7 @@ attn_dq_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
       tmem_st32(t_ds + 64 * b + 32 * half + lane_addr, dw);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&sm.p_full[b]);
+      warp_arrive(&sm.p_full[b]);
     }
     // Epilogue: dQ * scale, rotated back by the row's RoPE angle, in bf16.  This thread owns the
     // pairs (k, k + 64) for k in [32 half, 32 half + 32).

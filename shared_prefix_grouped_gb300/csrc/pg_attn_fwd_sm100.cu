@@ -111,7 +111,7 @@ struct FwdSmem {
   uint64_t q_full;
   uint64_t k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV];
   uint64_t s_full[2];       // S of [query tile] complete
-  uint64_t p_full[2];       // P of [query tile] written (128 softmax threads)
+  uint64_t p_full[2];       // P of [query tile] written (its 4 softmax warps)
   uint64_t pv_done[2];      // the P V product of [query tile] has completed
   uint64_t mma_done;
   uint32_t tmem;
@@ -208,7 +208,7 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.s_full[i], 1);
-      mbar_init(&sm.p_full[i], 128);
+      mbar_init(&sm.p_full[i], 4);   // softmax warps of the tile
       mbar_init(&sm.pv_done[i], 1);
     }
     mbar_init(&sm.mma_done, 1);
@@ -429,7 +429,7 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       ++c;
       if (debug & PG_DEBUG_WITHHOLD_P) continue;   // test hook: never signal P (bounded waits)
       tc_fence_before();
-      mbar_arrive(&sm.p_full[i]);
+      warp_arrive(&sm.p_full[i]);
     }
     // Epilogue: O / l and the natural-log LSE.
     if (active && ok && c > 0 && warp_wait(&sm.pv_done[i], (c - 1) & 1, wait_ns)) {
