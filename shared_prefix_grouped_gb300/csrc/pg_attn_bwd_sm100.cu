@@ -258,19 +258,30 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       const float4* dsv = reinterpret_cast<const float4*>(sm.dsum[st] + c0);
       uint32_t pw[16], dw[16];
       if (full) {
+        // Column pairs through the packed fp32 unit (same roundings as the scalar forms).
+        const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 l = l2v[c4], dd = dsv[c4];
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[4 * c4]), scale_log2, -l.x));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[4 * c4 + 1]), scale_log2, -l.y));
-          const float p2 = fast_exp2(fmaf(__uint_as_float(sr[4 * c4 + 2]), scale_log2, -l.z));
-          const float p3 = fast_exp2(fmaf(__uint_as_float(sr[4 * c4 + 3]), scale_log2, -l.w));
+          float p0, p1, p2, p3, d0, d1, d2, d3;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * c4]), __uint_as_float(sr[4 * c4 + 1])),
+                           sc2, f2_pack(-l.x, -l.y)), p0, p1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * c4 + 2]), __uint_as_float(sr[4 * c4 + 3])),
+                           sc2, f2_pack(-l.z, -l.w)), p2, p3);
+          p0 = fast_exp2(p0);
+          p1 = fast_exp2(p1);
+          p2 = fast_exp2(p2);
+          p3 = fast_exp2(p3);
           pw[2 * c4] = pack_bf16x2(p0, p1);
           pw[2 * c4 + 1] = pack_bf16x2(p2, p3);
-          dw[2 * c4] = pack_bf16x2(p0 * (__uint_as_float(dr[4 * c4]) - dd.x),
-                                   p1 * (__uint_as_float(dr[4 * c4 + 1]) - dd.y));
-          dw[2 * c4 + 1] = pack_bf16x2(p2 * (__uint_as_float(dr[4 * c4 + 2]) - dd.z),
-                                       p3 * (__uint_as_float(dr[4 * c4 + 3]) - dd.w));
+          f2_unpack(f2_mul(f2_pack(p0, p1),
+                           f2_sub(f2_pack(__uint_as_float(dr[4 * c4]), __uint_as_float(dr[4 * c4 + 1])),
+                                  f2_pack(dd.x, dd.y))), d0, d1);
+          f2_unpack(f2_mul(f2_pack(p2, p3),
+                           f2_sub(f2_pack(__uint_as_float(dr[4 * c4 + 2]), __uint_as_float(dr[4 * c4 + 3])),
+                                  f2_pack(dd.z, dd.w))), d2, d3);
+          dw[2 * c4] = pack_bf16x2(d0, d1);
+          dw[2 * c4 + 1] = pack_bf16x2(d2, d3);
         }
       } else {
         const int4* tq4 = sm.tokq[st] + c0;

@@ -134,24 +134,30 @@ __device__ __forceinline__ void load64(uint32_t taddr, uint32_t (&r)[64]) {
 }
 
 // Max of 64 raw scores (columns c0 .. c0 + 63 of the tile); with kMasked, columns outside the
-// visible run [lo, lo + len) count as -inf.
+// visible run [lo, lo + len) count as -inf.  Two columns per three-input max.
 template <bool kMasked>
 __device__ __forceinline__ float max64(const uint32_t (&r)[64], int c0, int lo, int len) {
   float mx = -INFINITY;
 #pragma unroll
-  for (int cc = 0; cc < 64; ++cc) {
-    const float x = __uint_as_float(r[cc]);
-    mx = fmaxf(mx, (!kMasked || (unsigned)(c0 + cc - lo) < (unsigned)len) ? x : -INFINITY);
+  for (int cc = 0; cc < 64; cc += 2) {
+    float x0 = __uint_as_float(r[cc]), x1 = __uint_as_float(r[cc + 1]);
+    if (kMasked) {
+      x0 = (unsigned)(c0 + cc - lo) < (unsigned)len ? x0 : -INFINITY;
+      x1 = (unsigned)(c0 + cc + 1 - lo) < (unsigned)len ? x1 : -INFINITY;
+    }
+    mx = fmax3(mx, x0, x1);
   }
   return mx;
 }
 
 // P = exp2(s * scale_log2 - mref) of 64 columns (c0 ..), rounded to bf16 and stored to TMEM
-// columns [p_addr, p_addr + 32); returns the sum of the fp32 values.
+// columns [p_addr, p_addr + 32); returns the sum of the fp32 values (even and odd columns summed
+// separately, then added).  The scale-and-shift and the sums run on column pairs.
 template <bool kMasked>
 __device__ __forceinline__ float exp64(const uint32_t (&r)[64], int c0, int lo, int len,
                                        float scale_log2, float mref, uint32_t p_addr) {
-  float sum0 = 0.f, sum1 = 0.f;
+  const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(-mref, -mref);
+  uint64_t sum2 = f2_pack(0.f, 0.f);
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     uint32_t pw[16];
@@ -163,15 +169,18 @@ __device__ __forceinline__ float exp64(const uint32_t (&r)[64], int c0, int lo, 
         x0 = (unsigned)(c0 + cc - lo) < (unsigned)len ? x0 : -INFINITY;
         x1 = (unsigned)(c0 + cc + 1 - lo) < (unsigned)len ? x1 : -INFINITY;
       }
-      const float p0 = fast_exp2(fmaf(x0, scale_log2, -mref));
-      const float p1 = fast_exp2(fmaf(x1, scale_log2, -mref));
-      sum0 += p0;
-      sum1 += p1;
+      float a0, a1;
+      f2_unpack(f2_fma(f2_pack(x0, x1), sc2, nm2), a0, a1);
+      const float p0 = fast_exp2(a0);
+      const float p1 = fast_exp2(a1);
+      sum2 = f2_add(sum2, f2_pack(p0, p1));
       pw[e] = pack_bf16x2(p0, p1);
     }
     tmem_st16(p_addr + 16 * h, pw);
   }
-  return sum0 + sum1;
+  float s0, s1;
+  f2_unpack(sum2, s0, s1);
+  return s0 + s1;
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
