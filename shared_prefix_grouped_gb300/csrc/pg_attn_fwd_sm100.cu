@@ -183,6 +183,35 @@ __device__ __forceinline__ float exp64(const uint32_t (&r)[64], int c0, int lo, 
   return s0 + s1;
 }
 
+// As exp64 with the running reference, but P stays in registers (pw) and the raw max of the
+// visible columns is folded into mx: the steady-state pass, whose P is stored only if no row's
+// max has grown past the rescale threshold.
+template <bool kMasked>
+__device__ __forceinline__ float exp64_keep(const uint32_t (&r)[64], int c0, int lo, int len,
+                                            float scale_log2, float mref, uint32_t (&pw)[32],
+                                            float& mx) {
+  const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(-mref, -mref);
+  uint64_t sum2 = f2_pack(0.f, 0.f);
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    float x0 = __uint_as_float(r[2 * e]), x1 = __uint_as_float(r[2 * e + 1]);
+    if (kMasked) {
+      x0 = (unsigned)(c0 + 2 * e - lo) < (unsigned)len ? x0 : -INFINITY;
+      x1 = (unsigned)(c0 + 2 * e + 1 - lo) < (unsigned)len ? x1 : -INFINITY;
+    }
+    mx = fmax3(mx, x0, x1);
+    float a0, a1;
+    f2_unpack(f2_fma(f2_pack(x0, x1), sc2, nm2), a0, a1);
+    const float p0 = fast_exp2(a0);
+    const float p1 = fast_exp2(a1);
+    sum2 = f2_add(sum2, f2_pack(p0, p1));
+    pw[e] = pack_bf16x2(p0, p1);
+  }
+  float s0, s1;
+  f2_unpack(sum2, s0, s1);
+  return s0 + s1;
+}
+
 __global__ void __launch_bounds__(NTHREADS, 1)
 attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ o,
@@ -389,7 +418,8 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       if (!rel(i, kt)) continue;
       if (!warp_wait(&sm.s_full[i], c & 1, wait_ns)) { ok = false; break; }
       tc_fence_after();
-      // The row is handled 64 columns at a time (64 score registers): the max of columns
+      // The row is handled 64 columns at a time (64 score registers).  Exact path (the first
+      // key tile, or a tile whose max grows past the rescale threshold): the max of columns
       // 64..127 first (values dropped), then columns 0..63 (max, exp2, P), then 64..127 again
       // (exp2, P).  P of columns [32 h, 32 h + 32) goes to TMEM columns [16 h, 16 h + 16), over
       // scores this thread has already read.  Masked columns become -inf, so their P is exactly
@@ -400,40 +430,67 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       const int lo = (j < n_a) ? 0 : max(ti.z - kt, 0);
       const int len = max(min(hi, rowc + 1) - kt - lo, 0);
       uint32_t sr[64];
-      load64(t_s + 64, sr);
-      float mx = full_tile ? max64<false>(sr, 64, lo, len) : max64<true>(sr, 64, lo, len);
-      load64(t_s, sr);
-      mx = fmaxf(mx, full_tile ? max64<false>(sr, 0, lo, len) : max64<true>(sr, 0, lo, len));
-      const float m_new = fmaxf(m_used, mx * scale_log2);
-      const bool rescale = m_new > m_used + kRescaleThreshold;   // false when m_new is -inf
-      float corr = 1.f;
-      if (rescale) {
-        corr = (m_used == -INFINITY) ? 0.f : fast_exp2(m_used - m_new);
-        m_used = m_new;
-        l *= corr;
-      }
-      const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-      // Rescaling O needs the previous key tile's P V product done (it is: its S completed after
-      // it, and a commit covers every earlier product; the wait returns at once).
-      const bool any_rescale = __any_sync(0xffffffffu, rescale) && c > 0;
-      if (any_rescale) {
-        if (!warp_wait(&sm.pv_done[i], (c - 1) & 1, wait_ns)) { ok = false; break; }
-        tc_fence_after();
-#pragma unroll 1
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t orr[32];
-          tmem_ld32(t_o + q4 * 32, orr);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * corr);
-          tmem_st32(t_o + q4 * 32, orr);
+      bool stored = false;
+      if (c > 0) {
+        // Steady state: both halves straight to P with the running reference, the tile's max
+        // tracked on the way; P is stored only if no row of the warp needs a rescale (then the
+        // values are exactly those of the path below, which S, still intact, is rerun through).
+        uint32_t pa[32], pb[32];
+        float mxk = -INFINITY;
+        const float mref0 = (m_used == -INFINITY) ? 0.f : m_used;
+        load64(t_s, sr);
+        const float sa = full_tile ? exp64_keep<false>(sr, 0, lo, len, scale_log2, mref0, pa, mxk)
+                                   : exp64_keep<true>(sr, 0, lo, len, scale_log2, mref0, pa, mxk);
+        load64(t_s + 64, sr);
+        const float sb = full_tile ? exp64_keep<false>(sr, 64, lo, len, scale_log2, mref0, pb, mxk)
+                                   : exp64_keep<true>(sr, 64, lo, len, scale_log2, mref0, pb, mxk);
+        const bool grow = fmaxf(m_used, mxk * scale_log2) > m_used + kRescaleThreshold;
+        if (!__any_sync(0xffffffffu, grow)) {
+          tmem_st16(t_s, pa);
+          tmem_st16(t_s + 16, pa + 16);
+          tmem_st16(t_s + 32, pb);
+          tmem_st16(t_s + 48, pb + 16);
+          l += sa;
+          l += sb;
+          stored = true;
         }
       }
-      l += full_tile ? exp64<false>(sr, 0, lo, len, scale_log2, mref, t_s)
-                     : exp64<true>(sr, 0, lo, len, scale_log2, mref, t_s);
-      load64(t_s + 64, sr);
-      l += full_tile ? exp64<false>(sr, 64, lo, len, scale_log2, mref, t_s + 32)
-                     : exp64<true>(sr, 64, lo, len, scale_log2, mref, t_s + 32);
+      if (!stored) {
+        load64(t_s + 64, sr);
+        float mx = full_tile ? max64<false>(sr, 64, lo, len) : max64<true>(sr, 64, lo, len);
+        load64(t_s, sr);
+        mx = fmaxf(mx, full_tile ? max64<false>(sr, 0, lo, len) : max64<true>(sr, 0, lo, len));
+        const float m_new = fmaxf(m_used, mx * scale_log2);
+        const bool rescale = m_new > m_used + kRescaleThreshold;   // false when m_new is -inf
+        float corr = 1.f;
+        if (rescale) {
+          corr = (m_used == -INFINITY) ? 0.f : fast_exp2(m_used - m_new);
+          m_used = m_new;
+          l *= corr;
+        }
+        const float mref = (m_used == -INFINITY) ? 0.f : m_used;
+        // Rescaling O needs the previous key tile's P V product done (it is: its S completed after
+        // it, and a commit covers every earlier product; the wait returns at once).
+        const bool any_rescale = __any_sync(0xffffffffu, rescale) && c > 0;
+        if (any_rescale) {
+          if (!warp_wait(&sm.pv_done[i], (c - 1) & 1, wait_ns)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll 1
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t orr[32];
+            tmem_ld32(t_o + q4 * 32, orr);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * corr);
+            tmem_st32(t_o + q4 * 32, orr);
+          }
+        }
+        l += full_tile ? exp64<false>(sr, 0, lo, len, scale_log2, mref, t_s)
+                       : exp64<true>(sr, 0, lo, len, scale_log2, mref, t_s);
+        load64(t_s + 64, sr);
+        l += full_tile ? exp64<false>(sr, 64, lo, len, scale_log2, mref, t_s + 32)
+                       : exp64<true>(sr, 64, lo, len, scale_log2, mref, t_s + 32);
+      }
       tmem_st_wait();
       ++c;
       if (debug & PG_DEBUG_WITHHOLD_P) continue;   // test hook: never signal P (bounded waits)
