@@ -796,6 +796,84 @@ def run_layer_bench(args):
         print(json.dumps(line))
 
 
+# The decoder layer's GEMM shapes (tokens x out x in, B MN-major where the layer stores the weight
+# that way), and a smaller gate/up case that a full ncu capture can hold.
+GEMM_WORKLOADS = {
+    "gemm_bf16_qkv_m32768_n6144_k4096": (32768, 6144, 4096, False),
+    "gemm_bf16_gate_up_m32768_n28672_k4096": (32768, 28672, 4096, False),
+    "gemm_bf16_down_m32768_n4096_k14336": (32768, 4096, 14336, False),
+    "gemm_bf16_gate_up_m8192_n28672_k4096": (8192, 28672, 4096, False),
+}
+
+GEMM_METRIC = "bf16 tensor-core GEMM TFLOP/s (decoder-layer projection shapes, 1 GB300)"
+
+
+def run_gemm_bench(args):
+    """One of the decoder layer's projection GEMMs, C = A B^T in bf16 through pg_gemm_bf16."""
+    world, rank, local = dist_setup()
+    device = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(device)
+    M, N, K, b_mn = GEMM_WORKLOADS[args.workload]
+    gen = torch.Generator().manual_seed(1007 + rank)
+    a = (torch.randn((M, K), generator=gen) * 0.5).to(torch.bfloat16).to(device)
+    b = (torch.randn((K, N) if b_mn else (N, K), generator=gen) * 0.02).to(torch.bfloat16).to(device)
+    c = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+    in_bytes = (a.numel() + b.numel()) * 2
+    flush = None if in_bytes > L2_BYTES else torch.empty(2 * L2_BYTES, dtype=torch.uint8,
+                                                         device=device)
+
+    def call():
+        if flush is not None:
+            flush.zero_()
+        api.gemm_bf16(a, b, b_mn=b_mn, out_dtype=torch.bfloat16, out=c)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(device)
+    L = _lib.lib()
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    kev = [(mk(), mk()) for _ in range(args.steps)]
+    for e0, e1 in kev:
+        e0.record()
+        e1.record()
+    prof = _lib.PgProfile(_lib.PG_KERNEL_GEMM, 0, None, None, 0)
+    sampler = ClockSampler(device.index)
+    sampler.start()
+    barrier(world, device)
+    start, end = mk(), mk()
+    start.record()
+    L.pg_set_profile(prof)
+    for i in range(args.steps):
+        prof.ev_begin, prof.ev_end = kev[i][0].cuda_event, kev[i][1].cuda_event
+        call()
+    L.pg_set_profile(None)
+    end.record()
+    barrier(world, device)
+    clocks = sampler.stop()
+    assert api.device_status() == 0, "a kernel reported an error"
+    sec = start.elapsed_time(end) / 1e3 / args.steps
+    sec = max_over_ranks(sec, world, device)
+    ksec = sum(e0.elapsed_time(e1) for e0, e1 in kev) / 1e3 / args.steps
+    fl = 2.0 * M * N * K
+    peaks, peak_src = load_peaks()
+    peak = peaks["bf16_tflops"]
+    line = {"metric": GEMM_METRIC, "value": fl * world / sec / 1e12, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights)",
+            "config": {"workload": args.workload, "M": M, "N": N, "K": K, "b_mn_major": b_mn,
+                       "out": "bf16", "l2": "inputs larger than L2" if flush is None else
+                       "L2 flushed before every call"},
+            "pct_bf16_peak": 100.0 * fl / sec / 1e12 / peak, "peak_source": peak_src,
+            "roofline": {"bound": "tensor", "kernel": "pg_gemm_bf16 (tcgen05, 128x256 tiles)",
+                         "achieved": fl / ksec / 1e12, "peak": peak, "unit": "TFLOP/s",
+                         "frac": fl / ksec / 1e12 / peak, "traffic": None,
+                         "peak_source": f"bf16 dense burst, {peak_src}"},
+            "clocks": clocks, "gpu_launches": int(prof.launches)}
+    if rank == 0:
+        print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -804,7 +882,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=[w.name for w in workloads.WORKLOADS] + [workloads.LayerWorkload().name]
-                    + [w.name for w in workloads.TREE_WORKLOADS])
+                    + [w.name for w in workloads.TREE_WORKLOADS] + list(GEMM_WORKLOADS))
     ap.add_argument("--simt", action="store_true", help="force the fp32 SIMT kernels")
     ap.add_argument("--deterministic", action="store_true",
                     help="bitwise-reproducible backward (query-major dQ kernel)")
@@ -817,6 +895,8 @@ def main():
         run_reference(args)
     elif args.workload == workloads.LayerWorkload().name:
         run_layer_bench(args)
+    elif args.workload in GEMM_WORKLOADS:
+        run_gemm_bench(args)
     elif args.workload in [w.name for w in workloads.TREE_WORKLOADS]:
         run_tree_bench(args)
     elif workloads.by_name(args.workload).responses_only:
