@@ -40,8 +40,8 @@ L2_BYTES = 129 * 2 ** 20
 # this kernel on this workload.  Reported only while the kernel source still has the hash it had
 # when the counters were taken, and only for that workload.
 TRAFFIC = {"file": "shared_prefix_grouped_gb300/csrc/pg_attn_bwd_sm100.cu",
-           "sha256": "0380c77e89292ef83272bae39b180f2a64d44fd5bd91ad0a162cf2706e5cea6f",
-           "workload": "bf16_gqa32x8_d128_p16384_g16_r256-1024", "bytes": 2995614000}
+           "sha256": "dae3c22facdcd0adef468ca3a9535c2519aece4168f3e01386f689d893cf46bc",
+           "workload": "bf16_gqa32x8_d128_p16384_g16_r256-1024", "bytes": 3043422000}
 
 
 def key_major_flops(pairs: int, w, deterministic: bool) -> float:
