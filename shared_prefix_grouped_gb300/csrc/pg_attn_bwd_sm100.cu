@@ -2,7 +2,8 @@
 //
 // Key-major: one CTA owns 128 keys of one group and one key/value head (a BwdTile) and sweeps, in
 // a fixed order, every block of 64 query rows that can see its keys and, for each block, every
-// query head of that KV head (the heads innermost, so consecutive steps read neighbouring rows).  For a prefix key block that is the rest of the prefix and then all responses of the
+// query head of that KV head (the heads innermost, so consecutive steps read neighbouring rows).
+// For a prefix key block that is the rest of the prefix and then all responses of the
 // group, so the prefix dK / dV -- the sum over the G baseline copies of the shared prefix (Pith
 // review of Prefix Grouper, Appendix A.1 objection: the shared prefix's gradient equals the sum of
 // the copies' gradients) -- is accumulated in TMEM by one CTA in a fixed order: bitwise
@@ -28,9 +29,9 @@
 // dV, dK (and dQ^T) of each block as soon as its P^T / dS^T are ready, so the next block's scores
 // never queue behind the previous block's gradient waits and the tensor core computes them while
 // the softmax warps work on the current ones.
-// The epilogue applies the softmax scale and the inverse RoPE rotation to dK in registers (a
-// thread holds a whole key row, so each (k, k + d/2) pair is local; cos/sin come from the table
-// the RoPE pass of the same call wrote) and writes dK, dV in bf16.
+// The epilogue stages dV (bf16) and scale * dK (fp32) row by row in the freed Q / dO rings, then
+// each warp writes whole rows: dK rotated back by the inverse RoPE angle (the pair (k, k + d/2)
+// of one row; cos/sin from the table the RoPE pass of the same call wrote), coalesced stores.
 //
 // Warps: 0 TMA producer, 1 TMEM allocation and the score MMAs, 2..9 softmax (key rows; two
 // warpgroups split the 64 query columns), 10..13 dQ drain, 14 the gradient MMAs.  Every mbarrier
@@ -324,67 +325,89 @@ attn_bwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       tc_fence_before();
       mbar_arrive(&sm.p_full);
     }
-    // Epilogue of this thread's key row: warps 2..5 write dV, warps 6..9 write scale * dK,
-    // rotated back by the key's RoPE angle (columns c and c + 64 form a rotation pair).
-    if (ok && warp_wait(&sm.pds_free, (n_it - 1) & 1, wait_ns)) {
+    // Epilogue, through shared memory (the Q / dO rings, 96 KB, are free once every product has
+    // completed): each thread stages its key row -- dV rounded to bf16 (256-byte rows), scale * dK
+    // in fp32 (512-byte rows), 16-byte chunks XOR-swizzled by the row so the staging stores are
+    // conflict-free -- then each warp writes whole rows, so the global stores and the RoPE table
+    // reads are coalesced instead of every warp access touching 32 rows.  dK is rotated back by
+    // the key's RoPE angle on the way out: columns p and p + 64 form rotation pair p, and lane l
+    // of a warp handles pairs 2l and 2l + 1 of a row.  The warp's 16 rows of (cos, sin) are read
+    // into registers before the wait for the last products, so their L2 round trip (long under
+    // the dQ reduce traffic of the other CTAs) overlaps it and the staging.  The eight warps
+    // decide together, so none waits at the staging barrier alone.
+    const int wl = warp - 2;                    // rows 16 wl .. 16 wl + 15 in the copy-out
+    const int nrows = tl.k1 - tl.k0;
+    float4 cs[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int row = wl * 16 + i;
+      cs[i] = (rope_tab && row < nrows)
+                  ? *reinterpret_cast<const float4*>(rope_tab + (size_t)(tl.k0 + row) * (D / 2) +
+                                                     2 * lane)
+                  : make_float4(1.f, 0.f, 1.f, 0.f);
+    }
+    if (named_bar_and(2, 256, ok && warp_wait(&sm.pds_free, (n_it - 1) & 1, wait_ns))) {
       tc_fence_after();
-      const size_t off = ((size_t)keyc * Hkv + kh) * D;
+      uint8_t* dks = sm.q[0];                   // [128][128] fp32
+      uint8_t* dvs = sm.q[0] + BKV * D * 4;     // [128][128] bf16
       if (half == 0) {
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t v32[32];
           tmem_ld32(t_dv + lane_addr + c * 32, v32);
           tmem_ld_wait();
-          if (kvalid) {
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(v32[i]), __uint_as_float(v32[i + 1]));
-              w.y = pack_bf16x2(__uint_as_float(v32[i + 2]), __uint_as_float(v32[i + 3]));
-              w.z = pack_bf16x2(__uint_as_float(v32[i + 4]), __uint_as_float(v32[i + 5]));
-              w.w = pack_bf16x2(__uint_as_float(v32[i + 6]), __uint_as_float(v32[i + 7]));
-              *reinterpret_cast<uint4*>(dv + off + c * 32 + i) = w;
-            }
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t* e = v32 + 8 * k;
+            *reinterpret_cast<uint4*>(dvs + stage_offset(r, c * 4 + k, 256)) = make_uint4(
+                pack_bf16x2(__uint_as_float(e[0]), __uint_as_float(e[1])),
+                pack_bf16x2(__uint_as_float(e[2]), __uint_as_float(e[3])),
+                pack_bf16x2(__uint_as_float(e[4]), __uint_as_float(e[5])),
+                pack_bf16x2(__uint_as_float(e[6]), __uint_as_float(e[7])));
           }
         }
       } else {
-        const float2* cs = rope_tab ? rope_tab + (size_t)keyc * (D / 2) : nullptr;
 #pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          uint32_t a32[32], b32[32];
+        for (int c = 0; c < 4; ++c) {
+          uint32_t a32[32];
           tmem_ld32(t_dk + lane_addr + c * 32, a32);
-          tmem_ld32(t_dk + lane_addr + 64 + c * 32, b32);
           tmem_ld_wait();
-          float lo[32], hi[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float x1 = __uint_as_float(a32[i]) * scale;
-            const float x2 = __uint_as_float(b32[i]) * scale;
-            if (cs) {
-              const float2 e = cs[c * 32 + i];   // (cos, sin)
-              lo[i] = x1 * e.x + x2 * e.y;
-              hi[i] = x2 * e.x - x1 * e.y;
-            } else {
-              lo[i] = x1;
-              hi[i] = x2;
-            }
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t* e = a32 + 4 * k;
+            *reinterpret_cast<float4*>(dks + stage_offset(r, c * 8 + k, 512)) =
+                make_float4(__uint_as_float(e[0]) * scale, __uint_as_float(e[1]) * scale,
+                            __uint_as_float(e[2]) * scale, __uint_as_float(e[3]) * scale);
           }
-          if (kvalid) {
+        }
+      }
+      named_bar_sync(2, 256);
+#pragma unroll 4
+      for (int i = 0; i < 8; ++i) {             // dV: two rows per access, 16 lanes x 16 B each
+        const int row = wl * 16 + 2 * i + (lane >> 4), ch = lane & 15;
+        if (row < nrows)
+          *reinterpret_cast<uint4*>(dv + ((size_t)(tl.k0 + row) * Hkv + kh) * D + ch * 8) =
+              *reinterpret_cast<const uint4*>(dvs + stage_offset(row, ch, 256));
+      }
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              uint4 w;
-              w.x = pack_bf16x2(lo[i], lo[i + 1]);
-              w.y = pack_bf16x2(lo[i + 2], lo[i + 3]);
-              w.z = pack_bf16x2(lo[i + 4], lo[i + 5]);
-              w.w = pack_bf16x2(lo[i + 6], lo[i + 7]);
-              *reinterpret_cast<uint4*>(dk + off + c * 32 + i) = w;
-              w.x = pack_bf16x2(hi[i], hi[i + 1]);
-              w.y = pack_bf16x2(hi[i + 2], hi[i + 3]);
-              w.z = pack_bf16x2(hi[i + 4], hi[i + 5]);
-              w.w = pack_bf16x2(hi[i + 6], hi[i + 7]);
-              *reinterpret_cast<uint4*>(dk + off + 64 + c * 32 + i) = w;
-            }
+      for (int i = 0; i < 16; ++i) {            // dK: one row per access
+        const int row = wl * 16 + i;
+        if (row < nrows) {
+          const float2 x1 = *reinterpret_cast<const float2*>(
+              dks + stage_offset(row, lane >> 1, 512) + (lane & 1) * 8);
+          const float2 x2 = *reinterpret_cast<const float2*>(
+              dks + stage_offset(row, 16 + (lane >> 1), 512) + (lane & 1) * 8);
+          float lo0 = x1.x, lo1 = x1.y, hi0 = x2.x, hi1 = x2.y;
+          if (rope_tab) {
+            const float4 e = cs[i];             // (cos, sin) of pairs 2l and 2l + 1
+            lo0 = x1.x * e.x + x2.x * e.y;
+            hi0 = x2.x * e.x - x1.x * e.y;
+            lo1 = x1.y * e.z + x2.y * e.w;
+            hi1 = x2.y * e.z - x1.y * e.w;
           }
+          __nv_bfloat16* drow = dk + ((size_t)(tl.k0 + row) * Hkv + kh) * D;
+          *reinterpret_cast<uint32_t*>(drow + 2 * lane) = pack_bf16x2(lo0, lo1);
+          *reinterpret_cast<uint32_t*>(drow + 64 + 2 * lane) = pack_bf16x2(hi0, hi1);
         }
       }
     } else {

@@ -497,27 +497,40 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       tc_fence_before();
       warp_arrive(&sm.p_full[i]);
     }
-    // Epilogue: O / l and the natural-log LSE.
-    if (active && ok && c > 0 && warp_wait(&sm.pv_done[i], (c - 1) & 1, wait_ns)) {
+    // Epilogue: O / l and the natural-log LSE.  O goes out through shared memory: Q_i's buffer is
+    // free (the tile's last score product completed before its last softmax), each thread stages
+    // its row in bf16 (256-byte rows, 16-byte chunks XOR-swizzled by the row), then each warp
+    // writes two whole rows per access, so the global stores are coalesced instead of every warp
+    // access touching 32 rows.  The tile's four warps decide together (whatever each one's count
+    // of key tiles when a wait gave up), so none waits at the staging barrier alone.
+    const bool go = active && named_bar_and(2 + i, 128, ok && c > 0 &&
+                                                  warp_wait(&sm.pv_done[i], (c - 1) & 1, wait_ns));
+    if (go) {
       tc_fence_after();
       const float inv = 1.f / l;
-      __nv_bfloat16* orow = o + ((size_t)rowc * Hq + h) * D;
+      uint8_t* os = sm.q[i];
 #pragma unroll 1
       for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t orr[32];
         tmem_ld32(t_o + q4 * 32, orr);
         tmem_ld_wait();
-        if (valid) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(orr[e]) * inv, __uint_as_float(orr[e + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(orr[e + 2]) * inv, __uint_as_float(orr[e + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(orr[e + 4]) * inv, __uint_as_float(orr[e + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(orr[e + 6]) * inv, __uint_as_float(orr[e + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + q4 * 32 + e) = w;
-          }
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t* e = orr + 8 * k;
+          *reinterpret_cast<uint4*>(os + stage_offset(r, q4 * 4 + k, 256)) = make_uint4(
+              pack_bf16x2(__uint_as_float(e[0]) * inv, __uint_as_float(e[1]) * inv),
+              pack_bf16x2(__uint_as_float(e[2]) * inv, __uint_as_float(e[3]) * inv),
+              pack_bf16x2(__uint_as_float(e[4]) * inv, __uint_as_float(e[5]) * inv),
+              pack_bf16x2(__uint_as_float(e[6]) * inv, __uint_as_float(e[7]) * inv));
         }
+      }
+      named_bar_sync(2 + i, 128);
+#pragma unroll 4
+      for (int it = 0; it < 16; ++it) {         // rows 32 w .. 32 w + 31 of the tile (w = warp % 4)
+        const int rr = quarter * 32 + 2 * it + (lane >> 4), ch = lane & 15;
+        if (first_row + rr <= qlast)
+          *reinterpret_cast<uint4*>(o + ((size_t)(first_row + rr) * Hq + h) * D + ch * 8) =
+              *reinterpret_cast<const uint4*>(os + stage_offset(rr, ch, 256));
       }
       if (valid) {
         const float lse_row = (m_used + log2f(l)) * kLn2;

@@ -354,6 +354,14 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t
   return row * 128u + ((chunk ^ (row & 7u)) << 4);
 }
 
+// Byte offset of 16-byte chunk `chunk` of row `row` in a staging tile of `row_bytes`-byte rows (a
+// multiple of 128): within each 128-byte segment the chunk index is XOR-ed with the row, so eight
+// consecutive rows' copies of one chunk fall into distinct shared-memory bank groups.
+__host__ __device__ __forceinline__ uint32_t stage_offset(uint32_t row, uint32_t chunk,
+                                                          uint32_t row_bytes) {
+  return row * row_bytes + (((chunk & ~7u) | ((chunk ^ row) & 7u)) << 4);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
