@@ -175,6 +175,44 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ------------------------------------------------------------------- cluster launch control --
+
+// Persistent work claiming that keeps the hardware's launch order: ask the scheduler to cancel a
+// CTA of this grid that has not launched yet and hand its index to this CTA (the grid is launched
+// with one CTA per work item; a CTA that has finished an item takes the next pending one instead
+// of exiting).  One thread; `resp` is a 16-byte shared-memory slot and `bar` an mbarrier of
+// arrival count 1 used only for these responses, `phase` its next phase parity.  Returns the
+// claimed blockIdx.x, -1 when no CTA is left to claim (the caller then stops claiming), or -2 when
+// the response did not arrive within `limit_ns` (a request is then still in flight).
+__device__ __forceinline__ int clc_claim(uint4* resp, uint64_t* bar, uint32_t& phase,
+                                         uint64_t limit_ns) {
+  fence_proxy_async_smem();   // earlier generic reads of the slot come before the async write
+  mbar_expect_tx(bar, 16);
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 "
+      "[%0], [%1];" ::"r"(smem_u32(resp)),
+      "r"(smem_u32(bar))
+      : "memory");
+  if (!mbar_wait(bar, phase, limit_ns)) return -2;
+  phase ^= 1u;
+  uint64_t lo, hi;
+  asm volatile("ld.shared.v2.u64 {%0, %1}, [%2];" : "=l"(lo), "=l"(hi) : "r"(smem_u32(resp)) : "memory");
+  uint32_t canceled;
+  asm volatile(
+      "{\n .reg .b128 h;\n .reg .pred p;\n mov.b128 h, {%1, %2};\n"
+      " clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, h;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(canceled)
+      : "l"(lo), "l"(hi));
+  if (!canceled) return -1;
+  uint32_t x;
+  asm volatile(
+      "{\n .reg .b128 h;\n mov.b128 h, {%1, %2};\n"
+      " clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, h;\n}\n"
+      : "=r"(x)
+      : "l"(lo), "l"(hi));
+  return (int)x;
+}
+
 // ----------------------------------------------------------------------------------- tcgen05 --
 
 // Allocate `ncols` TMEM columns (power of two >= 32); one full warp executes this.  The base
