@@ -17,32 +17,37 @@
 //   * every CTA writes its partial O (fp32, normalised by its own row sum) and its log2-domain LSE;
 //     score_combine_kernel merges the splits by their LSEs.  With nsplit == 1 the CTA writes the
 //     final bf16 O and natural-log LSE itself.
-// Pipeline and warp roles are those of the training forward: warp 0 TMA producer (64-key K/V
-// tiles, 4-stage ring), warp 1 score MMAs (S_i = Q_i K^T, M 128 x N 64 x K 128), warp 10 P V MMAs
-// (P from TMEM), warps 2..9 softmax of query tiles 0 and 1 (one thread per row).  Every mbarrier
-// wait is bounded (PG_ERR_TIMEOUT in the status word, then an orderly exit).
+// Pipeline and warp roles are those of the training forward: 128-key K / V tiles (3-stage K and
+// 2-stage V rings, K one tile ahead), S_i = Q_i K^T (M 128 x N 128 x K 128) in TMEM columns
+// [128 i, 128 i + 128) with P_i written over its first 64 columns, O_i in [256 + 128 i, ...), one
+// MMA-issuing thread (warp 1) whose issue order keeps P_i read before S_i is overwritten, warp 0
+// the TMA producer, warps 2..9 the row softmax of query tiles 0 and 1 (one thread per row).  Every
+// mbarrier wait is bounded (PG_ERR_TIMEOUT in the status word, then an orderly exit).
 #include <math.h>
 
 #include <algorithm>
 
 #include "pg_internal.h"
+#include "pg_rowsoftmax.cuh"
 #include "pg_sm100.cuh"
 #include "pg_tmap.h"
 
 namespace pg {
 
 using namespace sm100;
+using namespace rowsoftmax;
 
 namespace {
 
 constexpr int D = 128;
 constexpr int BM = 128;                      // rows per query tile (two per CTA)
 constexpr int ROWS = 2 * BM;                 // query rows per CTA
-constexpr int BN = 64;                       // keys per K/V tile
-constexpr int NS = 4;                        // K/V pipeline stages
+constexpr int BN = 128;                      // keys per K/V tile
+constexpr int NSK = 3;                       // K pipeline stages
+constexpr int NSV = 2;                       // V pipeline stages
 constexpr uint32_t QH = ROWS * 128;          // one 64-dim half of the 256 query rows: 32 KiB
-constexpr uint32_t KHALF = BN * 64 * 2;      // [64 keys][64 dims] bf16: 8 KiB
-constexpr int NTHREADS = 352;
+constexpr uint32_t KHALF = BN * 64 * 2;      // [128 keys][64 dims] bf16: 16 KiB
+constexpr int NTHREADS = 320;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;
@@ -51,22 +56,18 @@ __device__ int s_status_score = 0;
 
 struct ScoreSmem {
   uint8_t q[2][QH];            // [dim half][256 rows x 128 bytes]
-  uint8_t k[NS][2 * KHALF];
-  uint8_t v[NS][2 * KHALF];
+  uint8_t k[NSK][2 * KHALF];
+  uint8_t v[NSV][2 * KHALF];
   uint64_t q_full;
-  uint64_t k_full[NS], v_full[NS], kv_empty[NS];
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full[2][2];
-  uint64_t pv_done[2][2];
-  uint64_t mma_done, mma_done2;
+  uint64_t k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV];
+  uint64_t s_full[2];          // S of [query tile] complete
+  uint64_t p_full[2];          // P of [query tile] written (its 4 softmax warps)
+  uint64_t pv_done[2];         // the P V product of [query tile] has completed
+  uint64_t mma_done;
   uint32_t tmem;
 };
-
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
+// The 1024-byte alignment slack included, within the 227 KB a CTA may use.
+static_assert(sizeof(ScoreSmem) + 1024 <= 232448, "scoring shared memory");
 
 __device__ __forceinline__ void fail(int code) { atomicCAS(&s_status_score, 0, code); }
 
@@ -158,25 +159,23 @@ attn_score_sm100_kernel(const __grid_constant__ CUtensorMap tq,
       for (int m = threadIdx.x; m < wk.rows; m += NTHREADS) part_lse[slot * ROWS + m] = -INFINITY;
     return;
   }
-  const int nq = wk.last_tok[1] >= 0 ? 2 : 1;
 
   if (threadIdx.x == 0) {
     mbar_init(&sm.q_full, 1);
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < NSK; ++s) {
       mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.k_empty[s], 1);
+    }
+    for (int s = 0; s < NSV; ++s) {
       mbar_init(&sm.v_full[s], 1);
-      mbar_init(&sm.kv_empty[s], 1);
+      mbar_init(&sm.v_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.s_full[i], 1);
-      mbar_init(&sm.s_free[i], 128);
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(&sm.p_full[i][b], 128);
-        mbar_init(&sm.pv_done[i][b], 1);
-      }
+      mbar_init(&sm.p_full[i], 4);   // softmax warps of the tile
+      mbar_init(&sm.pv_done[i], 1);
     }
     mbar_init(&sm.mma_done, 1);
-    mbar_init(&sm.mma_done2, 1);
     fence_mbar_init();
   }
   // Rows past the TMA box (when hp does not divide 256) are zeroed so the MMAs read finite data.
@@ -200,6 +199,8 @@ attn_score_sm100_kernel(const __grid_constant__ CUtensorMap tq,
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer -----
+    // Q once (one 3-D box per 64-dim half), then K tiles into a 3-stage ring and V tiles into a
+    // 2-stage ring, K one tile ahead of V (the score product of a tile precedes its P V product).
     if (elect_one()) {
       prefetch_tmap(&tq);
       prefetch_tmap(&tk);
@@ -208,93 +209,109 @@ attn_score_sm100_kernel(const __grid_constant__ CUtensorMap tq,
       mbar_expect_tx(&sm.q_full, 2 * box_rows * 128);
       tma_load_3d(sm.q[0], &tq, &sm.q_full, 0, wk.kh * hp, wk.t0);
       tma_load_3d(sm.q[1], &tq, &sm.q_full, 64, wk.kh * hp, wk.t0);
-      int issued = 0;
-      for (int j = 0; j < wk.n; ++j) {
-        const int s = j % NS;
-        if (!mbar_wait(&sm.kv_empty[s], ((j / NS) & 1) ^ 1, wait_ns)) {
-          fail(PG_ERR_TIMEOUT);
-          break;
-        }
+      int k_issued = 0, v_issued = 0;
+      auto load_k = [&](int j) -> bool {
+        const int s = j % NSK;
+        if (!mbar_wait(&sm.k_empty[s], ((j / NSK) & 1) ^ 1, wait_ns)) return false;
         int kt, hi;
         wk.get(j, kt, hi);
         mbar_expect_tx(&sm.k_full[s], 2 * KHALF);
         tma_load_2d(sm.k[s], &tk, &sm.k_full[s], xk, kt);
         tma_load_2d(sm.k[s] + KHALF, &tk, &sm.k_full[s], xk + 64, kt);
+        ++k_issued;
+        return true;
+      };
+      auto load_v = [&](int j) -> bool {
+        const int s = j % NSV;
+        if (!mbar_wait(&sm.v_empty[s], ((j / NSV) & 1) ^ 1, wait_ns)) return false;
+        int kt, hi;
+        wk.get(j, kt, hi);
         mbar_expect_tx(&sm.v_full[s], 2 * KHALF);
         tma_load_2d(sm.v[s], &tv, &sm.v_full[s], xk, kt);
         tma_load_2d(sm.v[s] + KHALF, &tv, &sm.v_full[s], xk + 64, kt);
-        ++issued;
+        ++v_issued;
+        return true;
+      };
+      bool ok = load_k(0);
+      for (int j = 0; ok && j < wk.n; ++j) {
+        if (j + 1 < wk.n && !load_k(j + 1)) { ok = false; break; }
+        if (!load_v(j)) { ok = false; break; }
       }
+      if (!ok) fail(PG_ERR_TIMEOUT);
+      // Leave no copy in flight: the last stages' loads must have landed before exit.
       mbar_wait(&sm.q_full, 0, wait_ns);
-      for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j) {
-        mbar_wait(&sm.k_full[j % NS], (j / NS) & 1, wait_ns);
-        mbar_wait(&sm.v_full[j % NS], (j / NS) & 1, wait_ns);
-      }
+      for (int j = (k_issued > NSK ? k_issued - NSK : 0); j < k_issued; ++j)
+        mbar_wait(&sm.k_full[j % NSK], (j / NSK) & 1, wait_ns);
+      for (int j = (v_issued > NSV ? v_issued - NSV : 0); j < v_issued; ++j)
+        mbar_wait(&sm.v_full[j % NSV], (j / NSV) & 1, wait_ns);
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ score MMAs -------
+    // ------------------------------------------------------------------ MMA issuer -------
+    // One thread issues every product, in the order P V of tile 0 (key tile j), S of tile 0
+    // (j + 1), P V of tile 1 (j), S of tile 1 (j + 1): the tensor core executes them in issue
+    // order, so P_i(j), written over S_i's first 64 columns, is read before S_i(j + 1) lands there.
     if (elect_one()) {
       constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
-      int n_s[2] = {0, 0};
-      bool ok = mbar_wait(&sm.q_full, 0, wait_ns);
+      constexpr uint32_t idesc_pv = idesc_bf16(BM, D, 0, 1);
       const uint64_t qd0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
       const uint64_t kd0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
-      for (int j = 0; ok && j < wk.n; ++j) {
-        for (int i = 0; i < nq; ++i) {
-          if (!wk.rel(i, j)) continue;
-          if (!mbar_wait(&sm.k_full[j % NS], (j / NS) & 1, wait_ns)) { ok = false; break; }
-          if (n_s[i] > 0 && !mbar_wait(&sm.s_free[i], (n_s[i] - 1) & 1, wait_ns)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          // Query tile i is rows [128 i, 128 i + 128) of each half.
-          const uint64_t qd = desc_add(qd0, i * BM * 128);
-          const uint64_t kd = desc_add(kd0, (j % NS) * 2 * KHALF);
-          const uint32_t ts = tmem + 64 * i;
+      // V as the MN-major B operand of P V: the two 64-dim halves are LBO apart.
+      const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0]), KHALF, 1024);
+      int n_pv[2] = {0, 0};
+      bool ok = mbar_wait(&sm.q_full, 0, wait_ns);
+      auto wait_k = [&](int j) { return mbar_wait(&sm.k_full[j % NSK], (j / NSK) & 1, wait_ns); };
+      auto wait_v = [&](int j) { return mbar_wait(&sm.v_full[j % NSV], (j / NSV) & 1, wait_ns); };
+      // S_i(j): query tile i (rows [128 i, 128 i + 128) of each Q half) against key tile j.
+      auto issue_s = [&](int i, int j) {
+        tc_fence_after();
+        const uint64_t qd = desc_add(qd0, i * BM * 128);
+        const uint64_t kd = desc_add(kd0, (j % NSK) * 2 * KHALF);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            mma_ss(ts, desc_add(qd, (kk >> 2) * QH + (kk & 3) * 32),
-                   desc_add(kd, (kk >> 2) * KHALF + (kk & 3) * 32), idesc_s, kk != 0);
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + 128 * i, desc_add(qd, (kk >> 2) * QH + (kk & 3) * 32),
+                 desc_add(kd, (kk >> 2) * KHALF + (kk & 3) * 32), idesc_s, kk != 0);
+        mma_commit(&sm.s_full[i]);
+      };
+      // O_i += P_i(j) V_j, P_i read from the first 64 columns of S_i.
+      auto issue_pv = [&](int i, int j) -> bool {
+        if (!mbar_wait(&sm.p_full[i], n_pv[i] & 1, wait_ns)) return false;
+        tc_fence_after();
+        const uint64_t vd = desc_add(vd0, (j % NSV) * 2 * KHALF);
+        const uint32_t acc0 = n_pv[i] != 0;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(tmem + 256 + 128 * i, tmem + 128 * i + kk * 8, desc_add(vd, kk * 2048), idesc_pv,
+                 kk == 0 ? acc0 : 1u);
+        mma_commit(&sm.pv_done[i]);
+        ++n_pv[i];
+        return true;
+      };
+      if (ok) {
+        ok = wait_k(0);
+        for (int i = 0; ok && i < 2; ++i)
+          if (wk.rel(i, 0)) issue_s(i, 0);
+        mma_commit(&sm.k_empty[0]);
+      }
+      for (int j = 0; ok && j < wk.n; ++j) {
+        const bool more = j + 1 < wk.n;
+        if (!wait_v(j)) { ok = false; break; }
+        bool k_ready = !more;
+        for (int i = 0; ok && i < 2; ++i) {
+          if (wk.rel(i, j) && !issue_pv(i, j)) { ok = false; break; }
+          if (more && wk.rel(i, j + 1)) {
+            if (!k_ready && !(k_ready = wait_k(j + 1))) { ok = false; break; }
+            issue_s(i, j + 1);
           }
-          mma_commit(&sm.s_full[i]);
-          ++n_s[i];
         }
+        if (!ok) break;
+        if (!k_ready && !wait_k(j + 1)) { ok = false; break; }
+        mma_commit(&sm.v_empty[j % NSV]);
+        if (more) mma_commit(&sm.k_empty[(j + 1) % NSK]);
       }
       if (!ok) fail(PG_ERR_TIMEOUT);
       mma_commit(&sm.mma_done);
       mbar_wait(&sm.mma_done, 0, wait_ns);
-    }
-    __syncwarp();
-  } else if (warp == 10) {
-    // ------------------------------------------------------------------ P V MMAs ---------
-    if (elect_one()) {
-      constexpr uint32_t idesc_pv = idesc_bf16(BM, D, 0, 1);
-      int n_pv[2] = {0, 0};
-      const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0]), KHALF, 1024);
-      bool ok = true;
-      for (int j = 0; ok && j < wk.n; ++j) {
-        if (!mbar_wait(&sm.v_full[j % NS], (j / NS) & 1, wait_ns)) { ok = false; break; }
-        for (int i = 0; i < nq && ok; ++i) {
-          if (!wk.rel(i, j)) continue;
-          const int b = n_pv[i] & 1;
-          if (!mbar_wait(&sm.p_full[i][b], (n_pv[i] >> 1) & 1, wait_ns)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t pt = tmem + 384 + 64 * i + 32 * b, to = tmem + 128 + 128 * i;
-          const uint64_t vd = desc_add(vd0, (j % NS) * 2 * KHALF);
-          const uint32_t acc0 = n_pv[i] != 0;
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(to, pt + kk * 8, desc_add(vd, kk * 2048), idesc_pv, kk == 0 ? acc0 : 1u);
-          mma_commit(&sm.pv_done[i][b]);
-          ++n_pv[i];
-        }
-        mma_commit(&sm.kv_empty[j % NS]);
-      }
-      if (!ok) fail(PG_ERR_TIMEOUT);
-      mma_commit(&sm.mma_done2);
-      mbar_wait(&sm.mma_done2, 0, wait_ns);
     }
     __syncwarp();
   } else {
@@ -308,116 +325,109 @@ attn_score_sm100_kernel(const __grid_constant__ CUtensorMap tq,
     const int h = wk.kh * hp + m % hp;
     const int own_lo = tok[t].z;
     const bool any_valid = __any_sync(0xffffffffu, valid);
+    // The unmasked path is chosen per warp: its TMEM stores are warp-collective, so every lane of
+    // a warp must take the same path (a warp that mixes padding and real rows takes the masked one).
+    const bool all_valid = __all_sync(0xffffffffu, valid);
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-    const uint32_t t_s = tmem + 64 * i, t_o = tmem + 128 + 128 * i;
+    const uint32_t t_s = tmem + 128 * i + lane_addr, t_o = tmem + 256 + 128 * i + lane_addr;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    int cnt = 0;
+    int c = 0;
     for (int j = 0; active && j < wk.n; ++j) {
       if (!wk.rel(i, j)) continue;
       int kt, hi;
       wk.get(j, kt, hi);
-      if (!warp_wait(&sm.s_full[i], cnt & 1, wait_ns)) { ok = false; break; }
+      if (!warp_wait(&sm.s_full[i], c & 1, wait_ns)) { ok = false; break; }
       if (!any_valid) {
         // Padding rows only (the block has fewer than 256 query rows): keep the barrier protocol
-        // and nothing else.  Their P lanes are never written, so their O rows hold garbage that
-        // is never stored.
-        mbar_arrive(&sm.s_free[i]);
-        mbar_arrive(&sm.p_full[i][cnt & 1]);
-        ++cnt;
+        // and nothing else.  Their S columns go to the P V product as they are, so their O rows
+        // hold garbage that is never stored.
+        ++c;
+        warp_arrive(&sm.p_full[i]);
         continue;
       }
       tc_fence_after();
-      uint32_t sr[64];
-      tmem_ld32(t_s + lane_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(t_s + lane_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&sm.s_free[i]);
-      // Prefix keys are visible to every response row; response keys only from the row's own
-      // response up to the row itself.
+      // Prefix keys are visible to every response row; response keys from the row's own response
+      // start up to the row itself: one contiguous run [lo, lo + len) of the tile's columns
+      // (empty for padding rows).  Row handling as in the training forward: 64 columns at a time;
+      // an exact pass on the first tile and whenever a row's max grows past the rescale threshold,
+      // otherwise one pass straight to P against the running reference.
       const bool prefix = j < wk.n_a;
-      const bool full_tile = prefix && kt + BN <= hi;
-      float mx = -INFINITY;
-      if (full_tile && valid) {
-#pragma unroll
-        for (int cc = 0; cc < BN; ++cc) {
-          const float x = __uint_as_float(sr[cc]) * scale_log2;
-          sr[cc] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
-        }
-      } else {
-        // The row's visible keys in this tile are one contiguous run of columns: up to the split's
-        // end for prefix keys; from the row's own response start up to the row for response keys
-        // (empty for padding rows).  One unsigned compare per column, no branches.
-        const int lo = prefix ? 0 : max(own_lo - kt, 0);
-        const int len = valid ? max(min(hi, prefix ? hi : t + 1) - kt - lo, 0) : 0;
-#pragma unroll
-        for (int cc = 0; cc < BN; ++cc) {
-          const bool vis = (unsigned)(cc - lo) < (unsigned)len;
-          const float x = vis ? __uint_as_float(sr[cc]) * scale_log2 : -INFINITY;
-          sr[cc] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
-        }
-      }
-      const float m_new = fmaxf(m_used, mx);
-      const bool rescale = m_new > m_used + kRescaleThreshold;
-      float corr = 1.f;
-      if (rescale) {
-        corr = (m_used == -INFINITY) ? 0.f : fast_exp2(m_used - m_new);
-        m_used = m_new;
-        l *= corr;
-      }
-      const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-      uint32_t pw[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const float p0 = fast_exp2(__uint_as_float(sr[2 * e]) - mref);
-        const float p1 = fast_exp2(__uint_as_float(sr[2 * e + 1]) - mref);
-        l += p0 + p1;
-        pw[e] = pack_bf16x2(p0, p1);
-      }
-      const int b = cnt & 1;
-      const bool any_rescale = __any_sync(0xffffffffu, rescale) && cnt > 0;
-      if (any_rescale) {
-        if (!warp_wait(&sm.pv_done[i][(cnt - 1) & 1], ((cnt - 1) >> 1) & 1, wait_ns)) {
-          ok = false;
-          break;
+      const bool full_tile = prefix && all_valid && kt + BN <= hi;
+      const int lo = prefix ? 0 : max(own_lo - kt, 0);
+      const int len = valid ? max(min(hi, prefix ? hi : t + 1) - kt - lo, 0) : 0;
+      uint32_t sr[64];
+      bool stored = false;
+      if (c > 0) {
+        uint32_t pa[32], pb[32];
+        float mxk = -INFINITY;
+        const float mref0 = (m_used == -INFINITY) ? 0.f : m_used;
+        load64(t_s, sr);
+        const float sa = full_tile ? exp64_keep<false>(sr, 0, lo, len, scale_log2, mref0, pa, mxk)
+                                   : exp64_keep<true>(sr, 0, lo, len, scale_log2, mref0, pa, mxk);
+        load64(t_s + 64, sr);
+        const float sb = full_tile ? exp64_keep<false>(sr, 64, lo, len, scale_log2, mref0, pb, mxk)
+                                   : exp64_keep<true>(sr, 64, lo, len, scale_log2, mref0, pb, mxk);
+        const bool grow = fmaxf(m_used, mxk * scale_log2) > m_used + kRescaleThreshold;
+        if (!__any_sync(0xffffffffu, grow)) {
+          tmem_st16(t_s, pa);
+          tmem_st16(t_s + 16, pa + 16);
+          tmem_st16(t_s + 32, pb);
+          tmem_st16(t_s + 48, pb + 16);
+          l += sa;
+          l += sb;
+          stored = true;
         }
       }
-      if (cnt >= 2 && !warp_wait(&sm.pv_done[i][b], ((cnt >> 1) - 1) & 1, wait_ns)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (any_rescale) {
+      if (!stored) {
+        load64(t_s + 64, sr);
+        float mx = full_tile ? max64<false>(sr, 64, lo, len) : max64<true>(sr, 64, lo, len);
+        load64(t_s, sr);
+        mx = fmaxf(mx, full_tile ? max64<false>(sr, 0, lo, len) : max64<true>(sr, 0, lo, len));
+        const float m_new = fmaxf(m_used, mx * scale_log2);
+        const bool rescale = m_new > m_used + kRescaleThreshold;   // false when m_new is -inf
+        float corr = 1.f;
+        if (rescale) {
+          corr = (m_used == -INFINITY) ? 0.f : ex2(m_used - m_new);
+          m_used = m_new;
+          l *= corr;
+        }
+        const float mref = (m_used == -INFINITY) ? 0.f : m_used;
+        // Rescaling O needs the previous key tile's P V product done (its S completed after it).
+        const bool any_rescale = __any_sync(0xffffffffu, rescale) && c > 0;
+        if (any_rescale) {
+          if (!warp_wait(&sm.pv_done[i], (c - 1) & 1, wait_ns)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll 1
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t orr[32];
-          tmem_ld32(t_o + lane_addr + q4 * 32, orr);
-          tmem_ld_wait();
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t orr[32];
+            tmem_ld32(t_o + q4 * 32, orr);
+            tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * corr);
-          tmem_st32(t_o + lane_addr + q4 * 32, orr);
+            for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * corr);
+            tmem_st32(t_o + q4 * 32, orr);
+          }
         }
-        tmem_st_wait();
+        l += full_tile ? exp64<false>(sr, 0, lo, len, scale_log2, mref, t_s)
+                       : exp64<true>(sr, 0, lo, len, scale_log2, mref, t_s);
+        load64(t_s + 64, sr);
+        l += full_tile ? exp64<false>(sr, 64, lo, len, scale_log2, mref, t_s + 32)
+                       : exp64<true>(sr, 64, lo, len, scale_log2, mref, t_s + 32);
       }
-      tmem_st32(tmem + 384 + 64 * i + 32 * b + lane_addr, pw);
       tmem_st_wait();
-      ++cnt;
+      ++c;
       tc_fence_before();
-      mbar_arrive(&sm.p_full[i][b]);
+      warp_arrive(&sm.p_full[i]);
     }
     // Epilogue: O / l with the LSE, final (one split) or partial (fp32, log2-domain LSE).
-    if (active && ok && cnt > 0 &&
-        warp_wait(&sm.pv_done[i][(cnt - 1) & 1], ((cnt - 1) >> 1) & 1, wait_ns)) {
+    if (active && ok && c > 0 && warp_wait(&sm.pv_done[i], (c - 1) & 1, wait_ns)) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const float lse2 = l > 0.f ? m_used + log2f(l) : -INFINITY;
 #pragma unroll 1
       for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t orr[32];
-        tmem_ld32(t_o + lane_addr + q4 * 32, orr);
+        tmem_ld32(t_o + q4 * 32, orr);
         tmem_ld_wait();
         if (!valid) continue;
         if (partial) {
@@ -446,7 +456,7 @@ attn_score_sm100_kernel(const __grid_constant__ CUtensorMap tq,
         else
           lse[(size_t)h * Ttot + t] = lse2 * kLn2;
       }
-    } else if (active && cnt > 0) {
+    } else if (active && c > 0) {
       ok = false;
     } else if (valid && partial) {
       part_lse[slot * ROWS + m] = -INFINITY;      // no key tile reached this row in this split
