@@ -12,9 +12,9 @@
 //        bf16 and stored into TMEM cols [384 + 64 b, ...), double-buffered, as the A operand of)
 //   dQ += dS K            M 128 x N 128 dims x K 128 keys, K as the MN-major B operand
 //                                                            (TMEM cols [256, 384))
-// and the epilogue applies the softmax scale and the inverse RoPE rotation (a thread holds a whole
-// query row, so each (k, k + d/2) pair is local; cos/sin from the table the RoPE pass of the same
-// call wrote) and writes dQ in bf16.  Every row's dQ is summed by one CTA over the keys in a fixed
+// and the epilogue applies the softmax scale, stages dQ in the freed Q / dO tiles, and writes it
+// in bf16 by whole rows, rotated back by the inverse RoPE angle (the pair (k, k + d/2) of a row;
+// cos/sin from the table the RoPE pass of the same call wrote).  Every row's dQ is summed by one CTA over the keys in a fixed
 // order: no atomics, bitwise reproducible.
 //
 // Warps (352 threads): 0 TMA producer (Q and dO once, K and V tiles into a 2-stage ring), 1 TMEM
@@ -311,44 +311,61 @@ attn_dq_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
       tc_fence_before();
       warp_arrive(&sm.p_full[b]);
     }
-    // Epilogue: dQ * scale, rotated back by the row's RoPE angle, in bf16.  This thread owns the
-    // pairs (k, k + 64) for k in [32 half, 32 half + 32).
-    if (ok && warp_wait(&sm.dq_done, 0, wait_ns)) {
+    // Epilogue, through shared memory (the Q and dO tiles, 64 KB, are free once every product has
+    // completed): each thread stages scale * dQ of its row's rotation pairs (k, k + 64), k in
+    // [32 half, 32 half + 32), in fp32 (512-byte rows, 16-byte chunks XOR-swizzled by the row so
+    // the staging stores are conflict-free); then each warp writes whole rows, rotated back by the
+    // row's RoPE angle -- lane l handles pairs 2l and 2l + 1 -- so the global stores and the table
+    // reads are coalesced instead of every warp access touching 32 rows.  The warp's 16 rows of
+    // (cos, sin) are read before the wait for the last dQ product, whose L2 round trip they then
+    // overlap.  The eight warps decide together, so none waits at the staging barrier alone.
+    const int wl = warp - 2;                    // rows 16 wl .. 16 wl + 15 in the copy-out
+    const int nrows = tl.q1 - tl.q0;
+    float4 cs[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int rr = wl * 16 + i;
+      cs[i] = (rope_tab && rr < nrows)
+                  ? *reinterpret_cast<const float4*>(rope_tab + (size_t)(tl.q0 + rr) * (D / 2) +
+                                                     2 * lane)
+                  : make_float4(1.f, 0.f, 1.f, 0.f);
+    }
+    if (named_bar_and(2, 256, ok && warp_wait(&sm.dq_done, 0, wait_ns))) {
       tc_fence_after();
-      uint32_t a32[32], b32[32];
-      tmem_ld32(t_dq + lane_addr + 32 * half, a32);
-      tmem_ld32(t_dq + lane_addr + 64 + 32 * half, b32);
-      tmem_ld_wait();
-      if (valid) {
-        const float2* cs = rope_tab ? rope_tab + (size_t)row * (D / 2) + 32 * half : nullptr;
-        float lo_[32], hi_[32];
+      uint8_t* dqs = sm.q;                      // [128][128] fp32 over the Q and dO tiles
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float x1 = __uint_as_float(a32[i]) * scale;
-          const float x2 = __uint_as_float(b32[i]) * scale;
-          if (cs) {
-            const float2 e = cs[i];   // (cos, sin)
-            lo_[i] = x1 * e.x + x2 * e.y;
-            hi_[i] = x2 * e.x - x1 * e.y;
-          } else {
-            lo_[i] = x1;
-            hi_[i] = x2;
-          }
+      for (int part = 0; part < 2; ++part) {    // columns 32 half + 64 part .. + 31
+        uint32_t a32[32];
+        tmem_ld32(t_dq + lane_addr + 64 * part + 32 * half, a32);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t* e = a32 + 4 * k;
+          *reinterpret_cast<float4*>(dqs + stage_offset(r, 16 * part + 8 * half + k, 512)) =
+              make_float4(__uint_as_float(e[0]) * scale, __uint_as_float(e[1]) * scale,
+                          __uint_as_float(e[2]) * scale, __uint_as_float(e[3]) * scale);
         }
-        __nv_bfloat16* out = dq + ((size_t)row * Hq + h) * D + 32 * half;
+      }
+      named_bar_sync(2, 256);
 #pragma unroll
-        for (int i = 0; i < 32; i += 8) {
-          uint4 w;
-          w.x = pack_bf16x2(lo_[i], lo_[i + 1]);
-          w.y = pack_bf16x2(lo_[i + 2], lo_[i + 3]);
-          w.z = pack_bf16x2(lo_[i + 4], lo_[i + 5]);
-          w.w = pack_bf16x2(lo_[i + 6], lo_[i + 7]);
-          *reinterpret_cast<uint4*>(out + i) = w;
-          w.x = pack_bf16x2(hi_[i], hi_[i + 1]);
-          w.y = pack_bf16x2(hi_[i + 2], hi_[i + 3]);
-          w.z = pack_bf16x2(hi_[i + 4], hi_[i + 5]);
-          w.w = pack_bf16x2(hi_[i + 6], hi_[i + 7]);
-          *reinterpret_cast<uint4*>(out + 64 + i) = w;
+      for (int i = 0; i < 16; ++i) {            // one row per access
+        const int rr = wl * 16 + i;
+        if (rr < nrows) {
+          const float2 x1 = *reinterpret_cast<const float2*>(
+              dqs + stage_offset(rr, lane >> 1, 512) + (lane & 1) * 8);
+          const float2 x2 = *reinterpret_cast<const float2*>(
+              dqs + stage_offset(rr, 16 + (lane >> 1), 512) + (lane & 1) * 8);
+          float lo0 = x1.x, lo1 = x1.y, hi0 = x2.x, hi1 = x2.y;
+          if (rope_tab) {
+            const float4 e = cs[i];             // (cos, sin) of pairs 2l and 2l + 1
+            lo0 = x1.x * e.x + x2.x * e.y;
+            hi0 = x2.x * e.x - x1.x * e.y;
+            lo1 = x1.y * e.z + x2.y * e.w;
+            hi1 = x2.y * e.z - x1.y * e.w;
+          }
+          __nv_bfloat16* out = dq + ((size_t)(tl.q0 + rr) * Hq + h) * D;
+          *reinterpret_cast<uint32_t*>(out + 2 * lane) = pack_bf16x2(lo0, lo1);
+          *reinterpret_cast<uint32_t*>(out + 64 + 2 * lane) = pack_bf16x2(hi0, hi1);
         }
       }
     } else {
