@@ -424,6 +424,7 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     const uint32_t t_s = tmem + 128 * i + lane_addr, t_o = tmem + 256 + 128 * i + lane_addr;
     int cs = 0;                                   // S_i products consumed, over all items
+    const bool o_al32 = (reinterpret_cast<uintptr_t>(o) & 31) == 0;
     bool ok = true;
     for (uint32_t kq = 0; ok; ++kq) {
       const int slot = kq & 1;
@@ -543,13 +544,19 @@ attn_fwd_sm100_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
           tmem_ld_wait();
           if (valid) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 8) {
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(orr[e]) * inv, __uint_as_float(orr[e + 1]) * inv);
-              w.y = pack_bf16x2(__uint_as_float(orr[e + 2]) * inv, __uint_as_float(orr[e + 3]) * inv);
-              w.z = pack_bf16x2(__uint_as_float(orr[e + 4]) * inv, __uint_as_float(orr[e + 5]) * inv);
-              w.w = pack_bf16x2(__uint_as_float(orr[e + 6]) * inv, __uint_as_float(orr[e + 7]) * inv);
-              *reinterpret_cast<uint4*>(orow + q4 * 32 + e) = w;
+            for (int e = 0; e < 32; e += 16) {
+              uint32_t w[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                w[u] = pack_bf16x2(__uint_as_float(orr[e + 2 * u]) * inv,
+                                   __uint_as_float(orr[e + 2 * u + 1]) * inv);
+              // 32-byte stores when o is 32-byte aligned (rows are 256 bytes apart), else 16-byte
+              if (o_al32) {
+                st_global_v8(orow + q4 * 32 + e, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+              } else {
+                *reinterpret_cast<uint4*>(orow + q4 * 32 + e) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4*>(orow + q4 * 32 + e + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+              }
             }
           }
         }

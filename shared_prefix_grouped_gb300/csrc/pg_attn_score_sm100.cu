@@ -328,6 +328,8 @@ attn_score_sm100_kernel(const __grid_constant__ CUtensorMap tq,
     // The unmasked path is chosen per warp: its TMEM stores are warp-collective, so every lane of
     // a warp must take the same path (a warp that mixes padding and real rows takes the masked one).
     const bool all_valid = __all_sync(0xffffffffu, valid);
+    const bool o_al32 = (reinterpret_cast<uintptr_t>(o) & 31) == 0;
+    const bool p_al32 = (reinterpret_cast<uintptr_t>(part_o) & 31) == 0;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     const uint32_t t_s = tmem + 128 * i + lane_addr, t_o = tmem + 256 + 128 * i + lane_addr;
     float m_used = -INFINITY, l = 0.f;
@@ -430,23 +432,36 @@ attn_score_sm100_kernel(const __grid_constant__ CUtensorMap tq,
         tmem_ld32(t_o + q4 * 32, orr);
         tmem_ld_wait();
         if (!valid) continue;
+        // 32-byte stores where the buffer is 32-byte aligned (rows are 256 or 512 bytes apart).
         if (partial) {
           float* prow = part_o + (slot * ROWS + m) * D + q4 * 32;
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(prow + e) =
-                make_float4(__uint_as_float(orr[e]) * inv, __uint_as_float(orr[e + 1]) * inv,
-                            __uint_as_float(orr[e + 2]) * inv, __uint_as_float(orr[e + 3]) * inv);
+          for (int e = 0; e < 32; e += 8) {
+            uint32_t w[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) w[u] = __float_as_uint(__uint_as_float(orr[e + u]) * inv);
+            if (p_al32) {
+              st_global_v8(prow + e, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+            } else {
+              *reinterpret_cast<uint4*>(prow + e) = make_uint4(w[0], w[1], w[2], w[3]);
+              *reinterpret_cast<uint4*>(prow + e + 4) = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+          }
         } else {
           __nv_bfloat16* orow = o + ((size_t)t * Hq + h) * D + q4 * 32;
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(orr[e]) * inv, __uint_as_float(orr[e + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(orr[e + 2]) * inv, __uint_as_float(orr[e + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(orr[e + 4]) * inv, __uint_as_float(orr[e + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(orr[e + 6]) * inv, __uint_as_float(orr[e + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + e) = w;
+          for (int e = 0; e < 32; e += 16) {
+            uint32_t w[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              w[u] = pack_bf16x2(__uint_as_float(orr[e + 2 * u]) * inv,
+                                 __uint_as_float(orr[e + 2 * u + 1]) * inv);
+            if (o_al32) {
+              st_global_v8(orow + e, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+            } else {
+              *reinterpret_cast<uint4*>(orow + e) = make_uint4(w[0], w[1], w[2], w[3]);
+              *reinterpret_cast<uint4*>(orow + e + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+            }
           }
         }
       }

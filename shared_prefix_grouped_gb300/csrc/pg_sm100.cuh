@@ -392,6 +392,16 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t
   return row * 128u + ((chunk ^ (row & 7u)) << 4);
 }
 
+// One 32-byte global store (address 32-byte aligned): a warp writing one 32-byte piece of each of
+// 32 rows covers whole 32-byte sectors, with half the instructions of 16-byte stores.
+__device__ __forceinline__ void st_global_v8(void* p, uint32_t a0, uint32_t a1, uint32_t a2,
+                                             uint32_t a3, uint32_t a4, uint32_t a5, uint32_t a6,
+                                             uint32_t a7) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a0),
+               "r"(a1), "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+               : "memory");
+}
+
 // Byte offset of 16-byte chunk `chunk` of row `row` in a staging tile of `row_bytes`-byte rows (a
 // multiple of 128): within each 128-byte segment the chunk index is XOR-ed with the row, so eight
 // consecutive rows' copies of one chunk fall into distinct shared-memory bank groups.

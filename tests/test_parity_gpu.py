@@ -260,3 +260,35 @@ def test_keep_rotated_reuses_the_forward_rotation(path):
     for n in ["o", "lse", "dk", "dv"] + (["dq"] if path != "default" else []):
         assert torch.equal(got[n], ref[n]), n
     compare(prob, got, TOL[w.dtype])
+
+
+@pytest.mark.parametrize("flags", [0, _lib.PG_FLAG_RESPONSES_ONLY])
+def test_outputs_only_16_byte_aligned(flags):
+    # The API takes 16-byte aligned output and workspace pointers; the kernels write o (and the
+    # scoring kernel its split partials in the workspace) with 32-byte stores only where the
+    # buffer is 32-byte aligned.  Buffers 16 bytes off a 32-byte boundary get the same values.
+    w = workloads.small_variant(workloads.WORKLOADS[3], prefix_len=1100, suffix_lens=[70, 1, 129],
+                                heads_q=8, heads_kv=2)
+    prob = workloads.make_problem(w)
+    dev = torch.device("cuda")
+    lay = api.pack(prob.prefix_lens, prob.group_sizes, prob.suffix_lens, dev)
+    q, k, v = (t.to(dev) for t in (prob.q, prob.k, prob.v))
+    n_ws = api.workspace_size(lay, q.dtype, q.shape[1], k.shape[1], q.shape[2],
+                              api.make_opts(w.rope_theta, 0.0, flags), 0)
+    outs = []
+    for shift in (0, 8):                       # elements of bf16: 0 and 16 bytes
+        big = torch.full((q.numel() + 16,), float("nan"), dtype=q.dtype, device=dev)
+        ws_big = torch.empty(n_ws + 64, dtype=torch.uint8, device=dev)
+        assert big.data_ptr() % 32 == 0 and ws_big.data_ptr() % 32 == 0
+        o = big[shift:shift + q.numel()].view(q.shape)
+        ws = ws_big[2 * shift:2 * shift + n_ws]
+        lse = torch.full((q.shape[1], q.shape[0]), float("nan"), device=dev)
+        api.grouped_attn_fwd(lay, q, k, v, rope_theta=w.rope_theta, flags=flags, out=o, lse=lse,
+                             workspace=ws)
+        torch.cuda.synchronize()
+        assert api.device_status() == 0
+        outs.append((o.float().cpu(), lse.cpu()))
+    assert torch.equal(outs[0][0].nan_to_num(), outs[1][0].nan_to_num())
+    assert torch.equal(outs[0][1].nan_to_num(), outs[1][1].nan_to_num())
+    rows = slice(1100, None) if flags else slice(None)
+    assert bool(torch.isfinite(outs[1][0][rows]).all())
