@@ -5,7 +5,7 @@
 // prefix [g0, p_end) -- every response row sees all of it, prefix rows causally -- then the
 // responses' part [s_lo, s_hi) (Pith review of Prefix Grouper, "What carries the argument": prefix
 // self-attention plus suffix attention over the prefix and the row's own response).  Both query
-// tiles share each K/V tile loaded into shared memory, and the CTAs run in chunks of query heads
+// tiles share each K/V tile loaded into shared memory, and the items run in chunks of query heads
 // that share a few key/value heads (the query heads of one KV head side by side on the same query
 // tile), so a group's prefix K/V tiles are read from DRAM about once per chunk and served from L2
 // to every query tile of the group -- the prefix is encoded once, not once per response.
@@ -57,7 +57,7 @@ using namespace rowsoftmax;
 namespace {
 
 constexpr int D = 128;          // head_dim
-constexpr int BM = 128;         // query rows per query tile (two per CTA)
+constexpr int BM = 128;         // query rows per query tile (two per item)
 constexpr int BN = 128;         // keys per tile
 constexpr int NSK = 3;          // K pipeline stages
 constexpr int NSV = 2;          // V pipeline stages
@@ -70,9 +70,9 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 __device__ int s_status_fwd = 0;
 
-// Key tile j of a CTA: the tiles of its causal key ranges (the group's prefix, or a nested
-// prefix's ancestors) first, then of its own range; and which query tiles need it.  Built once per
-// CTA in shared memory.
+// Key tile j of an item: the tiles of its causal key ranges (the group's prefix, or a nested
+// prefix's ancestors) first, then of its own range; and which query tiles need it.  Built by the
+// producer in the item's shared-memory slot.
 struct Plan {
   int n_r, n_a, n;                  // key ranges, key tiles in causal ranges, all key tiles
   int lo[kMaxKeyRanges], hi[kMaxKeyRanges], cum[kMaxKeyRanges + 1];
