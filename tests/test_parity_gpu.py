@@ -292,3 +292,22 @@ def test_outputs_only_16_byte_aligned(flags):
     assert torch.equal(outs[0][1].nan_to_num(), outs[1][1].nan_to_num())
     rows = slice(1100, None) if flags else slice(None)
     assert bool(torch.isfinite(outs[1][0][rows]).all())
+
+
+@pytest.mark.parametrize("path", ["default", "det"])
+def test_many_work_items_all_rows(path):
+    # More forward work items (query-tile pairs x heads) and backward key blocks than the GPU has
+    # SMs, at a size the oracle checks on every row: the forward's CTAs claim pending items
+    # (cluster launch control) and run several each, with items of different lengths (groups of
+    # three prefix lengths), so every row of o / lse and of the gradients comes from a claimed item
+    # as often as from a launched one.
+    plens = [130, 260, 40] * 14
+    gsz = [2, 1, 3] * 14
+    rs = [30, 1, 99, 7, 12, 64] * 14
+    w = workloads.small_variant(workloads.WORKLOADS[2], prefix_len=plens[0], suffix_lens=rs,
+                                heads_q=8, heads_kv=2, num_groups=len(plens))
+    prob = workloads.make_problem(w, prefix_lens=plens, group_sizes=gsz, suffix_lens=rs)
+    dev_lay = api.pack(prob.prefix_lens, prob.group_sizes, prob.suffix_lens, torch.device("cuda"))
+    assert dev_lay.struct.n_tiles[4] * w.heads_q > 2 * 152          # 256-row forward items
+    got = run_gpu(prob, flags=PATH_FLAGS[path])
+    compare(prob, got, TOL[w.dtype])
