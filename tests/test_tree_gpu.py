@@ -55,10 +55,12 @@ TREES = [
     ((-1, 0, 0, 2, 2, 2), (0, 33, 100, 64, 1, 250), 4, 1, "bf16"),
     ((-1, 0, 1, 2, 3, 4, 5, 6), (70, 3, 66, 1, 128, 9, 64, 300), 2, 2, "bf16"),   # depth 8
     ((-1, 0, 1, 1, 0, 4, 4, 4), (96, 40, 20, 33, 17, 1, 60, 25), 2, 2, "f32"),
+    # 32 query heads: more forward items than SMs, so the forward's CTAs claim items
+    (*workloads.multi_turn(700, 3, 130, 3, 90), 32, 8, "bf16"),
 ]
 
 
-@pytest.mark.parametrize("tree", TREES, ids=lambda t: f"n{len(t[0])}_{t[4]}")
+@pytest.mark.parametrize("tree", TREES, ids=lambda t: f"n{len(t[0])}_h{t[2]}_{t[4]}")
 @pytest.mark.parametrize("path", ["default", "det", "simt"])
 def test_tree_matches_path_baseline(tree, path):
     parent, lens, hq, hkv, dtype = tree
